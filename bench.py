@@ -1,0 +1,432 @@
+#!/usr/bin/env python3
+"""Paged decode attention benchmark: one JSON line on rank 0.
+
+A step is one decode iteration of the whole hot path over one batch: the
+copy-on-write block copies (pa_copy_blocks), the new tokens' K/V append
+(pa_reshape_and_cache) and the decode attention (pa_decode: partition kernel +
+split-KV merge kernel), on inputs already resident in HBM.  The workload's
+allocator script (untimed) prepares the caches and tables.
+
+Metric: KV GB/s (algorithmic bytes of the step / device time of the step); the
+line also carries seq*layers/s (one pa_decode call = one layer), the roofline of
+the decode kernel against the measured HBM copy bandwidth, the fp64 CPU oracle's
+throughput on the host cores, and an end-to-end figure through the public API with
+host buffers (pinned host -> device inputs, device -> host output inside the timed
+region).  The L2 (129 MB) is flushed by writing a 512 MB buffer before every timed
+step.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py --impl reference ...     (the fp64 CPU oracle on the host cores)
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+DEFAULT_WORKLOAD = "mha_fp16"
+METRIC = "paged decode attention KV GB/s and % of GB300 HBM peak; seq-layers/s at 1 GPU"
+FALLBACK_HBM_GBS = 6800.0
+DECODE_SOURCES = ["pa_decode.cuh", "pa_device.cuh", "pa_api.cu", "pa_internal.h"]
+
+
+# ----------------------------------------------------------------------------
+# bytes accounting (algorithmic: each byte the step must move, counted once)
+# ----------------------------------------------------------------------------
+def step_bytes(w, bt, cl, n_tok, n_pairs):
+    import numpy as np
+    es = w.elem_bytes
+    row = w.num_kv_heads * w.head_dim * es          # one token's K (or V) row
+    B = w.block_size
+    S = len(cl)
+    logical = int(np.sum(cl)) * row * 2
+    # unique: each referenced physical block once, with its largest valid row count
+    rows_of = {}
+    for s in range(S):
+        T = int(cl[s])
+        nb = (T + B - 1) // B
+        for j in range(nb):
+            b = int(bt[s, j])
+            r = min(B, T - j * B)
+            if rows_of.get(b, 0) < r:
+                rows_of[b] = r
+    unique = sum(rows_of.values()) * row * 2
+    nb_total = int(sum((int(t) + B - 1) // B for t in cl))
+    io = 2 * S * w.num_q_heads * w.head_dim * es + 4 * nb_total + 4 * S
+    decode = unique + io
+    append = n_tok * row * 2 * 2 + 8 * n_tok
+    block_bytes = B * row
+    cow = n_pairs * block_bytes * 2 * 2 + 8 * n_pairs
+    return dict(decode=decode, decode_logical=logical + io, kv_unique=unique, kv_logical=logical,
+                append=append, cow=cow, step=decode + append + cow)
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def decode_source_hash():
+    h = hashlib.sha256()
+    for n in DECODE_SOURCES:
+        with open(os.path.join(ROOT, "paged_kv_cache_79_gb300", "csrc", n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload):
+    """DRAM bytes per decode launch from the committed ncu summary, if it was taken
+    on the current decode sources; else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        e = d.get(workload)
+        if e and e.get("source_hash") == decode_source_hash():
+            return e.get("dram_bytes_per_launch")
+    except Exception:
+        pass
+    return None
+
+
+def raw(t):
+    """Storage bits as numpy (float32 for fp32, uint16 for fp16/bf16)."""
+    import numpy as np
+    import torch
+    t = t.detach().contiguous().cpu()
+    if t.dtype == torch.float32:
+        return t.numpy()
+    return t.view(torch.int16).numpy().view(np.uint16)
+
+
+# ----------------------------------------------------------------------------
+# clocks sampled during the timed region
+# ----------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self._t = threading.Thread(target=self._read, daemon=True)
+            self._t.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self._t.join(timeout=2)
+        sm, mx, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = max(mx, float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------
+# our arm
+# ----------------------------------------------------------------------------
+def prepare(name, device, seed_offset=0):
+    import workloads as W
+    from paged_kv_cache_79_gb300 import runner
+    w = W.by_name(name)
+    if seed_offset:
+        w.data_seed += 97 * seed_offset
+    kc, vc = W.pool_tensors(w, device)
+    alloc, ds = runner.execute(w, kc, vc, lambda ev: W.step_tensors(w, ev, device),
+                               lambda ev: W.query_tensor(w, ev.index, device))
+    bt, cl = runner.tables_for(alloc, w.decode_seqs)
+    return w, ds, bt, cl
+
+
+def cpu_baseline(w, ds, bt, cl, budget_s=10.0):
+    """Time the fp64 oracle (as it stands) on the host cores on a bounded sample:
+    whole decode steps over the sequences' blocks, repeated until ~budget_s."""
+    import numpy as np
+    import torch
+    import oracle
+    B = w.block_size
+    nbs = [(int(t) + B - 1) // B for t in cl]
+    used = sorted({int(bt[s, j]) for s in range(len(cl)) for j in range(nbs[s])})
+    remap = {b: i for i, b in enumerate(used)}
+    idx = torch.tensor(used, dtype=torch.long, device=ds.k_cache.device)
+    kh, vh = raw(ds.k_cache.index_select(0, idx)), raw(ds.v_cache.index_select(0, idx))
+    sbt = np.full(bt.shape, -1, dtype=np.int32)
+    for s in range(len(cl)):
+        sbt[s, :nbs[s]] = [remap[int(b)] for b in bt[s, :nbs[s]]]
+    q = raw(ds.q)
+    # bound the sample: at most ~budget_s of work, at least one full decode step
+    t0 = time.perf_counter()
+    reps = 0
+    while True:
+        oracle.decode(q, kh, vh, sbt, cl, w.softmax_scale, w.dtype, w.num_q_heads, w.num_kv_heads,
+                      w.head_dim, B)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s or reps >= 50:
+            break
+    return reps, el, oracle.num_threads()
+
+
+def run_ours(args):
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    device = f"cuda:{local}"
+
+    from paged_kv_cache_79_gb300 import build as libbuild
+    libbuild.build()
+    w, ds, bt, cl = prepare(args.workload, device, seed_offset=rank)
+    n_tok = int(ds.slots.shape[0])
+    n_pairs = int(ds.pairs.shape[0])
+    by = step_bytes(w, bt, cl, n_tok, n_pairs)
+    S = len(cl)
+    stream = torch.cuda.Stream(device)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=device)
+    import paged_kv_cache_79_gb300 as P
+    parts = P.pa_decode_partition_size(S, w.num_q_heads, w.num_kv_heads, w.head_dim, w.block_size,
+                                       bt.shape[1], w.partition_size)
+    max_parts = -(-bt.shape[1] // (parts // w.block_size))
+    launches_per_step = (1 if n_pairs else 0) + (1 if n_tok else 0) + 1 + (1 if max_parts > 1 else 0)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            ds.run(stream)
+        torch.cuda.synchronize(device)
+        if world > 1:
+            dist.barrier()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+               torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+        clocks = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
+        if clocks:
+            clocks.start()
+            time.sleep(0.3)
+        torch.cuda.synchronize(device)
+        t_wall = time.perf_counter()
+        for i in range(args.steps):
+            flush.zero_()                                   # evict the previous step from L2
+            e0, e1, e2 = ev[i]
+            e0.record(stream)
+            if n_pairs:
+                P.pa_copy_blocks(ds.k_cache, ds.v_cache, ds.pairs, stream)
+            P.pa_reshape_and_cache(ds.step_k, ds.step_v, ds.k_cache, ds.v_cache, ds.slots, stream)
+            e1.record(stream)
+            ds.decode(stream)
+            e2.record(stream)
+        torch.cuda.synchronize(device)
+        wall = time.perf_counter() - t_wall
+        if world > 1:
+            dist.barrier()
+        clk = clocks.stop() if clocks else None
+
+    step_ms = [a.elapsed_time(c) for a, b, c in ev]
+    dec_ms = [b.elapsed_time(c) for a, b, c in ev]
+    t_step = sum(step_ms) / len(step_ms)
+    t_dec = sum(dec_ms) / len(dec_ms)
+    if world > 1:
+        t = torch.tensor([t_step, t_dec], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        t_step, t_dec = t.tolist()
+
+    # end to end through the public API with host buffers
+    e2e = run_e2e(ds, stream, device, args, by)
+
+    if rank != 0:
+        return None
+    value = world * by["step"] / (t_step * 1e-3) / 1e9
+    peak, peak_kind = measured_peak()
+    achieved = by["decode"] / (t_dec * 1e-3) / 1e9
+    line = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(t_step, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": w.dtype,
+        "data": "synthetic (seeded N(0,1) q/K/V; seeded allocator script)",
+        "config": {"workload": w.name, "num_seqs": S, "num_q_heads": w.num_q_heads,
+                   "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim, "block_size": w.block_size,
+                   "num_blocks": w.num_blocks, "context_tokens": int(np.sum(cl)),
+                   "max_context": int(np.max(cl)), "partition_size": parts, "appended_tokens": n_tok,
+                   "cow_pairs": n_pairs, "l2": "flushed (512 MB write) before every timed step",
+                   "parallelism": f"replica x{world} (independent batches)"},
+        "seq_layers_per_s": round(world * S / (t_step * 1e-3), 1),
+        "pct_of_hbm_peak": round(100 * value / world / peak, 2),
+        "decode_ms": round(t_dec, 5),
+        "bytes_per_step": by,
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "peak_kind": f"{peak_kind} copy bandwidth",
+                     "traffic": profiled_traffic(w.name),
+                     "kernel": "pa_decode (partition kernel + split-KV merge)"},
+        "e2e": e2e,
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk,
+        "wall_s_timed_region": round(wall, 4),
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        reps, el, cores = cpu_baseline(w, ds, bt, cl, args.cpu_budget)
+        line["cpu_baseline"] = {"value": round(reps * by["decode"] / el / 1e9, 4), "unit": "GB/s",
+                                "cores": cores, "kind": "oracle",
+                                "sample": f"{reps} full decode steps of this workload ({S} sequences), "
+                                          f"fp64 C oracle, {el:.1f} s"}
+    return line
+
+
+def run_e2e(ds, stream, device, args, by):
+    """Same step through the public API with inputs in pinned host memory: H2D of
+    the step's inputs, the step, D2H of the output -- all inside the timed region."""
+    import torch
+    host = {}
+    for name in ("q", "step_k", "step_v", "slots", "pairs", "block_tables", "context_lens"):
+        t = getattr(ds, name)
+        host[name] = t.cpu().pin_memory()
+    out_h = torch.empty(ds.out.shape, dtype=ds.out.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = out_h.numel() * out_h.element_size()
+    import paged_kv_cache_79_gb300 as P
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=device)
+    times = []
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup + args.steps):
+            flush.zero_()
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for name, t in host.items():
+                getattr(ds, name).copy_(t, non_blocking=True)
+            ds.run(stream)
+            out_h.copy_(ds.out, non_blocking=True)
+            b.record(stream)
+            b.synchronize()
+            if i >= args.warmup:
+                times.append(a.elapsed_time(b))
+    t = sum(times) / len(times)
+    return {"value": round(by["step"] / (t * 1e-3) / 1e9, 2), "unit": "GB/s", "ms_per_step": round(t, 5),
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+
+
+# ----------------------------------------------------------------------------
+# reference arm: the fp64 CPU oracle on the host cores
+# ----------------------------------------------------------------------------
+def run_reference(args):
+    import numpy as np
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return None
+    import oracle
+    import workloads as W
+    w = W.by_name(args.workload)
+    # the oracle executes the workload's script with its own allocator on a host
+    # pool; the pool holds N(0,1) data drawn on the CPU (same recipe, CPU generator)
+    oalloc, _ = oracle.run_script(w.events, w.num_blocks, w.block_size, w.free_order)
+    bt, cl = oracle.tables_for(oalloc, w.decode_seqs)
+    B = w.block_size
+    nbs = [(int(t) + B - 1) // B for t in cl]
+    used = sorted({int(bt[s, j]) for s in range(len(cl)) for j in range(nbs[s])})
+    remap = {b: i for i, b in enumerate(used)}
+    sbt = np.full(bt.shape, -1, dtype=np.int32)
+    for s in range(len(cl)):
+        sbt[s, :nbs[s]] = [remap[int(b)] for b in bt[s, :nbs[s]]]
+    shape = (len(used), B, w.num_kv_heads, w.head_dim)
+    kh = raw(W.randn(shape, w.dtype, w.data_seed * 10 + 1))
+    vh = raw(W.randn(shape, w.dtype, w.data_seed * 10 + 2))
+    q = raw(W.query_tensor(w, 0))
+    by = step_bytes(w, sbt, cl, 0, 0)
+    times = []
+    for i in range(args.warmup + args.steps):
+        t0 = time.perf_counter()
+        oracle.decode(q, kh, vh, sbt, cl, w.softmax_scale, w.dtype, w.num_q_heads, w.num_kv_heads,
+                      w.head_dim, B)
+        if i >= args.warmup:
+            times.append(time.perf_counter() - t0)
+    t = sum(times) / len(times)
+    value = by["decode"] / t / 1e9
+    cores = oracle.num_threads()
+    return {"metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": 0, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(t * 1e3, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "impl": "reference",
+            "config": {"workload": w.name, "num_seqs": len(cl), "context_tokens": int(np.sum(cl))},
+            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+                             "sample": f"one full decode step of {w.name} per timed step (fp64 C oracle)"},
+            "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=10.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    line = run_reference(args) if args.impl == "reference" else run_ours(args)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,240 @@
+/*
+ * pagedkv.h -- C ABI of libpagedkv.so: paged decode attention on GB300 (sm_103a).
+ *
+ * The operations follow three descriptions of PagedAttention:
+ *   [S]  "Efficient Memory Management for Large Language Model Serving with
+ *        PagedAttention" (azimuth.plus summary of Kwon et al., SOSP 2023):
+ *        sections "Core idea", "The PagedAttention algorithm" (block-wise
+ *        attention equation), "vLLM" (block manager), "Memory sharing"
+ *        (copy-on-write), "Inside: block-table lookup".
+ *   [T]  CSDN tutorial "PagedAttention实战": §2.1 Page / PageTable, §2.2
+ *        BlockManager, §3.1 SequenceManager.append_kv, §3.2 PagedAttention.compute,
+ *        §5.1 clone_sequence.
+ *
+ * Conventions shared by every entry point
+ *   - All device buffers are allocated and owned by the caller.  The library never
+ *     allocates device memory and keeps no per-call state between calls.
+ *   - Device work is enqueued asynchronously on `stream` (a cudaStream_t passed as
+ *     an opaque pointer; NULL = the legacy default stream).  Inputs must stay alive
+ *     and unmodified until the stream has executed the call.
+ *   - Arguments are validated on the host before anything is enqueued: a status
+ *     other than PA_OK means nothing was enqueued.  PA_ERR_CUDA reports a failed
+ *     launch (the CUDA error is cleared; pa_last_cuda_error returns it).
+ *   - No entry point aborts, exits or throws.
+ *   - Layouts are dense row-major, all with the innermost dimension contiguous:
+ *       q, out                [num_seqs][num_q_heads][head_dim]
+ *       k_cache, v_cache      [num_blocks][block_size][num_kv_heads][head_dim]
+ *                              ([T] §2.1: a page holds keys/values of shape
+ *                               [page_size, num_heads, head_dim])
+ *       block_tables          int32 [num_seqs][max_blocks_per_seq]; entry j of row s
+ *                             is the physical block of logical block j ([S] "Core
+ *                             idea": the block table maps logical to physical blocks);
+ *                             entries at j >= ceil(context_len / block_size) are not
+ *                             read (pad them with -1, [T] §2.1's unmapped value)
+ *       context_lens          int32 [num_seqs]
+ *       slot_mapping          int64 [num_tokens]: slot = physical_block * block_size
+ *                             + offset ([T] §3.1)
+ *       src_dst_pairs         int32 [num_pairs][2]
+ *   - Device pointers must be 16-byte aligned (PA_ERR_INVALID otherwise).
+ */
+#ifndef PAGEDKV_H
+#define PAGEDKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    PA_OK = 0,
+    PA_ERR_INVALID = 1,      /* bad pointer, shape, alignment or argument       */
+    PA_ERR_UNSUPPORTED = 2,  /* valid but not built (head_dim, block_size, ...)  */
+    PA_ERR_CUDA = 3,         /* a CUDA call or launch failed                     */
+    PA_ERR_OOM = 4,          /* host allocator: no free block ([T] §2.2)         */
+    PA_ERR_TIMEOUT = 5       /* a device-side wait gave up (pa_device_errors)    */
+} pa_status;
+
+typedef enum { PA_F32 = 0, PA_F16 = 1, PA_BF16 = 2 } pa_dtype;
+
+/* Human-readable name of a status; never NULL. */
+const char *pa_status_string(pa_status s);
+
+/* The CUDA error code of the last PA_ERR_CUDA returned on this thread (0 if none). */
+int pa_last_cuda_error(void);
+
+/* ------------------------------------------------------------------------- *
+ * Decode attention.                                                          *
+ * ------------------------------------------------------------------------- */
+
+/*
+ * pa_decode -- single-query attention of every sequence over its paged KV cache.
+ *
+ * Defines ([S] "The PagedAttention algorithm", block-wise attention equation; [T]
+ * §3.2): for sequence s with T = context_lens[s] tokens and query head h,
+ *     kv   = h / (num_q_heads / num_kv_heads)          (contiguous GQA groups)
+ *     K_t  = k_cache[block_tables[s][t / B]][t % B][kv][:]   (same for V_t)
+ *     s_t  = scale * dot(q[s][h], K_t)
+ *     out[s][h] = sum_t exp(s_t - max) V_t / sum_t exp(s_t - max)
+ * computed block by block with per-block maxima and exp-sums merged by the
+ * log-sum-exp rule the equation states.  Only the first T - (nb-1)*B rows of the
+ * last block count; stale rows past T never affect the result.  T = 0 yields a zero
+ * row ([T] §3.2 returns zeros for an empty sequence).  Context lengths are clamped
+ * to [0, max_blocks_per_seq * block_size].
+ *
+ * Long contexts are split into partitions of `partition_size` tokens processed by
+ * separate CTAs; their partial (max, exp-sum, weighted V) results are merged by a
+ * second kernel with the same rule.  partition_size = 0 lets the library choose;
+ * otherwise it must be a positive multiple of block_size.
+ *
+ * Arguments
+ *   out            device, [S][Hq][d], dtype `dtype`, written
+ *   q              device, [S][Hq][d], dtype `dtype`
+ *   k_cache/v_cache device, [num_blocks][B][Hkv][d], dtype `dtype`
+ *   block_tables   device int32 [S][max_blocks_per_seq]; referenced entries must be
+ *                  in [0, num_blocks) (an entry outside reads zeros, never faults)
+ *   context_lens   device int32 [S]
+ *   scale          softmax scale (1/sqrt(head_dim) for the pages' definition)
+ *   head_dim       64 or 128;  block_size 16 or 32;  num_q_heads % num_kv_heads == 0
+ *   workspace      device scratch of at least pa_decode_workspace_size(...) bytes
+ *                  (may be NULL when that size is 0); 16-byte aligned.  Its
+ *                  contents need no initialisation and are not meaningful after.
+ * Errors: PA_ERR_INVALID (null/misaligned pointer, non-positive size, bad
+ *   partition size, workspace too small, q/kv head mismatch, num_blocks*block_size
+ *   >= 2^31), PA_ERR_UNSUPPORTED (head_dim / block_size / dtype not built),
+ *   PA_ERR_CUDA (launch failure).
+ */
+pa_status pa_decode(void *out, const void *q, const void *k_cache, const void *v_cache,
+                    const int32_t *block_tables, int max_blocks_per_seq,
+                    const int32_t *context_lens, int num_seqs, int num_blocks, float scale,
+                    int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                    pa_dtype dtype, int partition_size, void *workspace,
+                    size_t workspace_bytes, void *stream);
+
+/*
+ * Partition size pa_decode uses for these arguments (resolves partition_size = 0
+ * on the current device).  Returns 0 for invalid arguments.
+ */
+int pa_decode_partition_size(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                             int block_size, int max_blocks_per_seq, int partition_size);
+
+/*
+ * Bytes of workspace pa_decode needs for these arguments (0 when every sequence
+ * fits one partition).  Layout: fp32 partial outputs [S][P][Hq][d] followed by
+ * fp32 partial log2-sum-exp values [S][P][Hq], P = ceil(max_blocks_per_seq *
+ * block_size / partition).  Returns (size_t)-1 for invalid arguments.
+ */
+size_t pa_decode_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                                int block_size, int max_blocks_per_seq, int partition_size);
+
+/* ------------------------------------------------------------------------- *
+ * Cache writes.                                                              *
+ * ------------------------------------------------------------------------- */
+
+/*
+ * pa_reshape_and_cache -- write each new token's K and V rows into its slot.
+ *
+ * Defines ([T] §3.1 append_kv: logical page pos // page_size, offset
+ * pos % page_size; [S] "Core idea": blocks fill one token at a time):
+ *     for t in [0, num_tokens): slot = slot_mapping[t];
+ *       k_cache[slot / B][slot % B][:][:] = k[t][:][:]   (and v likewise)
+ * A negative slot skips the token (padding).  A slot >= num_blocks * B is also
+ * skipped: the kernel never writes outside the caches.  Bit-exact copies.
+ *
+ *   k, v           device [num_tokens][num_kv_heads][head_dim], dtype `dtype`
+ *   slot_mapping   device int64 [num_tokens]
+ * Duplicate slots within one call: which token's row lands is unspecified.
+ * Errors: PA_ERR_INVALID, PA_ERR_UNSUPPORTED (head_dim * elem size not a multiple
+ *   of 16 bytes), PA_ERR_CUDA.  num_tokens = 0 is a no-op.
+ */
+pa_status pa_reshape_and_cache(const void *k, const void *v, void *k_cache, void *v_cache,
+                               const int64_t *slot_mapping, int num_tokens, int num_kv_heads,
+                               int head_dim, int block_size, int num_blocks, pa_dtype dtype,
+                               void *stream);
+
+/*
+ * pa_copy_blocks -- copy-on-write of whole blocks.
+ *
+ * Defines ([S] "Memory sharing": a sequence about to write into a shared block gets
+ * a private copy of that block only, like fork()):
+ *     for each pair i: k_cache[dst_i] = k_cache[src_i]; v_cache[dst_i] = v_cache[src_i]
+ * where a block is block_bytes contiguous bytes (block_size * num_kv_heads *
+ * head_dim * elem size).  Pairs run concurrently: no dst may equal any src or
+ * another dst (the allocator only produces fresh destinations).  Pairs with an
+ * index outside [0, num_blocks) are skipped.  Bit-exact.
+ *
+ *   src_dst_pairs  device int32 [num_pairs][2] (src, dst)
+ *   block_bytes    multiple of 16
+ * Errors: PA_ERR_INVALID, PA_ERR_CUDA.  num_pairs = 0 is a no-op.
+ */
+pa_status pa_copy_blocks(void *k_cache, void *v_cache, const int32_t *src_dst_pairs,
+                         int num_pairs, int num_blocks, size_t block_bytes, void *stream);
+
+/*
+ * Device-side error flags of the current device (bitwise OR of PA_DEVERR_*), read
+ * and cleared with a synchronous copy after `stream` drains.  A kernel that gives
+ * up on a wait (a TMA transfer that never lands, ~2 s) sets a flag and returns
+ * instead of hanging.
+ */
+#define PA_DEVERR_TIMEOUT_FULL  1u   /* consumer waited too long for a K/V tile   */
+#define PA_DEVERR_TIMEOUT_EMPTY 2u   /* producer waited too long for a free stage */
+pa_status pa_device_errors(unsigned int *flags, void *stream);
+
+/* ------------------------------------------------------------------------- *
+ * Host block allocator ([S] "vLLM": free list, reference counts, copy-on-write;  *
+ * [T] §2.2 BlockManager, §3.1 append_kv, §5.1 clone_sequence).  Host memory    *
+ * only; never touches the GPU.  Not thread-safe: one caller at a time.         *
+ * ------------------------------------------------------------------------- */
+typedef struct pa_alloc pa_alloc;
+
+/*
+ * Create a pool of num_blocks blocks of block_size tokens.  The free list starts as
+ * `free_order` (a permutation of 0..num_blocks-1; NULL = 0, 1, ..., num_blocks-1,
+ * the tutorial's list(range(total_pages))).  Allocation pops the LAST element.
+ */
+pa_status pa_alloc_create(pa_alloc **out, int num_blocks, int block_size,
+                          const int32_t *free_order);
+void pa_alloc_destroy(pa_alloc *a);
+
+/* New empty sequence; ids are 0, 1, 2, ... in creation order (forks included). */
+pa_status pa_alloc_new_seq(pa_alloc *a, int *seq_id);
+
+/* New sequence sharing all of `parent`'s blocks (each block's refcount + 1). */
+pa_status pa_alloc_fork(pa_alloc *a, int parent, int *child);
+
+/*
+ * Reserve the slot of the next token of `seq` (position p = current length):
+ *   - logical block p / B not mapped yet: pop a free block (refcount 1);
+ *   - mapped but shared (refcount > 1): copy-on-write -- pop a free block, emit
+ *     (*cow_src, *cow_dst) = (old, new), old refcount - 1, map the new block;
+ *   - otherwise write in place.
+ * *slot = block * B + p % B.  *cow_src = *cow_dst = -1 when nothing is copied.
+ * PA_ERR_OOM (no free block) leaves every piece of state unchanged.
+ */
+pa_status pa_alloc_append(pa_alloc *a, int seq, int64_t *slot, int32_t *cow_src,
+                          int32_t *cow_dst);
+
+/* Reserve n slots at once (same as n calls of pa_alloc_append); slots[n] and up to
+ * n copy pairs (cow_pairs[2*i], cow_pairs[2*i+1]) with *num_cow set.  On PA_ERR_OOM
+ * the appends made before the failing one stay (as with separate calls); *done
+ * (optional) tells how many succeeded. */
+pa_status pa_alloc_append_n(pa_alloc *a, int seq, int n, int64_t *slots, int32_t *cow_pairs,
+                            int *num_cow, int *done);
+
+/* Release a sequence: its blocks' refcounts drop in table order; a block reaching 0
+ * is appended to the end of the free list. */
+pa_status pa_alloc_free_seq(pa_alloc *a, int seq);
+
+/* Copy up to `cap` entries of the sequence's block table; *n = its full length. */
+pa_status pa_alloc_block_table(const pa_alloc *a, int seq, int32_t *out, int cap, int *n);
+pa_status pa_alloc_seq_len(const pa_alloc *a, int seq, int *len);
+int pa_alloc_refcount(const pa_alloc *a, int block);     /* -1 if out of range */
+int pa_alloc_num_free(const pa_alloc *a);
+/* Copy up to `cap` free-list entries (bottom to top: the next pop is the last). */
+pa_status pa_alloc_free_list(const pa_alloc *a, int32_t *out, int cap, int *n);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* PAGEDKV_H */

@@ -1,0 +1,253 @@
+"""GB300-native paged decode attention: Python binding of libpagedkv.so.
+
+Functions carry the names of the C ABI in include/pagedkv.h and only marshal
+arguments (torch tensors -> device pointers and sizes, current stream); every step
+of the computation runs in the library's CUDA kernels.  There is no CPU path:
+calls on tensors that are not CUDA tensors raise.
+
+    pa_decode               paged single-query attention (partition + merge kernels)
+    pa_reshape_and_cache    write new tokens' K/V rows through a slot mapping
+    pa_copy_blocks          copy-on-write block copies
+    BlockAllocator          host ref-counted block allocator (pa_alloc_*)
+"""
+from __future__ import annotations
+
+import ctypes
+from typing import List, Optional, Sequence, Tuple
+
+from ._lib import load as _load, library_path  # noqa: F401
+
+PA_OK, PA_ERR_INVALID, PA_ERR_UNSUPPORTED, PA_ERR_CUDA, PA_ERR_OOM, PA_ERR_TIMEOUT = range(6)
+PA_F32, PA_F16, PA_BF16 = 0, 1, 2
+
+
+class PagedKVError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        lib = _load()
+        msg = lib.pa_status_string(status).decode()
+        if status == PA_ERR_CUDA:
+            msg += f" (cudaError {lib.pa_last_cuda_error()})"
+        super().__init__(f"{where}: {msg}")
+        self.status = status
+
+
+class OutOfBlocks(PagedKVError, MemoryError):
+    pass
+
+
+def _check(status: int, where: str) -> None:
+    if status == PA_ERR_OOM:
+        raise OutOfBlocks(status, where)
+    if status != PA_OK:
+        raise PagedKVError(status, where)
+
+
+def _dtype_code(t) -> int:
+    import torch
+    codes = {torch.float32: PA_F32, torch.float16: PA_F16, torch.bfloat16: PA_BF16}
+    if t.dtype not in codes:
+        raise TypeError(f"unsupported dtype {t.dtype}")
+    return codes[t.dtype]
+
+
+def _cuda(t, name: str):
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor (the library has no CPU path)")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t.data_ptr()
+
+
+def _stream(stream) -> int:
+    import torch
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream if hasattr(s, "cuda_stream") else int(s)
+
+
+# ----------------------------------------------------------------------------
+# decode
+# ----------------------------------------------------------------------------
+def pa_decode_partition_size(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+                             max_blocks_per_seq, partition_size=0) -> int:
+    return _load().pa_decode_partition_size(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+                                            max_blocks_per_seq, partition_size)
+
+
+def pa_decode_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+                             max_blocks_per_seq, partition_size=0) -> int:
+    n = _load().pa_decode_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+                                         max_blocks_per_seq, partition_size)
+    if n == ctypes.c_size_t(-1).value:
+        raise PagedKVError(PA_ERR_INVALID, "pa_decode_workspace_size")
+    return n
+
+
+def alloc_workspace(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq,
+                    partition_size=0, device="cuda"):
+    """A caller-owned workspace tensor of the size pa_decode needs (None if 0)."""
+    import torch
+    n = pa_decode_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+                                 max_blocks_per_seq, partition_size)
+    return torch.empty(n, dtype=torch.uint8, device=device) if n > 0 else None
+
+
+def pa_decode(out, q, k_cache, v_cache, block_tables, context_lens, scale: float,
+              num_q_heads: int, num_kv_heads: int, head_dim: int, block_size: int,
+              partition_size: int = 0, workspace=None, stream=None):
+    """out[S, Hq, d] <- paged decode attention (see pa_decode in include/pagedkv.h).
+
+    q/out [S, Hq, d]; caches [num_blocks, B, Hkv, d]; block_tables int32 [S, W];
+    context_lens int32 [S]; workspace: uint8 CUDA tensor or None (allocated here)."""
+    import torch
+    S = q.shape[0]
+    W = block_tables.shape[1]
+    if workspace is None:
+        workspace = alloc_workspace(S, num_q_heads, num_kv_heads, head_dim, block_size, W,
+                                    partition_size, q.device)
+    ws_ptr = _cuda(workspace, "workspace") if workspace is not None else None
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    if block_tables.dtype != torch.int32 or context_lens.dtype != torch.int32:
+        raise TypeError("block_tables and context_lens must be int32")
+    st = _load().pa_decode(_cuda(out, "out"), _cuda(q, "q"), _cuda(k_cache, "k_cache"),
+                           _cuda(v_cache, "v_cache"), _cuda(block_tables, "block_tables"), W,
+                           _cuda(context_lens, "context_lens"), S, k_cache.shape[0], float(scale),
+                           num_q_heads, num_kv_heads, head_dim, block_size, _dtype_code(q),
+                           partition_size, ws_ptr, ws_bytes, _stream(stream))
+    _check(st, "pa_decode")
+    return out
+
+
+# ----------------------------------------------------------------------------
+# cache writes
+# ----------------------------------------------------------------------------
+def pa_reshape_and_cache(k, v, k_cache, v_cache, slot_mapping, stream=None):
+    """k_cache[slot // B][slot % B] = k[t] (and v) for every token t with slot >= 0."""
+    import torch
+    if slot_mapping.dtype != torch.int64:
+        raise TypeError("slot_mapping must be int64")
+    n = slot_mapping.shape[0]
+    if n == 0:
+        return
+    nb, B, hkv, d = k_cache.shape
+    st = _load().pa_reshape_and_cache(_cuda(k, "k"), _cuda(v, "v"), _cuda(k_cache, "k_cache"),
+                                      _cuda(v_cache, "v_cache"), _cuda(slot_mapping, "slot_mapping"),
+                                      n, hkv, d, B, nb, _dtype_code(k_cache), _stream(stream))
+    _check(st, "pa_reshape_and_cache")
+
+
+def pa_copy_blocks(k_cache, v_cache, src_dst_pairs, stream=None):
+    """k_cache[dst] = k_cache[src] (and v) for every (src, dst) row of the int32 [n, 2] pairs."""
+    import torch
+    if src_dst_pairs.dtype != torch.int32:
+        raise TypeError("src_dst_pairs must be int32")
+    n = src_dst_pairs.shape[0]
+    if n == 0:
+        return
+    block_bytes = k_cache[0].numel() * k_cache.element_size()
+    st = _load().pa_copy_blocks(_cuda(k_cache, "k_cache"), _cuda(v_cache, "v_cache"),
+                                _cuda(src_dst_pairs, "src_dst_pairs"), n, k_cache.shape[0],
+                                block_bytes, _stream(stream))
+    _check(st, "pa_copy_blocks")
+
+
+def pa_device_errors(stream=None) -> int:
+    flags = ctypes.c_uint(0)
+    _check(_load().pa_device_errors(ctypes.byref(flags), _stream(stream)), "pa_device_errors")
+    return flags.value
+
+
+def pa_status_string(status: int) -> str:
+    return _load().pa_status_string(status).decode()
+
+
+# ----------------------------------------------------------------------------
+# host allocator
+# ----------------------------------------------------------------------------
+class BlockAllocator:
+    """Ref-counted block allocator (pa_alloc_* of include/pagedkv.h); host only."""
+
+    def __init__(self, num_blocks: int, block_size: int, free_order: Optional[Sequence[int]] = None):
+        import numpy as np
+        self._lib = _load()
+        self._h = ctypes.c_void_p()
+        self.num_blocks = num_blocks
+        self.block_size = block_size
+        ptr = None
+        if free_order is not None:
+            self._order = np.ascontiguousarray(free_order, dtype=np.int32)
+            if self._order.shape != (num_blocks,):
+                raise ValueError("free_order must have num_blocks entries")
+            ptr = self._order.ctypes.data
+        _check(self._lib.pa_alloc_create(ctypes.byref(self._h), num_blocks, block_size, ptr),
+               "pa_alloc_create")
+
+    def __del__(self):
+        h = getattr(self, "_h", None)
+        if h is not None and h.value:
+            self._lib.pa_alloc_destroy(h)
+            self._h = None
+
+    def new_seq(self) -> int:
+        sid = ctypes.c_int()
+        _check(self._lib.pa_alloc_new_seq(self._h, ctypes.byref(sid)), "pa_alloc_new_seq")
+        return sid.value
+
+    def fork(self, parent: int) -> int:
+        sid = ctypes.c_int()
+        _check(self._lib.pa_alloc_fork(self._h, parent, ctypes.byref(sid)), "pa_alloc_fork")
+        return sid.value
+
+    def append(self, seq: int) -> Tuple[int, Optional[Tuple[int, int]]]:
+        slot = ctypes.c_int64()
+        src = ctypes.c_int32()
+        dst = ctypes.c_int32()
+        _check(self._lib.pa_alloc_append(self._h, seq, ctypes.byref(slot), ctypes.byref(src),
+                                         ctypes.byref(dst)), "pa_alloc_append")
+        return slot.value, ((src.value, dst.value) if src.value >= 0 else None)
+
+    def append_n(self, seq: int, n: int):
+        """n appends: (slots int64 [n], cow pairs int32 [k, 2])."""
+        import numpy as np
+        slots = np.empty(max(n, 1), dtype=np.int64)
+        pairs = np.empty((max(n, 1), 2), dtype=np.int32)
+        k = ctypes.c_int()
+        _check(self._lib.pa_alloc_append_n(self._h, seq, n, slots.ctypes.data, pairs.ctypes.data,
+                                           ctypes.byref(k), None), "pa_alloc_append_n")
+        return slots[:n], pairs[:k.value]
+
+    def free_seq(self, seq: int) -> None:
+        _check(self._lib.pa_alloc_free_seq(self._h, seq), "pa_alloc_free_seq")
+
+    def block_table(self, seq: int) -> List[int]:
+        import numpy as np
+        n = ctypes.c_int()
+        _check(self._lib.pa_alloc_block_table(self._h, seq, None, 0, ctypes.byref(n)), "pa_alloc_block_table")
+        out = np.empty(max(n.value, 1), dtype=np.int32)
+        _check(self._lib.pa_alloc_block_table(self._h, seq, out.ctypes.data, n.value, ctypes.byref(n)),
+               "pa_alloc_block_table")
+        return out[:n.value].tolist()
+
+    def seq_len(self, seq: int) -> int:
+        n = ctypes.c_int()
+        _check(self._lib.pa_alloc_seq_len(self._h, seq, ctypes.byref(n)), "pa_alloc_seq_len")
+        return n.value
+
+    def refcount(self, block: int) -> int:
+        return self._lib.pa_alloc_refcount(self._h, block)
+
+    def num_free(self) -> int:
+        return self._lib.pa_alloc_num_free(self._h)
+
+    def free_list(self) -> List[int]:
+        import numpy as np
+        n = ctypes.c_int()
+        _check(self._lib.pa_alloc_free_list(self._h, None, 0, ctypes.byref(n)), "pa_alloc_free_list")
+        out = np.empty(max(n.value, 1), dtype=np.int32)
+        _check(self._lib.pa_alloc_free_list(self._h, out.ctypes.data, n.value, ctypes.byref(n)),
+               "pa_alloc_free_list")
+        return out[:n.value].tolist()
+
+
+__all__ = ["pa_decode", "pa_decode_workspace_size", "pa_decode_partition_size", "alloc_workspace",
+           "pa_reshape_and_cache", "pa_copy_blocks", "pa_device_errors", "pa_status_string",
+           "BlockAllocator", "PagedKVError", "OutOfBlocks", "library_path"]

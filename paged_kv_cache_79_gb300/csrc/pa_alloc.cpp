@@ -1,0 +1,257 @@
+// Host block allocator: free list + reference counts + copy-on-write.
+//
+// Policy ("Efficient Memory Management for LLM Serving with PagedAttention",
+// azimuth.plus summary, sections "vLLM" and "Memory sharing"; CSDN tutorial
+// "PagedAttention实战" §2.2 BlockManager, §3.1 append_kv, §5.1 clone_sequence):
+//   - all blocks exist up front; the free list is a stack whose top is its last
+//     element (the tutorial pops from the end of a Python list);
+//   - allocating sets refcount 1, forking adds 1 to every shared block, freeing
+//     subtracts 1 and pushes a block back when it reaches 0;
+//   - a token lands at logical block pos / B, offset pos % B; writing into a block
+//     that other sequences still reference copies that block first.
+// Host memory only; every failure leaves the state unchanged.
+#include <algorithm>
+#include <new>
+#include <vector>
+
+#include "../../include/pagedkv.h"
+
+struct pa_alloc {
+    int num_blocks = 0;
+    int block_size = 0;
+    std::vector<int32_t> free_stack;            // top = back()
+    std::vector<int32_t> refs;
+    struct Seq {
+        bool live = false;
+        int64_t len = 0;
+        std::vector<int32_t> blocks;
+    };
+    std::vector<Seq> seqs;                      // index = sequence id
+};
+
+namespace {
+
+bool live(const pa_alloc *a, int seq)
+{
+    return a && seq >= 0 && seq < (int)a->seqs.size() && a->seqs[seq].live;
+}
+
+// One append; `stage` receives the copy pair.  No state changes on PA_ERR_OOM.
+pa_status append_one(pa_alloc *a, int seq, int64_t *slot, int32_t *src, int32_t *dst)
+{
+    pa_alloc::Seq &s = a->seqs[seq];
+    const int64_t pos = s.len;
+    const size_t logical = (size_t)(pos / a->block_size);
+    const int offset = (int)(pos % a->block_size);
+    *src = -1;
+    *dst = -1;
+    if (logical == s.blocks.size()) {
+        if (a->free_stack.empty())
+            return PA_ERR_OOM;
+        const int32_t b = a->free_stack.back();
+        a->free_stack.pop_back();
+        a->refs[b] = 1;
+        s.blocks.push_back(b);
+    } else {
+        const int32_t old = s.blocks[logical];
+        if (a->refs[old] > 1) {
+            if (a->free_stack.empty())
+                return PA_ERR_OOM;
+            const int32_t b = a->free_stack.back();
+            a->free_stack.pop_back();
+            a->refs[b] = 1;
+            a->refs[old] -= 1;
+            s.blocks[logical] = b;
+            *src = old;
+            *dst = b;
+        }
+    }
+    s.len = pos + 1;
+    *slot = (int64_t)s.blocks[logical] * a->block_size + offset;
+    return PA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+pa_status pa_alloc_create(pa_alloc **out, int num_blocks, int block_size, const int32_t *free_order)
+{
+    if (!out || num_blocks <= 0 || block_size <= 0)
+        return PA_ERR_INVALID;
+    *out = nullptr;
+    pa_alloc *a = new (std::nothrow) pa_alloc;
+    if (!a)
+        return PA_ERR_OOM;
+    try {
+        a->num_blocks = num_blocks;
+        a->block_size = block_size;
+        a->refs.assign(num_blocks, 0);
+        a->free_stack.resize(num_blocks);
+        if (free_order) {
+            std::vector<char> seen(num_blocks, 0);
+            for (int i = 0; i < num_blocks; ++i) {
+                const int32_t b = free_order[i];
+                if (b < 0 || b >= num_blocks || seen[b]) {
+                    delete a;
+                    return PA_ERR_INVALID;
+                }
+                seen[b] = 1;
+                a->free_stack[i] = b;
+            }
+        } else {
+            for (int i = 0; i < num_blocks; ++i)
+                a->free_stack[i] = i;
+        }
+    } catch (...) {
+        delete a;
+        return PA_ERR_OOM;
+    }
+    *out = a;
+    return PA_OK;
+}
+
+void pa_alloc_destroy(pa_alloc *a) { delete a; }
+
+pa_status pa_alloc_new_seq(pa_alloc *a, int *seq_id)
+{
+    if (!a || !seq_id)
+        return PA_ERR_INVALID;
+    try {
+        a->seqs.emplace_back();
+    } catch (...) {
+        return PA_ERR_OOM;
+    }
+    a->seqs.back().live = true;
+    *seq_id = (int)a->seqs.size() - 1;
+    return PA_OK;
+}
+
+pa_status pa_alloc_fork(pa_alloc *a, int parent, int *child)
+{
+    if (!live(a, parent) || !child)
+        return PA_ERR_INVALID;
+    try {
+        pa_alloc::Seq c;
+        c.live = true;
+        c.len = a->seqs[parent].len;
+        c.blocks = a->seqs[parent].blocks;
+        a->seqs.push_back(std::move(c));
+    } catch (...) {
+        return PA_ERR_OOM;
+    }
+    for (int32_t b : a->seqs.back().blocks)
+        a->refs[b] += 1;
+    *child = (int)a->seqs.size() - 1;
+    return PA_OK;
+}
+
+pa_status pa_alloc_append(pa_alloc *a, int seq, int64_t *slot, int32_t *cow_src, int32_t *cow_dst)
+{
+    if (!live(a, seq) || !slot)
+        return PA_ERR_INVALID;
+    int32_t s = -1, d = -1;
+    try {
+        a->seqs[seq].blocks.reserve(a->seqs[seq].blocks.size() + 1);
+    } catch (...) {
+        return PA_ERR_OOM;
+    }
+    const pa_status st = append_one(a, seq, slot, &s, &d);
+    if (cow_src)
+        *cow_src = s;
+    if (cow_dst)
+        *cow_dst = d;
+    return st;
+}
+
+pa_status pa_alloc_append_n(pa_alloc *a, int seq, int n, int64_t *slots, int32_t *cow_pairs,
+                            int *num_cow, int *done)
+{
+    if (!live(a, seq) || n < 0 || (n > 0 && !slots) || !num_cow)
+        return PA_ERR_INVALID;
+    *num_cow = 0;
+    if (done)
+        *done = 0;
+    for (int i = 0; i < n; ++i) {
+        int32_t s, d;
+        try {
+            a->seqs[seq].blocks.reserve(a->seqs[seq].blocks.size() + 1);
+        } catch (...) {
+            return PA_ERR_OOM;
+        }
+        const pa_status st = append_one(a, seq, &slots[i], &s, &d);
+        if (st != PA_OK)
+            return st;
+        if (s >= 0 && cow_pairs) {
+            cow_pairs[2 * *num_cow] = s;
+            cow_pairs[2 * *num_cow + 1] = d;
+        }
+        if (s >= 0)
+            *num_cow += 1;
+        if (done)
+            *done = i + 1;
+    }
+    return PA_OK;
+}
+
+pa_status pa_alloc_free_seq(pa_alloc *a, int seq)
+{
+    if (!live(a, seq))
+        return PA_ERR_INVALID;
+    pa_alloc::Seq &s = a->seqs[seq];
+    // the free stack never exceeds num_blocks entries, so reserve up front
+    try {
+        a->free_stack.reserve(a->num_blocks);
+    } catch (...) {
+        return PA_ERR_OOM;
+    }
+    for (int32_t b : s.blocks) {
+        a->refs[b] -= 1;
+        if (a->refs[b] == 0)
+            a->free_stack.push_back(b);
+    }
+    s.blocks.clear();
+    s.blocks.shrink_to_fit();
+    s.len = 0;
+    s.live = false;
+    return PA_OK;
+}
+
+pa_status pa_alloc_block_table(const pa_alloc *a, int seq, int32_t *out, int cap, int *n)
+{
+    if (!live(a, seq) || !n || cap < 0 || (cap > 0 && !out))
+        return PA_ERR_INVALID;
+    const std::vector<int32_t> &b = a->seqs[seq].blocks;
+    *n = (int)b.size();
+    std::copy(b.begin(), b.begin() + std::min<size_t>(b.size(), (size_t)cap), out);
+    return PA_OK;
+}
+
+pa_status pa_alloc_seq_len(const pa_alloc *a, int seq, int *len)
+{
+    if (!live(a, seq) || !len)
+        return PA_ERR_INVALID;
+    *len = (int)a->seqs[seq].len;
+    return PA_OK;
+}
+
+int pa_alloc_refcount(const pa_alloc *a, int block)
+{
+    if (!a || block < 0 || block >= a->num_blocks)
+        return -1;
+    return a->refs[block];
+}
+
+int pa_alloc_num_free(const pa_alloc *a) { return a ? (int)a->free_stack.size() : -1; }
+
+pa_status pa_alloc_free_list(const pa_alloc *a, int32_t *out, int cap, int *n)
+{
+    if (!a || !n || cap < 0 || (cap > 0 && !out))
+        return PA_ERR_INVALID;
+    *n = (int)a->free_stack.size();
+    std::copy(a->free_stack.begin(),
+              a->free_stack.begin() + std::min<size_t>(a->free_stack.size(), (size_t)cap), out);
+    return PA_OK;
+}
+
+}  // extern "C"

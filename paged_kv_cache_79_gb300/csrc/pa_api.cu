@@ -1,0 +1,386 @@
+// extern "C" entry points of libpagedkv.so: argument validation, tensor-map
+// encoding, partition sizing and kernel dispatch.  Declarations and the contract
+// of every function are in include/pagedkv.h.
+#include <cmath>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <tuple>
+
+#include "pa_internal.h"
+
+namespace pagedkv {
+
+namespace {
+
+__device__ unsigned int g_device_errors;  // PA_DEVERR_* flags raised by kernels
+
+thread_local int t_last_cuda_error = 0;
+
+pa_status cuda_fail(cudaError_t e)
+{
+    t_last_cuda_error = (int)e;
+    cudaGetLastError();  // clear the sticky launch error of this thread
+    return PA_ERR_CUDA;
+}
+
+bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int elem_size(pa_dtype d) { return d == PA_F32 ? 4 : 2; }
+
+bool dtype_ok(int d) { return d == PA_F32 || d == PA_F16 || d == PA_BF16; }
+
+std::mutex g_mu;
+
+// ---- per-device facts ----------------------------------------------------------
+std::map<int, int> g_sm_count;
+std::map<std::tuple<void *, int, size_t>, int> g_occupancy;
+std::map<std::pair<void *, int>, size_t> g_smem_limit;
+std::map<int, unsigned int *> g_err_ptr;
+
+unsigned int *device_error_word(int dev, cudaError_t *err)
+{
+    std::lock_guard<std::mutex> lk(g_mu);
+    auto it = g_err_ptr.find(dev);
+    if (it != g_err_ptr.end())
+        return it->second;
+    void *ptr = nullptr;
+    *err = cudaGetSymbolAddress(&ptr, g_device_errors);
+    if (*err != cudaSuccess)
+        return nullptr;
+    g_err_ptr[dev] = static_cast<unsigned int *>(ptr);
+    return static_cast<unsigned int *>(ptr);
+}
+
+// ---- tensor maps ---------------------------------------------------------------
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn()
+{
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+        cudaGetLastError();
+    });
+    return fn;
+}
+
+// Cache [num_blocks][B][Hkv][d] seen as 4-D: (128-byte row of d, row index within
+// d, kv head, token slot).  One box = one kv head of one block, 128-byte swizzle.
+bool make_cache_map(CUtensorMap *map, const void *base, pa_dtype dt, int num_blocks, int B,
+                    int Hkv, int D)
+{
+    EncodeTiledFn enc = encode_fn();
+    if (!enc)
+        return false;
+    const int es = elem_size(dt);
+    const int ce = 128 / es;
+    const cuuint64_t dims[4] = {(cuuint64_t)ce, (cuuint64_t)(D / ce), (cuuint64_t)Hkv,
+                                (cuuint64_t)num_blocks * (cuuint64_t)B};
+    const cuuint64_t strides[3] = {128, (cuuint64_t)D * es, (cuuint64_t)Hkv * D * es};
+    const cuuint32_t box[4] = {(cuuint32_t)ce, 1, 1, (cuuint32_t)B};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    const CUtensorMapDataType tdt = dt == PA_F32   ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                    : dt == PA_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                                   : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    const CUresult r = enc(map, tdt, 4, const_cast<void *>(base), dims, strides, box, estr,
+                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+// ---- partition sizing ------------------------------------------------------------
+bool decode_shape_ok(int num_seqs, int Hq, int Hkv, int D, int B, int max_blocks, int part)
+{
+    if (num_seqs < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || max_blocks <= 0)
+        return false;
+    if (D != 64 && D != 128)
+        return false;
+    if (B != 16 && B != 32)
+        return false;
+    if (part < 0 || (part > 0 && part % B != 0))
+        return false;
+    if ((long long)max_blocks * B >= (1ll << 31))
+        return false;
+    return true;
+}
+
+int resolve_partition(int num_seqs, int Hq, int Hkv, int B, int max_blocks, int part, int sms)
+{
+    const long long max_ctx = (long long)max_blocks * B;
+    if (part > 0)
+        return part;
+    // Auto: aim for ~8 work items per resident CTA (2 per SM) assuming contexts
+    // average half the table capacity; never below 8 blocks, never above 1024
+    // tokens; one partition when the whole table fits.
+    const long long groups = (Hq / Hkv + kHeadsPerItem - 1) / kHeadsPerItem;
+    const long long units = (long long)num_seqs * Hkv * groups;
+    const long long target = 8ll * 2 * (sms > 0 ? sms : 148);
+    long long p = units > 0 ? (units * (max_ctx / 2)) / target : max_ctx;
+    const long long lo = 8ll * B, hi = 1024;
+    if (p < lo)
+        p = lo;
+    if (p > hi)
+        p = hi;
+    p = (p / B) * B;
+    if (p >= max_ctx)
+        p = ((max_ctx + B - 1) / B) * B;
+    return (int)p;
+}
+
+}  // namespace
+
+int sm_count(int device)
+{
+    std::lock_guard<std::mutex> lk(g_mu);
+    auto it = g_sm_count.find(device);
+    if (it != g_sm_count.end())
+        return it->second;
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, device) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    g_sm_count[device] = n;
+    return n;
+}
+
+int cached_occupancy(void *kernel, int device, size_t smem, size_t max_smem)
+{
+    std::lock_guard<std::mutex> lk(g_mu);
+    const auto key = std::make_tuple(kernel, device, smem);
+    auto it = g_occupancy.find(key);
+    if (it != g_occupancy.end())
+        return it->second;
+    const auto lkey = std::make_pair(kernel, device);
+    if (g_smem_limit[lkey] < max_smem) {
+        if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)max_smem) != cudaSuccess) {
+            cudaGetLastError();
+            return 0;
+        }
+        g_smem_limit[lkey] = max_smem;
+    }
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, kThreads, smem) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    g_occupancy[key] = n;
+    return n;
+}
+
+}  // namespace pagedkv
+
+using namespace pagedkv;
+
+extern "C" {
+
+const char *pa_status_string(pa_status s)
+{
+    switch (s) {
+    case PA_OK: return "ok";
+    case PA_ERR_INVALID: return "invalid argument";
+    case PA_ERR_UNSUPPORTED: return "unsupported configuration";
+    case PA_ERR_CUDA: return "CUDA error";
+    case PA_ERR_OOM: return "out of blocks";
+    case PA_ERR_TIMEOUT: return "device wait timed out";
+    }
+    return "unknown status";
+}
+
+int pa_last_cuda_error(void) { return t_last_cuda_error; }
+
+int pa_decode_partition_size(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                             int block_size, int max_blocks_per_seq, int partition_size)
+{
+    if (!decode_shape_ok(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+                         max_blocks_per_seq, partition_size))
+        return 0;
+    int dev = 0;
+    int sms = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess)
+        sms = sm_count(dev);
+    else
+        cudaGetLastError();
+    return resolve_partition(num_seqs, num_q_heads, num_kv_heads, block_size, max_blocks_per_seq,
+                             partition_size, sms);
+}
+
+size_t pa_decode_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                                int block_size, int max_blocks_per_seq, int partition_size)
+{
+    const int part = pa_decode_partition_size(num_seqs, num_q_heads, num_kv_heads, head_dim,
+                                              block_size, max_blocks_per_seq, partition_size);
+    if (part <= 0)
+        return (size_t)-1;
+    const long long pb = part / block_size;
+    const long long parts = (max_blocks_per_seq + pb - 1) / pb;
+    if (parts <= 1)
+        return 0;
+    const size_t rows = (size_t)num_seqs * (size_t)parts * (size_t)num_q_heads;
+    size_t bytes = rows * (size_t)head_dim * 4;
+    bytes = (bytes + 255) & ~size_t(255);
+    return bytes + rows * 4;
+}
+
+pa_status pa_decode(void *out, const void *q, const void *k_cache, const void *v_cache,
+                    const int32_t *block_tables, int max_blocks_per_seq,
+                    const int32_t *context_lens, int num_seqs, int num_blocks, float scale,
+                    int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                    pa_dtype dtype, int partition_size, void *workspace, size_t workspace_bytes,
+                    void *stream)
+{
+    if (num_seqs == 0)
+        return PA_OK;
+    if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens)
+        return PA_ERR_INVALID;
+    if (!aligned(out, 16) || !aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
+        !aligned(block_tables, 4) || !aligned(context_lens, 4))
+        return PA_ERR_INVALID;
+    if (num_seqs < 0 || num_blocks <= 0 || num_q_heads <= 0 || num_kv_heads <= 0 ||
+        max_blocks_per_seq <= 0 || num_q_heads % num_kv_heads != 0)
+        return PA_ERR_INVALID;
+    if (partition_size < 0 || (partition_size > 0 && partition_size % block_size != 0))
+        return PA_ERR_INVALID;
+    if (!dtype_ok(dtype))
+        return PA_ERR_UNSUPPORTED;
+    if ((head_dim != 64 && head_dim != 128) || (block_size != 16 && block_size != 32))
+        return PA_ERR_UNSUPPORTED;
+    if ((long long)num_blocks * block_size >= (1ll << 31) ||
+        (long long)max_blocks_per_seq * block_size >= (1ll << 31))
+        return PA_ERR_INVALID;
+
+    int dev = 0;
+    cudaError_t ce = cudaGetDevice(&dev);
+    if (ce != cudaSuccess)
+        return cuda_fail(ce);
+    const int sms = sm_count(dev);
+    if (sms <= 0)
+        return cuda_fail(cudaErrorNoDevice);
+
+    const int part = resolve_partition(num_seqs, num_q_heads, num_kv_heads, block_size,
+                                       max_blocks_per_seq, partition_size, sms);
+    const int pb = part / block_size;
+    const int parts = (max_blocks_per_seq + pb - 1) / pb;
+    const size_t need = pa_decode_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim,
+                                                 block_size, max_blocks_per_seq, partition_size);
+    if (need == (size_t)-1)
+        return PA_ERR_INVALID;
+    if (need > 0 && (!workspace || workspace_bytes < need || !aligned(workspace, 16)))
+        return PA_ERR_INVALID;
+
+    DecodeLaunch L;
+    std::memset(&L, 0, sizeof L);
+    DecodeParams &p = L.p;
+    p.out = out;
+    p.q = q;
+    p.block_tables = block_tables;
+    p.context_lens = context_lens;
+    if (parts > 1) {
+        const size_t rows = (size_t)num_seqs * parts * num_q_heads;
+        p.part_o = static_cast<float *>(workspace);
+        p.part_lse = reinterpret_cast<float *>(static_cast<char *>(workspace) +
+                                               ((rows * head_dim * 4 + 255) & ~size_t(255)));
+    }
+    p.errors = device_error_word(dev, &ce);
+    if (!p.errors)
+        return cuda_fail(ce);
+    p.scale_log2 = scale * 1.4426950408889634f;
+    p.num_seqs = num_seqs;
+    p.max_blocks = max_blocks_per_seq;
+    p.num_blocks = num_blocks;
+    p.num_q_heads = num_q_heads;
+    p.num_kv_heads = num_kv_heads;
+    p.group = num_q_heads / num_kv_heads;
+    p.head_groups = (p.group + kHeadsPerItem - 1) / kHeadsPerItem;
+    p.partition_blocks = pb;
+    p.max_parts = parts;
+    L.head_dim = head_dim;
+    L.block_size = block_size;
+    L.sm_count = sms;
+    L.grid = 0;
+    if (!make_cache_map(&L.tmap_k, k_cache, dtype, num_blocks, block_size, num_kv_heads, head_dim) ||
+        !make_cache_map(&L.tmap_v, v_cache, dtype, num_blocks, block_size, num_kv_heads, head_dim))
+        return cuda_fail(cudaErrorInvalidValue);
+
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e = dtype == PA_F32   ? launch_decode_f32(L, st)
+                    : dtype == PA_F16 ? launch_decode_f16(L, st)
+                                      : launch_decode_bf16(L, st);
+    if (e != cudaSuccess)
+        return cuda_fail(e);
+    return PA_OK;
+}
+
+pa_status pa_reshape_and_cache(const void *k, const void *v, void *k_cache, void *v_cache,
+                               const int64_t *slot_mapping, int num_tokens, int num_kv_heads,
+                               int head_dim, int block_size, int num_blocks, pa_dtype dtype,
+                               void *stream)
+{
+    if (num_tokens == 0)
+        return PA_OK;
+    if (!k || !v || !k_cache || !v_cache || !slot_mapping)
+        return PA_ERR_INVALID;
+    if (num_tokens < 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 || num_blocks <= 0)
+        return PA_ERR_INVALID;
+    if (!dtype_ok(dtype))
+        return PA_ERR_UNSUPPORTED;
+    if (!aligned(k, 16) || !aligned(v, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
+        !aligned(slot_mapping, 8))
+        return PA_ERR_INVALID;
+    const size_t row = (size_t)num_kv_heads * head_dim * elem_size(dtype);
+    if (row % 16 != 0)
+        return PA_ERR_UNSUPPORTED;
+    const cudaError_t e = launch_reshape_and_cache(
+        k, v, k_cache, v_cache, slot_mapping, num_tokens, row,
+        (long long)num_blocks * block_size, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PA_OK : cuda_fail(e);
+}
+
+pa_status pa_copy_blocks(void *k_cache, void *v_cache, const int32_t *src_dst_pairs,
+                         int num_pairs, int num_blocks, size_t block_bytes, void *stream)
+{
+    if (num_pairs == 0)
+        return PA_OK;
+    if (!k_cache || !v_cache || !src_dst_pairs || num_pairs < 0 || num_blocks <= 0 ||
+        block_bytes == 0 || block_bytes % 16 != 0)
+        return PA_ERR_INVALID;
+    if (!aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(src_dst_pairs, 4))
+        return PA_ERR_INVALID;
+    if (block_bytes / 16 > 65535ull * 1024ull)
+        return PA_ERR_UNSUPPORTED;
+    const cudaError_t e = launch_copy_blocks(k_cache, v_cache, src_dst_pairs, num_pairs, num_blocks,
+                                             block_bytes, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PA_OK : cuda_fail(e);
+}
+
+pa_status pa_device_errors(unsigned int *flags, void *stream)
+{
+    if (!flags)
+        return PA_ERR_INVALID;
+    cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess)
+        return cuda_fail(e);
+    unsigned int v = 0;
+    e = cudaMemcpyFromSymbol(&v, g_device_errors, sizeof v);
+    if (e != cudaSuccess)
+        return cuda_fail(e);
+    const unsigned int zero = 0;
+    e = cudaMemcpyToSymbol(g_device_errors, &zero, sizeof zero);
+    if (e != cudaSuccess)
+        return cuda_fail(e);
+    *flags = v;
+    return PA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,88 @@
+// Cache writes: KV append through a slot mapping and copy-on-write block copies.
+//
+// reshape_and_cache follows CSDN tutorial "PagedAttention实战" §3.1 append_kv
+// (token position -> logical page pos // page_size, offset pos % page_size; the
+// allocator turns that into a slot = physical_block * B + offset).  copy_blocks is
+// the copy half of copy-on-write ("Efficient Memory Management for LLM Serving with
+// PagedAttention", azimuth.plus summary, section "Memory sharing").  Both are plain
+// 16-byte vector copies: the cost is launch latency and HBM bytes.
+#include "pa_internal.h"
+
+namespace pagedkv {
+
+namespace {
+
+// One CTA per (token, K or V).  A token's row of num_kv_heads * head_dim elements is
+// contiguous both in the input and in the cache ([NB][B][Hkv][d] layout).
+__global__ void __launch_bounds__(128)
+    reshape_and_cache_kernel(const uint4 *__restrict__ k, const uint4 *__restrict__ v,
+                             uint4 *__restrict__ k_cache, uint4 *__restrict__ v_cache,
+                             const int64_t *__restrict__ slots, int vec_per_row, long long num_slots)
+{
+    const int t = blockIdx.x;
+    const int64_t slot = slots[t];
+    if (slot < 0 || slot >= num_slots)
+        return;
+    const uint4 *src = (blockIdx.y == 0 ? k : v) + (size_t)t * vec_per_row;
+    uint4 *dst = (blockIdx.y == 0 ? k_cache : v_cache) + (size_t)slot * vec_per_row;
+    for (int i = threadIdx.x; i < vec_per_row; i += blockDim.x)
+        dst[i] = __ldg(src + i);
+}
+
+constexpr int kCopyThreads = 256;
+constexpr int kCopyUnroll = 4;
+
+// grid = (pairs, 2 caches, chunks of kCopyThreads * kCopyUnroll 16-byte vectors)
+__global__ void __launch_bounds__(kCopyThreads)
+    copy_blocks_kernel(uint4 *__restrict__ k_cache, uint4 *__restrict__ v_cache,
+                       const int32_t *__restrict__ pairs, int num_blocks, long long vec_per_block)
+{
+    const int src = pairs[2 * blockIdx.x];
+    const int dst = pairs[2 * blockIdx.x + 1];
+    if (src < 0 || src >= num_blocks || dst < 0 || dst >= num_blocks)
+        return;
+    uint4 *cache = blockIdx.y == 0 ? k_cache : v_cache;
+    const uint4 *s = cache + (size_t)src * vec_per_block;
+    uint4 *d = cache + (size_t)dst * vec_per_block;
+    const long long first = (long long)blockIdx.z * kCopyThreads * kCopyUnroll + threadIdx.x;
+    uint4 tmp[kCopyUnroll];
+#pragma unroll
+    for (int u = 0; u < kCopyUnroll; ++u) {
+        const long long i = first + (long long)u * kCopyThreads;
+        if (i < vec_per_block)
+            tmp[u] = s[i];
+    }
+#pragma unroll
+    for (int u = 0; u < kCopyUnroll; ++u) {
+        const long long i = first + (long long)u * kCopyThreads;
+        if (i < vec_per_block)
+            d[i] = tmp[u];
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_reshape_and_cache(const void *k, const void *v, void *k_cache, void *v_cache,
+                                     const int64_t *slots, int num_tokens, size_t row_bytes,
+                                     long long num_slots, cudaStream_t stream)
+{
+    const int vec = (int)(row_bytes / 16);
+    const int threads = vec >= 128 ? 128 : (vec >= 64 ? 64 : 32);
+    reshape_and_cache_kernel<<<dim3((unsigned)num_tokens, 2), threads, 0, stream>>>(
+        static_cast<const uint4 *>(k), static_cast<const uint4 *>(v), static_cast<uint4 *>(k_cache),
+        static_cast<uint4 *>(v_cache), slots, vec, num_slots);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_copy_blocks(void *k_cache, void *v_cache, const int32_t *pairs, int num_pairs,
+                               int num_blocks, size_t block_bytes, cudaStream_t stream)
+{
+    const long long vec = (long long)(block_bytes / 16);
+    const long long per_cta = (long long)kCopyThreads * kCopyUnroll;
+    const unsigned z = (unsigned)((vec + per_cta - 1) / per_cta);
+    copy_blocks_kernel<<<dim3((unsigned)num_pairs, 2, z), kCopyThreads, 0, stream>>>(
+        static_cast<uint4 *>(k_cache), static_cast<uint4 *>(v_cache), pairs, num_blocks, vec);
+    return cudaGetLastError();
+}
+
+}  // namespace pagedkv

@@ -1,0 +1,78 @@
+// Internal declarations shared by the translation units of libpagedkv.so.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "../../include/pagedkv.h"
+
+namespace pagedkv {
+
+// Query heads handled by one work item: the M dimension of the m16n8k16 tiles.
+constexpr int kHeadsPerItem = 16;
+// Consumer warps per CTA; one more warp issues the TMA copies.
+constexpr int kConsumerWarps = 4;
+constexpr int kThreads = 32 * (kConsumerWarps + 1);
+// A device-side wait gives up after this long (ns) and raises an error flag.
+constexpr unsigned long long kWaitTimeoutNs = 2000000000ull;
+
+// Everything the decode kernels read besides the two tensor maps.
+struct DecodeParams {
+    void *out;                    // [S][Hq][D] storage dtype
+    const void *q;                // [S][Hq][D] storage dtype
+    const int32_t *block_tables;  // [S][max_blocks]
+    const int32_t *context_lens;  // [S]
+    float *part_o;                // [S][max_parts][Hq][D] fp32 (null if max_parts == 1)
+    float *part_lse;              // [S][max_parts][Hq]    fp32 log2-sum-exp
+    unsigned int *errors;         // device error flags (PA_DEVERR_*)
+    float scale_log2;             // softmax scale * log2(e)
+    int num_seqs;
+    int max_blocks;               // block-table row length
+    int num_blocks;               // physical blocks in the pool
+    int num_q_heads;
+    int num_kv_heads;
+    int group;                    // num_q_heads / num_kv_heads
+    int head_groups;              // ceil(group / kHeadsPerItem)
+    int partition_blocks;         // blocks per partition
+    int max_parts;                // ceil(max_blocks / partition_blocks)
+};
+
+struct DecodeLaunch {
+    DecodeParams p;
+    CUtensorMap tmap_k;
+    CUtensorMap tmap_v;
+    int head_dim;
+    int block_size;
+    int grid;                     // 0: let the launcher size it from occupancy
+    int sm_count;
+};
+
+// Per-dtype launchers (pa_decode_{f32,f16,bf16}.cu).  They size the persistent
+// grid from occupancy, launch the partition kernel and, when any sequence can
+// span several partitions, the merge kernel.
+cudaError_t launch_decode_f32(const DecodeLaunch &L, cudaStream_t stream);
+cudaError_t launch_decode_f16(const DecodeLaunch &L, cudaStream_t stream);
+cudaError_t launch_decode_bf16(const DecodeLaunch &L, cudaStream_t stream);
+
+// Shared-memory bytes the partition kernel needs (including alignment slack).
+size_t decode_smem_bytes_f32(int head_dim, int block_size, int group);
+size_t decode_smem_bytes_f16(int head_dim, int block_size, int group);
+size_t decode_smem_bytes_bf16(int head_dim, int block_size, int group);
+
+// Resident CTAs per SM of `kernel` with `smem` dynamic shared memory on `device`
+// (raises the kernel's dynamic shared-memory limit to `max_smem` first).  Cached.
+int cached_occupancy(void *kernel, int device, size_t smem, size_t max_smem);
+
+// Number of SMs of `device` (cached).
+int sm_count(int device);
+
+cudaError_t launch_reshape_and_cache(const void *k, const void *v, void *k_cache, void *v_cache,
+                                     const int64_t *slots, int num_tokens, size_t row_bytes,
+                                     long long num_slots, cudaStream_t stream);
+cudaError_t launch_copy_blocks(void *k_cache, void *v_cache, const int32_t *pairs, int num_pairs,
+                               int num_blocks, size_t block_bytes, cudaStream_t stream);
+
+}  // namespace pagedkv

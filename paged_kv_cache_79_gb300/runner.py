@@ -1,0 +1,124 @@
+"""Execute an allocator script on the GPU path and prepare decode-step inputs.
+
+A script is a list of events (new sequence, fork, prefill n tokens, decode step,
+free).  The host allocator (pa_alloc_*) decides slots and copy-on-write pairs;
+pa_copy_blocks and pa_reshape_and_cache apply them to the device caches.  The
+last decode step's inputs are kept as a `DecodeStep`, which can be replayed: a
+replay re-applies the same copy pairs and rows and recomputes the same decode.
+"""
+from __future__ import annotations
+
+import dataclasses
+from typing import Callable, List, Optional
+
+import numpy as np
+
+from . import BlockAllocator, alloc_workspace, pa_copy_blocks, pa_decode, pa_reshape_and_cache
+
+
+def _kind(ev) -> str:
+    return type(ev).__name__
+
+
+def tables_for(alloc: BlockAllocator, seqs, width: Optional[int] = None):
+    """(block_tables int32 [S, width], -1 padded; context_lens int32 [S]) as numpy."""
+    tabs = [alloc.block_table(s) for s in seqs]
+    w = width if width is not None else max(1, max(len(t) for t in tabs))
+    bt = np.full((len(seqs), w), -1, dtype=np.int32)
+    for i, t in enumerate(tabs):
+        bt[i, :len(t)] = t
+    cl = np.array([alloc.seq_len(s) for s in seqs], dtype=np.int32)
+    return bt, cl
+
+
+@dataclasses.dataclass
+class DecodeStep:
+    """Device-resident inputs of one decode step (all CUDA tensors)."""
+    q: "object"
+    k_cache: "object"
+    v_cache: "object"
+    step_k: "object"
+    step_v: "object"
+    slots: "object"            # int64 [n_tok]
+    pairs: "object"            # int32 [n_pairs, 2]
+    block_tables: "object"     # int32 [S, W]
+    context_lens: "object"     # int32 [S]
+    out: "object"
+    workspace: "object"
+    scale: float
+    num_q_heads: int
+    num_kv_heads: int
+    head_dim: int
+    block_size: int
+    partition_size: int = 0
+
+    def run(self, stream=None):
+        """copy-on-write pairs, then the new tokens' K/V, then decode."""
+        if self.pairs.shape[0]:
+            pa_copy_blocks(self.k_cache, self.v_cache, self.pairs, stream)
+        pa_reshape_and_cache(self.step_k, self.step_v, self.k_cache, self.v_cache, self.slots, stream)
+        return self.decode(stream)
+
+    def decode(self, stream=None):
+        return pa_decode(self.out, self.q, self.k_cache, self.v_cache, self.block_tables,
+                         self.context_lens, self.scale, self.num_q_heads, self.num_kv_heads,
+                         self.head_dim, self.block_size, self.partition_size, self.workspace,
+                         stream)
+
+
+def execute(w, k_cache, v_cache, step_kv: Callable, query: Callable,
+            on_step: Optional[Callable] = None, stream=None, width: Optional[int] = None):
+    """Run workload `w`'s script on the device caches.
+
+    step_kv(step) -> (k, v) CUDA tensors of the step's new tokens; query(step) ->
+    q [S, Hq, d].  After each step, `on_step(step, alloc, decode_step)` (if given) is
+    called with a DecodeStep holding that step's inputs; the step's copies and
+    writes have been enqueued, its decode has not.  Returns (alloc, last DecodeStep)."""
+    import torch
+    dev = k_cache.device
+    alloc = BlockAllocator(w.num_blocks, w.block_size, w.free_order)
+    last = None
+    for ev in w.events:
+        kind = _kind(ev)
+        if kind == "NewSeq":
+            alloc.new_seq()
+        elif kind == "Fork":
+            alloc.fork(ev.parent)
+        elif kind == "FreeSeq":
+            alloc.free_seq(ev.seq)
+        elif kind == "Prefill":
+            if ev.n <= 0:
+                continue
+            _, pairs = alloc.append_n(ev.seq, ev.n)
+            if len(pairs):
+                pa_copy_blocks(k_cache, v_cache, torch.from_numpy(pairs).to(dev), stream)
+        elif kind == "Step":
+            slots, pairs = [], []
+            for s in ev.seqs:
+                slot, cow = alloc.append(s)
+                slots.append(slot)
+                if cow is not None:
+                    pairs.append(cow)
+            k, v = step_kv(ev)
+            bt, cl = tables_for(alloc, w.decode_seqs, width)
+            S = len(w.decode_seqs)
+            q = query(ev)
+            ds = DecodeStep(
+                q=q, k_cache=k_cache, v_cache=v_cache, step_k=k, step_v=v,
+                slots=torch.tensor(slots, dtype=torch.int64, device=dev),
+                pairs=torch.tensor(np.array(pairs, dtype=np.int32).reshape(-1, 2), device=dev),
+                block_tables=torch.from_numpy(bt).to(dev), context_lens=torch.from_numpy(cl).to(dev),
+                out=torch.empty_like(q),
+                workspace=alloc_workspace(S, w.num_q_heads, w.num_kv_heads, w.head_dim, w.block_size,
+                                          bt.shape[1], w.partition_size, dev),
+                scale=w.softmax_scale, num_q_heads=w.num_q_heads, num_kv_heads=w.num_kv_heads,
+                head_dim=w.head_dim, block_size=w.block_size, partition_size=w.partition_size)
+            if ds.pairs.shape[0]:
+                pa_copy_blocks(k_cache, v_cache, ds.pairs, stream)
+            pa_reshape_and_cache(k, v, k_cache, v_cache, ds.slots, stream)
+            if on_step is not None:
+                on_step(ev, alloc, ds)
+            last = ds
+        else:
+            raise TypeError(f"unknown event {ev!r}")
+    return alloc, last

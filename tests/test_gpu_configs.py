@@ -1,0 +1,141 @@
+"""The five synthetic workloads end to end: allocator script, copy-on-write,
+appends and decode on the GPU path, against the oracle's own execution of the
+same script (allocator, cache ops and fp64 attention)."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_kv_cache_79_gb300 as P
+import workloads as W
+from paged_kv_cache_79_gb300 import runner
+from tests.gpu_harness import assert_close, raw
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def _gpu_tensors(w):
+    kc, vc = W.pool_tensors(w, DEV)
+    return kc, vc
+
+
+def _step_kv(w):
+    return lambda ev: W.step_tensors(w, ev, DEV)
+
+
+def _query(w):
+    return lambda ev: W.query_tensor(w, ev.index, DEV)
+
+
+def test_tiny_fifty_appends_each_decoded():
+    """The tutorial's workflow: 50 appends to one sequence, decode after each."""
+    w = W.tiny()
+    kc, vc = _gpu_tensors(w)
+    kh, vh = raw(kc).copy(), raw(vc).copy()
+    outs = []
+
+    def on_step(ev, alloc, ds):
+        outs.append((ds.decode().clone(), raw(ds.q), alloc.block_table(0), alloc.seq_len(0)))
+
+    alloc, _ = runner.execute(w, kc, vc, _step_kv(w), _query(w), on_step=on_step)
+    torch.cuda.synchronize()
+    assert alloc.block_table(0) == oracle.run_script(w.events, w.num_blocks, w.block_size,
+                                                     w.free_order)[0].block_table(0)
+    oalloc = oracle.BlockAllocator(w.num_blocks, w.block_size, w.free_order)
+    oalloc.new_seq()
+    for i, (out, q, table, T) in enumerate(outs):
+        slot, _ = oalloc.append(0)
+        k, v = W.step_tensors(w, W.Step((0,), i), "cpu")
+        oracle.reshape_and_cache(raw(k), raw(v), kh, vh, np.array([slot]), w.block_size)
+        assert table == oalloc.block_table(0) and T == i + 1
+        bt = np.array([table], dtype=np.int32)
+        want = oracle.decode(q, kh, vh, bt, np.array([T], np.int32), w.softmax_scale, "f32", 8, 8, 64, 16)
+        assert_close(out, want, "f32", f"step {i}")
+    assert np.array_equal(raw(kc), kh) and np.array_equal(raw(vc), vh)
+
+
+def _check_workload(w, sample=None, min_seqs=0):
+    """Run `w` on both sides; compare allocator state, caches and sampled outputs."""
+    kc, vc = _gpu_tensors(w)
+    kh, vh = raw(kc).copy(), raw(vc).copy()
+    alloc, ds = runner.execute(w, kc, vc, _step_kv(w), _query(w))
+    out = ds.decode()
+    torch.cuda.synchronize()
+
+    def step_kv_host(ev):
+        k, v = W.step_tensors(w, ev, DEV)
+        return raw(k), raw(v)
+
+    oalloc, recs = oracle.run_script(w.events, w.num_blocks, w.block_size, w.free_order, kh, vh,
+                                     step_kv=step_kv_host)
+    bt, cl = runner.tables_for(alloc, w.decode_seqs)
+    obt, ocl = oracle.tables_for(oalloc, w.decode_seqs)
+    assert np.array_equal(bt, obt) and np.array_equal(cl, ocl)
+    assert alloc.free_list() == oalloc.free_list()
+    # caches bit-exact after every copy-on-write and append
+    assert np.array_equal(raw(kc), kh) and np.array_equal(raw(vc), vh)
+    seqs = list(range(len(w.decode_seqs))) if sample is None else sample(cl)
+    q = raw(ds.q)
+    want = oracle.decode(q[seqs], kh, vh, obt[seqs], ocl[seqs], w.softmax_scale, w.dtype, w.num_q_heads,
+                         w.num_kv_heads, w.head_dim, w.block_size)
+    assert_close(out[seqs], want, w.dtype, w.name)
+    assert P.pa_device_errors() == 0
+    return out, ds
+
+
+def _sample(k, seed):
+    def pick(cl):
+        rng = np.random.default_rng(seed)
+        longest = int(np.argmax(cl))
+        rest = rng.choice(len(cl), size=min(k, len(cl)), replace=False).tolist()
+        return sorted(set(rest + [longest, int(np.argmin(cl))]))
+    return pick
+
+
+def test_mha_fp16():
+    _check_workload(W.mha_fp16())
+
+
+def test_gqa_bf16():
+    _check_workload(W.gqa_bf16(), sample=_sample(16, 3))
+
+
+@pytest.mark.parametrize("prompt", [1024, 1032])
+def test_shared_prefix_fp16(prompt):
+    _check_workload(W.shared_prefix_fp16(prompt_len=prompt), sample=_sample(24, 4))
+
+
+def test_long_multiturn_bf16():
+    """Full-size pool (~19 GB on the device); oracle on sampled sequences whose
+    blocks are gathered to the host (block permutation invariance is pinned)."""
+    w = W.long_multiturn_bf16()
+    kc, vc = _gpu_tensors(w)
+    alloc, ds = runner.execute(w, kc, vc, _step_kv(w), _query(w))
+    out = ds.decode()
+    torch.cuda.synchronize()
+    oalloc, _ = oracle.run_script(w.events, w.num_blocks, w.block_size, w.free_order)
+    bt, cl = runner.tables_for(alloc, w.decode_seqs)
+    obt, ocl = oracle.tables_for(oalloc, w.decode_seqs)
+    assert np.array_equal(bt, obt) and np.array_equal(cl, ocl)
+    seqs = _sample(30, 5)(cl)
+    used = sorted({int(b) for s in seqs for b in obt[s, :(ocl[s] + w.block_size - 1) // w.block_size]})
+    remap = {b: i for i, b in enumerate(used)}
+    idx = torch.tensor(used, dtype=torch.long, device=DEV)
+    ks, vs = raw(kc.index_select(0, idx)), raw(vc.index_select(0, idx))
+    sbt = np.full((len(seqs), obt.shape[1]), -1, dtype=np.int32)
+    for i, s in enumerate(seqs):
+        n = (ocl[s] + w.block_size - 1) // w.block_size
+        sbt[i, :n] = [remap[int(b)] for b in obt[s, :n]]
+    want = oracle.decode(raw(ds.q)[seqs], ks, vs, sbt, ocl[seqs], w.softmax_scale, "bf16", 32, 8, 128, 32)
+    assert_close(out[seqs], want, "bf16", w.name)
+    # the step's appended rows landed where the oracle's allocator put them
+    k_new, v_new = W.step_tensors(w, w.step_events()[-1], DEV)
+    slots = ds.slots.cpu().numpy()
+    kflat = kc.view(-1, w.num_kv_heads, w.head_dim)
+    assert torch.equal(kflat[torch.from_numpy(slots).to(DEV)], k_new)
+    del kc, vc
+    torch.cuda.empty_cache()
+    assert P.pa_device_errors() == 0

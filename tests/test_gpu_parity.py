@@ -1,0 +1,181 @@
+"""GPU path (through the C ABI) against the fp64 oracle: shapes, edges, cache ops."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_kv_cache_79_gb300 as P
+from tests.gpu_harness import assert_close, raw, small_case
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def run_decode(q, kc, vc, bt, cl, scale, hq, hkv, d, b, part=0):
+    out = torch.empty_like(q, device=DEV)
+    P.pa_decode(out, q.to(DEV), kc.to(DEV), vc.to(DEV), bt.to(DEV), cl.to(DEV), scale, hq, hkv, d, b,
+                partition_size=part)
+    torch.cuda.synchronize()
+    return out
+
+
+def oracle_decode(q, kc, vc, bt, cl, scale, dtype, hq, hkv, d, b):
+    return oracle.decode(raw(q), raw(kc), raw(vc), bt.numpy(), cl.numpy(), scale, dtype, hq, hkv, d, b)
+
+
+SHAPES = []
+for dtype in ("f32", "f16", "bf16"):
+    for D in (64, 128):
+        for B in (16, 32):
+            SHAPES.append((dtype, D, B, 8, 8, [1, B, B + 1, 300], 0))
+            SHAPES.append((dtype, D, B, 8, 2, [0, 5, 4 * B + 3, 1000], 4 * B))
+            SHAPES.append((dtype, D, B, 16, 1, [777, 2, B - 1], B))
+            SHAPES.append((dtype, D, B, 40, 2, [129, 64 * B + 7], 8 * B))
+SHAPES.append(("bf16", 128, 16, 12, 3, [3000, 1, 17, 4096, 2222, 16], 0))
+SHAPES.append(("f16", 128, 16, 5, 5, [1], 0))
+SHAPES.append(("bf16", 128, 32, 64, 8, [2049, 513], 512))
+
+
+@pytest.mark.parametrize("dtype,D,B,Hq,Hkv,lens,part", SHAPES,
+                         ids=lambda v: str(v).replace(" ", ""))
+def test_decode_matches_oracle(dtype, D, B, Hq, Hkv, lens, part):
+    seed = abs(hash((dtype, D, B, Hq, Hkv, tuple(lens), part))) % 10000
+    q, kc, vc, bt, cl = small_case(seed, dtype, D, B, Hq, Hkv, lens)
+    scale = 1.0 / math.sqrt(D)
+    got = run_decode(q, kc, vc, bt, cl, scale, Hq, Hkv, D, B, part)
+    want = oracle_decode(q, kc, vc, bt, cl, scale, dtype, Hq, Hkv, D, B)
+    assert_close(got, want, dtype, f"{dtype} D{D} B{B} G{Hq // Hkv} {lens} part{part}")
+
+
+@pytest.mark.parametrize("dtype", ["f32", "f16", "bf16"])
+def test_single_token_returns_value_row(dtype):
+    q, kc, vc, bt, cl = small_case(5, dtype, 128, 16, 8, 2, [1, 1, 1])
+    got = run_decode(q, kc, vc, bt, cl, 0.3, 8, 2, 128, 16)
+    for s in range(3):
+        for h in range(8):
+            assert torch.equal(got[s, h].cpu(), vc[bt[s, 0], 0, h // 4])
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_empty_context_gives_zeros(dtype):
+    q, kc, vc, bt, cl = small_case(6, dtype, 64, 16, 4, 4, [0, 40, 0])
+    got = run_decode(q, kc, vc, bt, cl, 0.1, 4, 4, 64, 16, part=16)
+    assert torch.count_nonzero(got[0]) == 0 and torch.count_nonzero(got[2]) == 0
+    want = oracle_decode(q, kc, vc, bt, cl, 0.1, dtype, 4, 4, 64, 16)
+    assert_close(got, want, dtype)
+
+
+def test_block_permutation_is_bitwise_invariant():
+    q, kc, vc, bt, cl = small_case(7, "bf16", 128, 16, 16, 4, [900, 33, 400])
+    a = run_decode(q, kc, vc, bt, cl, 0.08, 16, 4, 128, 16, part=256)
+    perm = torch.randperm(kc.shape[0], generator=torch.Generator().manual_seed(1))
+    kc2 = torch.empty_like(kc)
+    vc2 = torch.empty_like(vc)
+    kc2[perm] = kc
+    vc2[perm] = vc
+    bt2 = torch.where(bt >= 0, perm[bt.clamp(min=0).long()].int(), bt)
+    b = run_decode(q, kc2, vc2, bt2, cl, 0.08, 16, 4, 128, 16, part=256)
+    assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "f16"])
+def test_partition_size_changes_only_rounding(dtype):
+    q, kc, vc, bt, cl = small_case(8, dtype, 128, 16, 8, 8, [1500, 700, 31])
+    want = oracle_decode(q, kc, vc, bt, cl, 0.09, dtype, 8, 8, 128, 16)
+    for part in (16, 48, 128, 512, 1504):
+        got = run_decode(q, kc, vc, bt, cl, 0.09, 8, 8, 128, 16, part=part)
+        assert_close(got, want, dtype, f"partition {part}")
+
+
+def test_reblocking_agrees():
+    """The same logical keys stored in blocks of 16 or of 32 give the same result."""
+    rng = np.random.default_rng(9)
+    T, Hkv, D = 333, 2, 128
+    keys = torch.randn(T, Hkv, D).to(torch.float16)
+    vals = torch.randn(T, Hkv, D).to(torch.float16)
+    q = torch.randn(1, 8, D).to(torch.float16)
+    outs = []
+    for B in (16, 32):
+        nb = (T + B - 1) // B
+        perm = torch.from_numpy(rng.permutation(nb + 3)[:nb].astype(np.int32))
+        kc = torch.zeros(nb + 3, B, Hkv, D, dtype=torch.float16)
+        vc = torch.zeros_like(kc)
+        for t in range(T):
+            kc[perm[t // B], t % B] = keys[t]
+            vc[perm[t // B], t % B] = vals[t]
+        outs.append(run_decode(q, kc, vc, perm[None, :], torch.tensor([T], dtype=torch.int32), 0.1, 8,
+                               Hkv, D, B))
+    diff = (outs[0].float() - outs[1].float()).abs().max().item()
+    assert diff <= 2e-3
+
+
+def test_out_of_pool_table_entries_read_zeros():
+    """A table entry outside [0, num_blocks) reads a zero block instead of faulting."""
+    q, kc, vc, bt, cl = small_case(10, "f16", 128, 16, 4, 4, [64], stale=0.0)
+    bad = bt.clone()
+    bad[0, 1] = kc.shape[0] + 5
+    bad[0, 2] = -7
+    got = run_decode(q, kc, vc, bad, cl, 0.1, 4, 4, 128, 16)
+    kz = kc.clone()
+    vz = vc.clone()
+    extra = torch.zeros((2,) + tuple(kc.shape[1:]), dtype=kc.dtype)
+    kz = torch.cat([kz, extra])
+    vz = torch.cat([vz, extra])
+    ref_bt = bad.clone()
+    ref_bt[0, 1] = kc.shape[0]
+    ref_bt[0, 2] = kc.shape[0] + 1
+    want = oracle_decode(q, kz, vz, ref_bt, cl, 0.1, "f16", 4, 4, 128, 16)
+    assert_close(got, want, "f16")
+    assert P.pa_device_errors() == 0
+
+
+def test_context_clamped_to_table_capacity():
+    q, kc, vc, bt, cl = small_case(11, "bf16", 64, 16, 2, 2, [48], width_pad=0)
+    long = cl.clone()
+    long[0] = 10_000
+    a = run_decode(q, kc, vc, bt, long, 0.2, 2, 2, 64, 16)
+    b = run_decode(q, kc, vc, bt, cl, 0.2, 2, 2, 64, 16)
+    assert torch.equal(a, b)
+
+
+# ---------------------------------------------------------------------------
+# cache writes
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("dtype", ["f32", "f16", "bf16"])
+def test_reshape_and_cache_bit_exact(dtype):
+    rng = np.random.default_rng(12)
+    NB, B, Hkv, D, n = 40, 16, 8, 128, 300
+    td = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}[dtype]
+    kc = torch.randn(NB, B, Hkv, D).to(td)
+    vc = torch.randn(NB, B, Hkv, D).to(td)
+    k = torch.randn(n, Hkv, D).to(td)
+    v = torch.randn(n, Hkv, D).to(td)
+    slots = rng.choice(NB * B, size=n, replace=False).astype(np.int64)
+    slots[::7] = -1
+    slots[5] = NB * B + 3          # outside the pool: skipped
+    kg, vg = kc.to(DEV), vc.to(DEV)
+    P.pa_reshape_and_cache(k.to(DEV), v.to(DEV), kg, vg, torch.from_numpy(slots).to(DEV))
+    kh, vh = raw(kc).copy(), raw(vc).copy()
+    s_ok = np.where(slots < NB * B, slots, -1)
+    oracle.reshape_and_cache(raw(k), raw(v), kh, vh, s_ok, B)
+    assert np.array_equal(raw(kg), kh) and np.array_equal(raw(vg), vh)
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16", "f32"])
+def test_copy_blocks_bit_exact(dtype):
+    NB, B, Hkv, D = 64, 16, 40, 128
+    td = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}[dtype]
+    kc = torch.randn(NB, B, Hkv, D).to(td)
+    vc = torch.randn(NB, B, Hkv, D).to(td)
+    pairs = [(3, 10), (4, 11), (60, 0), (7, 63), (70, 1), (2, -1)]   # the last two are skipped
+    kg, vg = kc.to(DEV), vc.to(DEV)
+    P.pa_copy_blocks(kg, vg, torch.tensor(pairs, dtype=torch.int32, device=DEV))
+    kh, vh = raw(kc).copy(), raw(vc).copy()
+    oracle.copy_blocks(kh, vh, pairs[:4])
+    assert np.array_equal(raw(kg), kh) and np.array_equal(raw(vg), vh)
+
+
+def test_no_device_errors_raised():
+    assert P.pa_device_errors() == 0

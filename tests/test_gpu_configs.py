@@ -48,7 +48,7 @@ def test_tiny_fifty_appends_each_decoded():
     oalloc.new_seq()
     for i, (out, q, table, T) in enumerate(outs):
         slot, _ = oalloc.append(0)
-        k, v = W.step_tensors(w, W.Step((0,), i), "cpu")
+        k, v = W.step_tensors(w, W.Step((0,), i), DEV)
         oracle.reshape_and_cache(raw(k), raw(v), kh, vh, np.array([slot]), w.block_size)
         assert table == oalloc.block_table(0) and T == i + 1
         bt = np.array([table], dtype=np.int32)

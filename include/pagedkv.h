@@ -128,6 +128,37 @@ int pa_decode_partition_size(int num_seqs, int num_q_heads, int num_kv_heads, in
 size_t pa_decode_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
                                 int block_size, int max_blocks_per_seq, int partition_size);
 
+/*
+ * pa_decode_noalloc -- pa_decode for callers that cannot allocate device memory.
+ *
+ * The pages have no counterpart: this is a deployment variant of pa_decode, with
+ * the same arguments, the same result and the same kernels, minus the workspace.
+ * It is for callers that may not allocate device memory on their hot path, such as
+ * a plugin of an inference engine that has planned every buffer up front, an
+ * embedded runtime with a fixed memory budget, or a C caller with no device
+ * allocator (cudaMalloc can synchronise the device).  The split-KV scratch is a
+ * fixed device array inside the library, PA_DECODE_NOALLOC_SCRATCH_BYTES long,
+ * which every GPU that loads the library keeps until the process exits.
+ *
+ *   - Sizes whose scratch (pa_decode_workspace_size) exceeds the array are
+ *     rejected with PA_ERR_UNSUPPORTED before anything is enqueued; use pa_decode
+ *     with a caller workspace (or a larger partition_size) for those.
+ *   - The first call on each device, with that device current, looks up the
+ *     array's device address (cudaGetSymbolAddress); make that first call before
+ *     any stream capture.
+ *   - Every call shares the one array and it keeps the last call's contents.
+ *     Nothing in it needs to start at zero.  Calls whose work overlaps on the GPU
+ *     (different streams, or several host threads) race on it: serialise them.
+ *   - It never calls cudaMalloc, cudaFree or an allocating library routine.
+ * Errors: as pa_decode, plus PA_ERR_UNSUPPORTED for sizes beyond the array.
+ */
+#define PA_DECODE_NOALLOC_SCRATCH_BYTES (64u << 20)
+pa_status pa_decode_noalloc(void *out, const void *q, const void *k_cache, const void *v_cache,
+                            const int32_t *block_tables, int max_blocks_per_seq,
+                            const int32_t *context_lens, int num_seqs, int num_blocks,
+                            float scale, int num_q_heads, int num_kv_heads, int head_dim,
+                            int block_size, pa_dtype dtype, int partition_size, void *stream);
+
 /* ------------------------------------------------------------------------- *
  * Cache writes.                                                              *
  * ------------------------------------------------------------------------- */

@@ -117,6 +117,26 @@ def pa_decode(out, q, k_cache, v_cache, block_tables, context_lens, scale: float
     return out
 
 
+def pa_decode_noalloc(out, q, k_cache, v_cache, block_tables, context_lens, scale: float,
+                      num_q_heads: int, num_kv_heads: int, head_dim: int, block_size: int,
+                      partition_size: int = 0, stream=None):
+    """pa_decode for callers that cannot allocate device memory: the split-KV
+    scratch is the library's fixed device array (PA_DECODE_NOALLOC_SCRATCH_BYTES,
+    shared by every call; calls overlapping on the GPU race).  Sizes needing more
+    scratch raise PagedKVError (PA_ERR_UNSUPPORTED)."""
+    import torch
+    if block_tables.dtype != torch.int32 or context_lens.dtype != torch.int32:
+        raise TypeError("block_tables and context_lens must be int32")
+    st = _load().pa_decode_noalloc(_cuda(out, "out"), _cuda(q, "q"), _cuda(k_cache, "k_cache"),
+                                   _cuda(v_cache, "v_cache"), _cuda(block_tables, "block_tables"),
+                                   block_tables.shape[1], _cuda(context_lens, "context_lens"),
+                                   q.shape[0], k_cache.shape[0], float(scale), num_q_heads,
+                                   num_kv_heads, head_dim, block_size, _dtype_code(q), partition_size,
+                                   _stream(stream))
+    _check(st, "pa_decode_noalloc")
+    return out
+
+
 # ----------------------------------------------------------------------------
 # cache writes
 # ----------------------------------------------------------------------------
@@ -248,6 +268,6 @@ class BlockAllocator:
         return out[:n.value].tolist()
 
 
-__all__ = ["pa_decode", "pa_decode_workspace_size", "pa_decode_partition_size", "alloc_workspace",
+__all__ = ["pa_decode", "pa_decode_noalloc", "pa_decode_workspace_size", "pa_decode_partition_size", "alloc_workspace",
            "pa_reshape_and_cache", "pa_copy_blocks", "pa_device_errors", "pa_status_string",
            "BlockAllocator", "PagedKVError", "OutOfBlocks", "library_path"]

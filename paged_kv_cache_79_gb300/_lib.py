@@ -22,6 +22,9 @@ SIGNATURES = {
     "pa_decode": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_void_p, c_int,
                           c_int, c_float, c_int, c_int, c_int, c_int, c_int, c_int, c_void_p,
                           c_size_t, c_void_p]),
+    "pa_decode_noalloc": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_void_p,
+                                  c_int, c_int, c_float, c_int, c_int, c_int, c_int, c_int, c_int,
+                                  c_void_p]),
     "pa_decode_partition_size": (c_int, [c_int] * 7),
     "pa_decode_workspace_size": (c_size_t, [c_int] * 7),
     "pa_reshape_and_cache": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_int,

@@ -139,6 +139,8 @@ int resolve_partition(int num_seqs, int Hq, int Hkv, int B, int max_blocks, int 
 
 }  // namespace
 
+void note_cuda_error(cudaError_t e) { cuda_fail(e); }
+
 int sm_count(int device)
 {
     std::lock_guard<std::mutex> lk(g_mu);

@@ -69,6 +69,10 @@ int cached_occupancy(void *kernel, int device, size_t smem, size_t max_smem);
 // Number of SMs of `device` (cached).
 int sm_count(int device);
 
+// Record `e` as this thread's last CUDA error (read by pa_last_cuda_error) and
+// clear the runtime's sticky launch error.
+void note_cuda_error(cudaError_t e);
+
 cudaError_t launch_reshape_and_cache(const void *k, const void *v, void *k_cache, void *v_cache,
                                      const int64_t *slots, int num_tokens, size_t row_bytes,
                                      long long num_slots, cudaStream_t stream);

@@ -239,8 +239,9 @@ def run_ours(args):
     import paged_kv_cache_79_gb300 as P
     parts = P.pa_decode_partition_size(S, w.num_q_heads, w.num_kv_heads, w.head_dim, w.block_size,
                                        bt.shape[1], w.partition_size)
-    max_parts = -(-bt.shape[1] // (parts // w.block_size))
-    launches_per_step = (1 if n_pairs else 0) + (1 if n_tok else 0) + 1 + (1 if max_parts > 1 else 0)
+    # balanced split (0): partition + merge kernels; fixed: merge only if a table spans partitions
+    merge = parts == 0 or -(-bt.shape[1] // (parts // w.block_size)) > 1
+    launches_per_step = (1 if n_pairs else 0) + (1 if n_tok else 0) + 1 + (1 if merge else 0)
 
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
@@ -305,7 +306,9 @@ def run_ours(args):
         "config": {"workload": w.name, "num_seqs": S, "num_q_heads": w.num_q_heads,
                    "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim, "block_size": w.block_size,
                    "num_blocks": w.num_blocks, "context_tokens": int(np.sum(cl)),
-                   "max_context": int(np.max(cl)), "partition_size": parts, "appended_tokens": n_tok,
+                   "max_context": int(np.max(cl)),
+                   "split": "balanced" if parts == 0 else f"fixed partitions of {parts} tokens",
+                   "appended_tokens": n_tok,
                    "cow_pairs": n_pairs, "l2": "flushed (512 MB write) before every timed step",
                    "parallelism": f"replica x{world} (independent batches)"},
         "seq_layers_per_s": round(world * S / (t_step * 1e-3), 1),

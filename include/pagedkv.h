@@ -83,10 +83,14 @@ int pa_last_cuda_error(void);
  * row ([T] §3.2 returns zeros for an empty sequence).  Context lengths are clamped
  * to [0, max_blocks_per_seq * block_size].
  *
- * Long contexts are split into partitions of `partition_size` tokens processed by
- * separate CTAs; their partial (max, exp-sum, weighted V) results are merged by a
- * second kernel with the same rule.  partition_size = 0 lets the library choose;
- * otherwise it must be a positive multiple of block_size.
+ * Long contexts are split so that several CTAs share one sequence; their partial
+ * (max, exp-sum, weighted V) results are merged by a second kernel with the same
+ * rule.  partition_size selects the split:
+ *   0      balanced split: the K/V of all (sequence, kv head) pairs is cut into
+ *          equal shares, one per CTA of a persistent grid, so every CTA streams the
+ *          same number of bytes whatever the length mix;
+ *   > 0    fixed partitions of partition_size tokens (a multiple of block_size).
+ * Both give the same result up to fp32 rounding order.
  *
  * Arguments
  *   out            device, [S][Hq][d], dtype `dtype`, written
@@ -113,17 +117,20 @@ pa_status pa_decode(void *out, const void *q, const void *k_cache, const void *v
                     size_t workspace_bytes, void *stream);
 
 /*
- * Partition size pa_decode uses for these arguments (resolves partition_size = 0
- * on the current device).  Returns 0 for invalid arguments.
+ * Partition size pa_decode uses for these arguments: 0 for the balanced split,
+ * else the fixed partition size (capped at the table capacity).  Returns -1 for
+ * invalid arguments.
  */
 int pa_decode_partition_size(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
                              int block_size, int max_blocks_per_seq, int partition_size);
 
 /*
- * Bytes of workspace pa_decode needs for these arguments (0 when every sequence
- * fits one partition).  Layout: fp32 partial outputs [S][P][Hq][d] followed by
- * fp32 partial log2-sum-exp values [S][P][Hq], P = ceil(max_blocks_per_seq *
- * block_size / partition).  Returns (size_t)-1 for invalid arguments.
+ * Bytes of workspace pa_decode needs for these arguments.  Fixed partitions: 0
+ * when one partition covers the table, else fp32 partial outputs [S][P][Hq][d]
+ * (256-byte aligned end) followed by fp32 log2-sum-exp values [S][P][Hq], P =
+ * ceil(max_blocks_per_seq * block_size / partition_size).  Balanced split: the
+ * same two arrays with 2 * 4 * (SMs of the current device) * 16 rows, whatever the
+ * lengths.  Returns (size_t)-1 for invalid arguments.
  */
 size_t pa_decode_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
                                 int block_size, int max_blocks_per_seq, int partition_size);

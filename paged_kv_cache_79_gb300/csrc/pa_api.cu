@@ -9,6 +9,10 @@
 
 #include "pa_internal.h"
 
+#ifndef PA_L2_PROMOTION
+#define PA_L2_PROMOTION CU_TENSOR_MAP_L2_PROMOTION_L2_256B
+#endif
+
 namespace pagedkv {
 
 namespace {
@@ -94,7 +98,7 @@ bool make_cache_map(CUtensorMap *map, const void *base, pa_dtype dt, int num_blo
                                                    : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
     const CUresult r = enc(map, tdt, 4, const_cast<void *>(base), dims, strides, box, estr,
                            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                           (CUtensorMapL2promotion)PA_L2_PROMOTION, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
 
@@ -114,27 +118,25 @@ bool decode_shape_ok(int num_seqs, int Hq, int Hkv, int D, int B, int max_blocks
     return true;
 }
 
-int resolve_partition(int num_seqs, int Hq, int Hkv, int B, int max_blocks, int part, int sms)
+// Fixed partitions: a partition size at least as long as the table means one
+// partition per sequence.
+int resolve_partition(int B, int max_blocks, int part)
 {
     const long long max_ctx = (long long)max_blocks * B;
-    if (part > 0)
-        return part;
-    // Auto: aim for ~8 work items per resident CTA (2 per SM) assuming contexts
-    // average half the table capacity; never below 8 blocks, never above 1024
-    // tokens; one partition when the whole table fits.
-    const long long groups = (Hq / Hkv + kHeadsPerItem - 1) / kHeadsPerItem;
-    const long long units = (long long)num_seqs * Hkv * groups;
-    const long long target = 8ll * 2 * (sms > 0 ? sms : 148);
-    long long p = units > 0 ? (units * (max_ctx / 2)) / target : max_ctx;
-    const long long lo = 8ll * B, hi = 1024;
-    if (p < lo)
-        p = lo;
-    if (p > hi)
-        p = hi;
-    p = (p / B) * B;
-    if (p >= max_ctx)
-        p = ((max_ctx + B - 1) / B) * B;
-    return (int)p;
+    return part >= max_ctx ? (int)(((max_ctx + B - 1) / B) * B) : part;
+}
+
+// Balanced split: partial rows reserved for 2 slots x 16 query heads per CTA.
+size_t balanced_rows(int sms) { return (size_t)2 * kMaxCtasPerSm * (size_t)sms * kHeadsPerItem; }
+
+int current_sms()
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    return sm_count(dev);
 }
 
 }  // namespace
@@ -207,15 +209,8 @@ int pa_decode_partition_size(int num_seqs, int num_q_heads, int num_kv_heads, in
 {
     if (!decode_shape_ok(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
                          max_blocks_per_seq, partition_size))
-        return 0;
-    int dev = 0;
-    int sms = 0;
-    if (cudaGetDevice(&dev) == cudaSuccess)
-        sms = sm_count(dev);
-    else
-        cudaGetLastError();
-    return resolve_partition(num_seqs, num_q_heads, num_kv_heads, block_size, max_blocks_per_seq,
-                             partition_size, sms);
+        return -1;
+    return partition_size == 0 ? 0 : resolve_partition(block_size, max_blocks_per_seq, partition_size);
 }
 
 size_t pa_decode_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
@@ -223,8 +218,13 @@ size_t pa_decode_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads,
 {
     const int part = pa_decode_partition_size(num_seqs, num_q_heads, num_kv_heads, head_dim,
                                               block_size, max_blocks_per_seq, partition_size);
-    if (part <= 0)
+    if (part < 0)
         return (size_t)-1;
+    if (part == 0) {
+        const int sms = current_sms();
+        const size_t rows = balanced_rows(sms > 0 ? sms : 160);
+        return ((rows * (size_t)head_dim * 4 + 255) & ~size_t(255)) + rows * 4;
+    }
     const long long pb = part / block_size;
     const long long parts = (max_blocks_per_seq + pb - 1) / pb;
     if (parts <= 1)
@@ -270,10 +270,10 @@ pa_status pa_decode(void *out, const void *q, const void *k_cache, const void *v
     if (sms <= 0)
         return cuda_fail(cudaErrorNoDevice);
 
-    const int part = resolve_partition(num_seqs, num_q_heads, num_kv_heads, block_size,
-                                       max_blocks_per_seq, partition_size, sms);
-    const int pb = part / block_size;
-    const int parts = (max_blocks_per_seq + pb - 1) / pb;
+    const bool balanced = partition_size == 0;
+    const int part = balanced ? 0 : resolve_partition(block_size, max_blocks_per_seq, partition_size);
+    const int pb = balanced ? max_blocks_per_seq : part / block_size;
+    const int parts = balanced ? 1 : (max_blocks_per_seq + pb - 1) / pb;
     const size_t need = pa_decode_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim,
                                                  block_size, max_blocks_per_seq, partition_size);
     if (need == (size_t)-1)
@@ -288,8 +288,9 @@ pa_status pa_decode(void *out, const void *q, const void *k_cache, const void *v
     p.q = q;
     p.block_tables = block_tables;
     p.context_lens = context_lens;
-    if (parts > 1) {
-        const size_t rows = (size_t)num_seqs * parts * num_q_heads;
+    if (balanced || parts > 1) {
+        const size_t rows =
+            balanced ? balanced_rows(sms) : (size_t)num_seqs * parts * num_q_heads;
         p.part_o = static_cast<float *>(workspace);
         p.part_lse = reinterpret_cast<float *>(static_cast<char *>(workspace) +
                                                ((rows * head_dim * 4 + 255) & ~size_t(255)));
@@ -307,10 +308,15 @@ pa_status pa_decode(void *out, const void *q, const void *k_cache, const void *v
     p.head_groups = (p.group + kHeadsPerItem - 1) / kHeadsPerItem;
     p.partition_blocks = pb;
     p.max_parts = parts;
+    p.balanced = balanced ? 1 : 0;
     L.head_dim = head_dim;
     L.block_size = block_size;
     L.sm_count = sms;
+#ifdef PA_FORCE_GRID
+    L.grid = PA_FORCE_GRID;
+#else
     L.grid = 0;
+#endif
     if (!make_cache_map(&L.tmap_k, k_cache, dtype, num_blocks, block_size, num_kv_heads, head_dim) ||
         !make_cache_map(&L.tmap_v, v_cache, dtype, num_blocks, block_size, num_kv_heads, head_dim))
         return cuda_fail(cudaErrorInvalidValue);

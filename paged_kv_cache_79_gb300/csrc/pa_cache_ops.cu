@@ -6,6 +6,7 @@
 // the copy half of copy-on-write ("Efficient Memory Management for LLM Serving with
 // PagedAttention", azimuth.plus summary, section "Memory sharing").  Both are plain
 // 16-byte vector copies: the cost is launch latency and HBM bytes.
+#include "pa_device.cuh"
 #include "pa_internal.h"
 
 namespace pagedkv {
@@ -19,6 +20,8 @@ __global__ void __launch_bounds__(128)
                              uint4 *__restrict__ k_cache, uint4 *__restrict__ v_cache,
                              const int64_t *__restrict__ slots, int vec_per_row, long long num_slots)
 {
+    dev::grid_dependency_wait();  // the cache and the inputs may come from the previous kernel
+    dev::grid_launch_dependents();
     const int t = blockIdx.x;
     const int64_t slot = slots[t];
     if (slot < 0 || slot >= num_slots)
@@ -37,6 +40,8 @@ __global__ void __launch_bounds__(kCopyThreads)
     copy_blocks_kernel(uint4 *__restrict__ k_cache, uint4 *__restrict__ v_cache,
                        const int32_t *__restrict__ pairs, int num_blocks, long long vec_per_block)
 {
+    dev::grid_dependency_wait();
+    dev::grid_launch_dependents();
     const int src = pairs[2 * blockIdx.x];
     const int dst = pairs[2 * blockIdx.x + 1];
     if (src < 0 || src >= num_blocks || dst < 0 || dst >= num_blocks)
@@ -68,10 +73,22 @@ cudaError_t launch_reshape_and_cache(const void *k, const void *v, void *k_cache
 {
     const int vec = (int)(row_bytes / 16);
     const int threads = vec >= 128 ? 128 : (vec >= 64 ? 64 : 32);
-    reshape_and_cache_kernel<<<dim3((unsigned)num_tokens, 2), threads, 0, stream>>>(
-        static_cast<const uint4 *>(k), static_cast<const uint4 *>(v), static_cast<uint4 *>(k_cache),
-        static_cast<uint4 *>(v_cache), slots, vec, num_slots);
-    return cudaGetLastError();
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    #ifdef PA_NO_PDL
+    attr[0].val.programmaticStreamSerializationAllowed = 0;
+#else
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+#endif
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)num_tokens, 2);
+    cfg.blockDim = dim3(threads);
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, reshape_and_cache_kernel, static_cast<const uint4 *>(k),
+                              static_cast<const uint4 *>(v), static_cast<uint4 *>(k_cache),
+                              static_cast<uint4 *>(v_cache), slots, vec, num_slots);
 }
 
 cudaError_t launch_copy_blocks(void *k_cache, void *v_cache, const int32_t *pairs, int num_pairs,
@@ -80,9 +97,21 @@ cudaError_t launch_copy_blocks(void *k_cache, void *v_cache, const int32_t *pair
     const long long vec = (long long)(block_bytes / 16);
     const long long per_cta = (long long)kCopyThreads * kCopyUnroll;
     const unsigned z = (unsigned)((vec + per_cta - 1) / per_cta);
-    copy_blocks_kernel<<<dim3((unsigned)num_pairs, 2, z), kCopyThreads, 0, stream>>>(
-        static_cast<uint4 *>(k_cache), static_cast<uint4 *>(v_cache), pairs, num_blocks, vec);
-    return cudaGetLastError();
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    #ifdef PA_NO_PDL
+    attr[0].val.programmaticStreamSerializationAllowed = 0;
+#else
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+#endif
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)num_pairs, 2, z);
+    cfg.blockDim = dim3(kCopyThreads);
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, copy_blocks_kernel, static_cast<uint4 *>(k_cache),
+                              static_cast<uint4 *>(v_cache), pairs, num_blocks, vec);
 }
 
 }  // namespace pagedkv

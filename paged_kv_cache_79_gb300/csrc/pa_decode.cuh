@@ -8,17 +8,25 @@
 // the section "Inside: block-table lookup").  The same rule merges the partial
 // results of the split-KV partitions in pa_merge_kernel.
 //
-// Work decomposition.  A work item is (sequence, partition of `partition_blocks`
-// blocks, kv head, group of <= 16 query heads sharing that kv head).  A persistent
-// grid of CTAs walks the items with a static stride.  Per CTA:
+// Work decomposition.  A unit is (sequence, kv head, group of <= 16 query heads
+// sharing that kv head); a work item is a range of a unit's blocks.  A persistent
+// grid of CTAs takes the items in one of two ways:
+//   balanced split (partition_size 0): the units' K/V streams are concatenated and
+//               each CTA takes an equal contiguous range of ring stages, so every CTA
+//               moves the same number of bytes; a unit cut by CTA boundaries leaves
+//               partials that pa_merge_balanced_kernel combines;
+//   fixed partitions (partition_size > 0): units are cut every partition_size
+//               tokens and CTA c takes items c, c + grid, ...; pa_merge_kernel
+//               combines the partitions of multi-partition sequences.
+// Per CTA:
 //   warp 4      producer: reads the block table of the item, and for every block
 //               issues TMA tile loads of K and V (box = head_dim x block_size of one
 //               kv head, 128-byte swizzle) into a ring of shared-memory stages;
 //   warps 0..3  consumers: block g of the CTA's stream goes to warp g % 4; each
 //               keeps an online-softmax state (max, exp-sum, weighted V) per query
 //               head; at the end of an item the four states are merged through
-//               shared memory and written as the final output (single-partition
-//               sequence) or as a partial (fp32 output + log2-sum-exp).
+//               shared memory and written as the final output (the item is a whole
+//               unit) or as a partial (fp32 output + log2-sum-exp).
 // For fp16/bf16 the consumers use mma.sync.m16n8k16 with fp32 accumulation:
 // S[16 heads x 8 tokens] = Q K^T, then O[16 heads x 8 dims] += P V, P kept in
 // registers (the C fragment of Q K^T is the A fragment of P V).  For fp32 they use
@@ -32,26 +40,82 @@
 
 namespace pagedkv {
 
+#ifndef PA_STAGE_TOKENS
+#define PA_STAGE_TOKENS 32  // tokens per ring stage (fp16/bf16): blocks of 16 go two per stage
+#endif
+#ifndef PA_ITEM_ORDER
+#define PA_ITEM_ORDER 0
+#endif
+#ifndef PA_RING_BYTES
+#define PA_RING_BYTES 65536  // shared memory of the stage ring (two CTAs per SM)
+#endif
+
+// A ring stage holds the K and V tiles of kBPS consecutive blocks of one item
+// (kStageTokens token rows of one kv head); the consumer treats it as one tile.
 template <typename T, int D, int BS>
 struct Cfg {
     static constexpr int kElem = (int)sizeof(T);
     static constexpr int kChunkElems = 128 / kElem;  // elements in one 128-byte swizzle row
-    static constexpr int kChunks = D / kChunkElems;  // TMA boxes per tile
-    static constexpr int kTileBytes = BS * D * kElem;
+    static constexpr int kChunks = D / kChunkElems;  // TMA boxes per block tile
+    static constexpr int kStageTokens =
+        (sizeof(T) == 4 || PA_STAGE_TOKENS <= BS) ? BS : PA_STAGE_TOKENS;
+    static constexpr int kBPS = kStageTokens / BS;   // blocks per stage
+    static constexpr int kTileBytes = kStageTokens * D * kElem;  // K (or V) of one stage
     static constexpr int kStageBytes = 2 * kTileBytes;
-    static constexpr int kStages = (kStageBytes <= 8192) ? 8 : 4;
+    static constexpr int kStagesRaw = (PA_RING_BYTES / kStageBytes) / kConsumerWarps * kConsumerWarps;
+    static constexpr int kStages = kStagesRaw < kConsumerWarps ? kConsumerWarps : kStagesRaw;
     static_assert(kStages % kConsumerWarps == 0, "stages must split evenly over consumers");
     static_assert(D % kChunkElems == 0, "head_dim must be a whole number of 128-byte rows");
+    static_assert(kStageTokens % BS == 0 && 32 % kBPS == 0, "a stage is a whole number of blocks");
 };
 
 constexpr int kAccPad = 8;  // floats of padding per merge row (spreads banks)
 
+// Debug builds (-DPA_TRACE) record per-CTA timestamps (ns) and counters into a
+// device array read back with pa_debug_trace_<dtype>; normal builds compile the
+// hooks away.
+#ifdef PA_TRACE
+constexpr int kTraceSlots = 16;
+constexpr int kTraceCtas = 4096;
+static __device__ unsigned long long g_trace[kTraceCtas * kTraceSlots];
+__device__ __forceinline__ void trace_set(int slot, unsigned long long v)
+{
+    if (blockIdx.x < kTraceCtas)
+        g_trace[blockIdx.x * kTraceSlots + slot] = v;
+}
+__device__ __forceinline__ void trace_add(int slot, unsigned long long v)
+{
+    if (blockIdx.x < kTraceCtas)
+        g_trace[blockIdx.x * kTraceSlots + slot] += v;
+}
+#define PA_TRACE_SET(slot, v) trace_set((slot), (v))
+#define PA_TRACE_ADD(slot, v) trace_add((slot), (v))
+#define PA_TRACE_DEFINE_READER(name)                                                     \
+    extern "C" int pa_debug_trace_##name(unsigned long long *host, int n, int clear)      \
+    {                                                                                   \
+        int e = (int)cudaMemcpyFromSymbol(host, pagedkv::g_trace, (size_t)n * 8);        \
+        if (clear) {                                                                    \
+            static unsigned long long zeros[pagedkv::kTraceCtas * pagedkv::kTraceSlots]; \
+            cudaMemcpyToSymbol(pagedkv::g_trace, zeros, sizeof zeros);                  \
+        }                                                                               \
+        return e;                                                                       \
+    }
+#else
+#define PA_TRACE_SET(slot, v)
+#define PA_TRACE_ADD(slot, v)
+#define PA_TRACE_DEFINE_READER(name)
+#endif
+
 struct SmemLayout {
-    uint32_t acc, ml, q, bars, flag, total;
+    uint32_t acc, ml, items, q, bars, flag, total;
 };
 
+constexpr int kItemSlots = 2;  // work-item descriptors (and their query rows) in flight
+
+// Shared memory: stage ring | merge accumulators | merge (max, sum) | item
+// descriptors | query rows per item slot | mbarriers | abort flag.
 __host__ __device__ inline SmemLayout make_layout(int stages, int stage_bytes, int rows, int D,
-                                                  bool q_in_smem)
+                                                  int elem_bytes)
 {
     SmemLayout L;
     uint32_t o = (uint32_t)stages * (uint32_t)stage_bytes;
@@ -59,14 +123,16 @@ __host__ __device__ inline SmemLayout make_layout(int stages, int stage_bytes, i
     o += (uint32_t)(kConsumerWarps * rows * (D + kAccPad) * 4);
     L.ml = o;
     o += kConsumerWarps * kHeadsPerItem * 2 * 4;
+    o = (o + 127u) & ~127u;
+    L.items = o;
+    o += kItemSlots * 64u;
     L.q = o;
-    if (q_in_smem)
-        o += (uint32_t)(kConsumerWarps * kHeadsPerItem * D * 4);
+    o += (uint32_t)(kItemSlots * kHeadsPerItem * D * elem_bytes);
     o = (o + 15u) & ~15u;
     L.bars = o;
-    o += 2u * (uint32_t)stages * 8u;
-    L.flag = o;
-    o += 16u;
+    o += (2u * (uint32_t)stages + 2u * kItemSlots + 1u) * 8u;
+    L.flag = o;  // abort flag, then one scratch word per consumer warp
+    o += 16u + 4u * kConsumerWarps;
     L.total = o + 1024u;  // slack to align the base to 1024 bytes (128-byte swizzle)
     return L;
 }
@@ -116,8 +182,12 @@ __device__ __forceinline__ bool find_item(const DecodeParams &p, int bs, long lo
 }
 
 struct Item {
-    int seq, part, kvh, hg, len, j0, j1, qrow0, rows;
-    bool single;
+    int seq, kvh, hg, len;  // unit and its context length
+    int j0, j1;             // blocks [j0, j1) of the unit
+    int qrow0, rows;        // query heads qrow0 .. qrow0 + rows - 1
+    int partial;            // 0: write the output; 1: write partial row prow0 + r
+    int prow0;
+    int pad[6];             // 64 bytes: one shared-memory descriptor slot
 };
 
 __device__ __forceinline__ Item decode_item(const DecodeParams &p, int bs, long long w, int seq,
@@ -127,86 +197,440 @@ __device__ __forceinline__ Item decode_item(const DecodeParams &p, int bs, long 
     const long long units = (long long)p.num_kv_heads * p.head_groups;
     const long long rem = w - base;
     it.seq = seq;
-    it.part = (int)(rem / units);
+#if PA_ITEM_ORDER == 1
+    // the partitions of one (kv head, head group) are adjacent
+    const int np_seq = num_parts(p, seq, bs);
+    const int part = (int)(rem % np_seq);
+    const int u = (int)(rem / np_seq);
+#else
+    // the kv heads of one partition are adjacent (they share DRAM pages)
+    const int part = (int)(rem / units);
     const int u = (int)(rem % units);
+#endif
     it.kvh = u / p.head_groups;
     it.hg = u % p.head_groups;
     it.len = clamp_len(p, seq, bs);
     const int nb = (it.len + bs - 1) / bs;
-    it.j0 = it.part * p.partition_blocks;
+    it.j0 = part * p.partition_blocks;
     it.j1 = min(nb, it.j0 + p.partition_blocks);
     it.qrow0 = it.kvh * p.group + it.hg * kHeadsPerItem;
     it.rows = min(kHeadsPerItem, p.group - it.hg * kHeadsPerItem);
-    it.single = num_parts(p, seq, bs) == 1;
+    it.partial = num_parts(p, seq, bs) == 1 ? 0 : 1;
+    it.prow0 = (int)(((long long)seq * p.max_parts + part) * p.num_q_heads + it.qrow0);
     return it;
 }
 
 // ---------------------------------------------------------------------------
-// Producer warp: block-table lookup and TMA tile loads into the stage ring.
+// Per-CTA shared state.
 // ---------------------------------------------------------------------------
-template <int D, int BS, int kChunks, int kTileBytes, int kStages>
-__device__ __forceinline__ void producer_loop(const DecodeParams &p, const CUtensorMap *tk,
-                                              const CUtensorMap *tv, uint8_t *ring,
-                                              uint64_t *full, uint64_t *empty, volatile int *abort,
-                                              int lane)
+struct CtaState {
+    uint8_t *ring;
+    float *macc;
+    float *mml;
+    Item *items;
+    uint8_t *qslots;
+    uint64_t *full, *empty;            // per ring stage
+    uint64_t *item_full, *item_empty;  // per item slot
+    uint64_t *csync;                   // consumer-only barrier (all consumer threads arrive)
+    volatile int *abort;
+    volatile uint32_t *sink;           // per consumer warp: see dev::settle_loads
+};
+
+__device__ __forceinline__ CtaState cta_state(uint8_t *smem, const SmemLayout &lay, int stages)
 {
-    if (lane == 0) {
-        dev::tma_prefetch_desc(tk);
-        dev::tma_prefetch_desc(tv);
+    CtaState c;
+    c.ring = smem;
+    c.macc = reinterpret_cast<float *>(smem + lay.acc);
+    c.mml = reinterpret_cast<float *>(smem + lay.ml);
+    c.items = reinterpret_cast<Item *>(smem + lay.items);
+    c.qslots = smem + lay.q;
+    c.full = reinterpret_cast<uint64_t *>(smem + lay.bars);
+    c.empty = c.full + stages;
+    c.item_full = c.empty + stages;
+    c.item_empty = c.item_full + kItemSlots;
+    c.csync = c.item_empty + kItemSlots;
+    c.abort = reinterpret_cast<volatile int *>(smem + lay.flag);
+    c.sink = reinterpret_cast<volatile uint32_t *>(smem + lay.flag + 16);
+    return c;
+}
+
+__device__ __forceinline__ void init_cta(const CtaState &c, int stages)
+{
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < stages; ++s) {
+            dev::mbar_init(dev::smem_addr(&c.full[s]), 1);
+            dev::mbar_init(dev::smem_addr(&c.empty[s]), 1);
+        }
+        for (int i = 0; i < kItemSlots; ++i) {
+            dev::mbar_init(dev::smem_addr(&c.item_full[i]), 1);
+            dev::mbar_init(dev::smem_addr(&c.item_empty[i]), kConsumerWarps);
+        }
+        dev::mbar_init(dev::smem_addr(c.csync), 32 * kConsumerWarps);
+        *c.abort = 0;
+        dev::fence_mbar_init();
     }
-    int seq = 0;
-    long long base = 0;
-    uint32_t g = 0;
-    bool failed = false;
-    for (long long w = blockIdx.x; !failed; w += gridDim.x) {
-        if (!find_item(p, BS, w, seq, base, lane) || *abort)
-            break;
-        const Item it = decode_item(p, BS, w, seq, base);
+    __syncthreads();
+    // Everything read below may be produced by the previous kernel in the stream.
+    dev::grid_dependency_wait();
+    dev::grid_launch_dependents();
+}
+
+// Copy a descriptor out of its slot.  The volatile reads happen here and only here:
+// once the slot is released the producer may overwrite it with a later item, so
+// the compiler must not re-read fields from shared memory afterwards.
+__device__ __forceinline__ Item load_item(const Item *slot)
+{
+    const volatile int *v = reinterpret_cast<const volatile int *>(slot);
+    Item it;
+    it.seq = v[0];
+    it.kvh = v[1];
+    it.hg = v[2];
+    it.len = v[3];
+    it.j0 = v[4];
+    it.j1 = v[5];
+    it.qrow0 = v[6];
+    it.rows = v[7];
+    it.partial = v[8];
+    it.prow0 = v[9];
+    return it;
+}
+
+__device__ __forceinline__ void raise_error(const DecodeParams &p, volatile int *abort,
+                                            unsigned int flag)
+{
+    atomicOr(p.errors, flag);
+    *abort = 1;
+}
+
+// Bounded wait on an mbarrier phase by every lane of a warp; warp-uniform result.
+__device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity)
+{
+    const bool ok = dev::mbar_wait(dev::smem_addr(bar), parity, kWaitTimeoutNs);
+    return __all_sync(0xffffffffu, ok);
+}
+
+// Barrier among the consumer warps only (the producer runs ahead), bounded.
+__device__ __forceinline__ bool consumer_sync(const CtaState &c, uint32_t &phase)
+{
+    dev::mbar_arrive(dev::smem_addr(c.csync));
+    const bool ok = warp_wait(c.csync, phase & 1u);
+    ++phase;
+    return ok;
+}
+
+// ---------------------------------------------------------------------------
+// Producer warp: walks the work items, publishes each item's descriptor and
+// query rows (one bulk copy) to an item slot, then looks the item's blocks up in
+// the block table and issues their K/V TMA tile loads into the stage ring.
+// ---------------------------------------------------------------------------
+template <typename T, int D, int BS, int kBPS, int kChunks, int kTileBytes, int kStages>
+struct Producer {
+    const DecodeParams &p;
+    const CUtensorMap *tk;
+    const CUtensorMap *tv;
+    const CtaState &c;
+    int lane;
+    uint32_t g;  // stages issued
+    uint32_t n;  // items published
+    bool failed;
+#ifdef PA_TRACE
+    unsigned long long t_last_issue;
+#endif
+
+    __device__ Producer(const DecodeParams &p_, const CUtensorMap *tk_, const CUtensorMap *tv_,
+                        const CtaState &c_, int lane_)
+        : p(p_), tk(tk_), tv(tv_), c(c_), lane(lane_), g(0), n(0), failed(false)
+    {
+#ifdef PA_TRACE
+        t_last_issue = 0;
+#endif
+        if (lane == 0) {
+            dev::tma_prefetch_desc(tk);
+            dev::tma_prefetch_desc(tv);
+        }
+    }
+
+    // Publish `it` and stream its blocks; false once something timed out.
+    __device__ bool emit(const Item &it)
+    {
+        constexpr uint32_t kQSlotBytes = kHeadsPerItem * D * sizeof(T);
+        {
+            const uint32_t slot = n % kItemSlots;
+            int ok = 1;
+            if (lane == 0) {
+                ok = dev::mbar_wait(dev::smem_addr(&c.item_empty[slot]),
+                                    ((n / kItemSlots) & 1u) ^ 1u, kWaitTimeoutNs);
+                if (ok) {
+                    c.items[slot] = it;
+                    const uint32_t qbytes = (uint32_t)it.rows * D * sizeof(T);
+                    const uint32_t fb = dev::smem_addr(&c.item_full[slot]);
+                    dev::mbar_arrive_expect_tx(fb, qbytes);
+                    dev::bulk_load(dev::smem_addr(c.qslots + slot * kQSlotBytes),
+                                   reinterpret_cast<const T *>(p.q) +
+                                       ((size_t)it.seq * p.num_q_heads + it.qrow0) * D,
+                                   qbytes, fb);
+                }
+            }
+            if (!__shfl_sync(0xffffffffu, ok, 0)) {
+                if (lane == 0)
+                    raise_error(p, c.abort, PA_DEVERR_TIMEOUT_EMPTY);
+                failed = true;
+                return false;
+            }
+            ++n;
+        }
         const int32_t *row = p.block_tables + (size_t)it.seq * p.max_blocks;
-        for (int jb = it.j0; jb < it.j1 && !failed; jb += 32) {
+        for (int jb = it.j0; jb < it.j1; jb += 32) {
             const int j = jb + lane;
             const int phys = (j < it.j1) ? row[j] : 0;  // one coalesced read per 32 blocks
-            const int n = min(32, it.j1 - jb);
-            for (int i = 0; i < n; ++i, ++g) {
-                const int ph = __shfl_sync(0xffffffffu, phys, i);
+            const int cnt = min(32, it.j1 - jb);
+            for (int i = 0; i < cnt; i += kBPS, ++g) {
+                const int nbs = min(kBPS, cnt - i);  // blocks in this stage
                 const uint32_t st = g % kStages;
                 int ok = 1;
+#ifdef PA_TRACE
+                const unsigned long long t_w0 = dev::global_timer_ns();
+#endif
                 if (lane == 0)
-                    ok = dev::mbar_wait(dev::smem_addr(&empty[st]), ((g / kStages) & 1u) ^ 1u,
+                    ok = dev::mbar_wait(dev::smem_addr(&c.empty[st]), ((g / kStages) & 1u) ^ 1u,
                                         kWaitTimeoutNs);
-                ok = __shfl_sync(0xffffffffu, ok, 0);
-                if (!ok) {
-                    if (lane == 0) {
-                        atomicOr(p.errors, PA_DEVERR_TIMEOUT_EMPTY);
-                        *abort = 1;
-                    }
-                    failed = true;
-                    break;
-                }
+#ifdef PA_TRACE
                 if (lane == 0) {
-                    const uint32_t fb = dev::smem_addr(&full[st]);
-                    dev::mbar_arrive_expect_tx(fb, 2u * kTileBytes);
-                    // an entry outside the pool reads zeros (fully out-of-bounds box)
-                    const int y = (ph >= 0 && ph < p.num_blocks) ? ph * BS : -BS;
-                    const uint32_t kd = dev::smem_addr(ring + (size_t)st * 2 * kTileBytes);
+                    const unsigned long long t_w1 = dev::global_timer_ns();
+                    PA_TRACE_ADD(6, t_w1 - t_w0);
+                    if (i == 0 && jb == it.j0 && t_last_issue)
+                        PA_TRACE_ADD(5, t_w0 - t_last_issue);
+                }
+#endif
+                if (!__shfl_sync(0xffffffffu, ok, 0)) {
+                    if (lane == 0)
+                        raise_error(p, c.abort, PA_DEVERR_TIMEOUT_EMPTY);
+                    failed = true;
+                    return false;
+                }
+                int ph[kBPS];
+#pragma unroll
+                for (int b = 0; b < kBPS; ++b)
+                    ph[b] = __shfl_sync(0xffffffffu, phys, (i + b) & 31);
+                if (lane == 0) {
+                    constexpr int kRowsPerStage = kTileBytes / (kChunks * 128);
+                    const uint32_t fb = dev::smem_addr(&c.full[st]);
+                    dev::mbar_arrive_expect_tx(fb, 2u * (uint32_t)nbs * (kTileBytes / kBPS));
+                    const uint32_t kd = dev::smem_addr(c.ring + (size_t)st * 2 * kTileBytes);
                     const uint32_t vd = kd + kTileBytes;
 #pragma unroll
-                    for (int c = 0; c < kChunks; ++c)
-                        dev::tma_load_4d(kd + c * BS * 128, tk, 0, c, it.kvh, y, fb);
+                    for (int b = 0; b < kBPS; ++b) {
+                        if (b < nbs) {
+                            // an entry outside the pool reads zeros (fully out-of-bounds box)
+                            const int y = (ph[b] >= 0 && ph[b] < p.num_blocks) ? ph[b] * BS : -BS;
+                            const uint32_t off = (uint32_t)b * BS * 128;
 #pragma unroll
-                    for (int c = 0; c < kChunks; ++c)
-                        dev::tma_load_4d(vd + c * BS * 128, tv, 0, c, it.kvh, y, fb);
+                            for (int ch = 0; ch < kChunks; ++ch)
+                                dev::tma_load_4d(kd + ch * kRowsPerStage * 128 + off, tk, 0, ch,
+                                                 it.kvh, y, fb);
+#pragma unroll
+                            for (int ch = 0; ch < kChunks; ++ch)
+                                dev::tma_load_4d(vd + ch * kRowsPerStage * 128 + off, tv, 0, ch,
+                                                 it.kvh, y, fb);
+                        }
+                    }
+#ifdef PA_TRACE
+                    t_last_issue = dev::global_timer_ns();
+                    PA_TRACE_ADD(7, 1);
+#endif
                 }
             }
         }
+        return true;
     }
-    if (failed && lane == 0) {
-        // Let the copies already issued land before the CTA's shared memory goes away.
-        const uint32_t first = g > kStages ? g - kStages : 0;
-        for (uint32_t q = first; q < g; ++q)
-            dev::mbar_wait(dev::smem_addr(&full[q % kStages]), (q / kStages) & 1u,
-                           kWaitTimeoutNs / 8);
+
+    // End-of-work marker for the consumers; on failure, let issued copies land.
+    __device__ void finish()
+    {
+#ifdef PA_TRACE
+        if (lane == 0) {
+            PA_TRACE_SET(3, dev::global_timer_ns());
+            PA_TRACE_SET(4, n);
+        }
+#endif
+        if (lane != 0)
+            return;
+        const uint32_t slot = n % kItemSlots;
+        if (dev::mbar_wait(dev::smem_addr(&c.item_empty[slot]), ((n / kItemSlots) & 1u) ^ 1u,
+                           failed ? kWaitTimeoutNs / 8 : kWaitTimeoutNs)) {
+            c.items[slot].seq = -1;
+            dev::mbar_arrive(dev::smem_addr(&c.item_full[slot]));
+        } else if (!failed) {
+            raise_error(p, c.abort, PA_DEVERR_TIMEOUT_EMPTY);
+            failed = true;
+        }
+        if (failed) {
+            const uint32_t first = g > kStages ? g - kStages : 0;
+            for (uint32_t q = first; q < g; ++q)
+                dev::mbar_wait(dev::smem_addr(&c.full[q % kStages]), (q / kStages) & 1u,
+                               kWaitTimeoutNs / 8);
+            if (n > 0)
+                dev::mbar_wait(dev::smem_addr(&c.item_full[(n - 1) % kItemSlots]),
+                               ((n - 1) / kItemSlots) & 1u, kWaitTimeoutNs / 8);
+        }
     }
+};
+
+// ---------------------------------------------------------------------------
+// Balanced split helpers.  Work is measured in ring stages: a unit of a sequence
+// with nb blocks is ceil(nb / bps) stages; all units of all sequences, in order
+// (sequence, kv head, head group), form one stream of `total` stages.  CTA c of G
+// takes stages [c * total / G, (c + 1) * total / G).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ int seq_stages(const DecodeParams &p, int s, int bs, int bps)
+{
+    const int nb = (clamp_len(p, s, bs) + bs - 1) / bs;
+    return (nb + bps - 1) / bps;
+}
+
+__device__ __forceinline__ long long warp_sum_ll(long long v)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+// Stages of the whole stream (every lane gets the value).
+__device__ __forceinline__ long long stream_total(const DecodeParams &p, int bs, int bps, int lane)
+{
+    long long t = 0;
+    for (int s0 = 0; s0 < p.num_seqs; s0 += 32) {
+        const int s = s0 + lane;
+        if (s < p.num_seqs)
+            t += seq_stages(p, s, bs, bps);
+    }
+    return warp_sum_ll(t) * ((long long)p.num_kv_heads * p.head_groups);
+}
+
+// First sequence s with prefix(s) >= x or prefix(s + 1) > x, where prefix(s) is
+// the stream offset of sequence s.  Returns num_seqs if there is none; *base gets
+// prefix(s).  Warp-cooperative.
+__device__ __forceinline__ int find_seq_at(const DecodeParams &p, int bs, int bps, long long x,
+                                           long long *base_out, int lane)
+{
+    const long long units = (long long)p.num_kv_heads * p.head_groups;
+    long long base = 0;
+    for (int s0 = 0; s0 < p.num_seqs; s0 += 32) {
+        const int s = s0 + lane;
+        const long long w = (s < p.num_seqs) ? units * seq_stages(p, s, bs, bps) : 0;
+        long long incl = w;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const long long v = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o)
+                incl += v;
+        }
+        const long long excl = incl - w;
+        const unsigned hit =
+            __ballot_sync(0xffffffffu, s < p.num_seqs && (base + excl >= x || base + incl > x));
+        if (hit) {
+            const int L = __ffs(hit) - 1;
+            *base_out = base + __shfl_sync(0xffffffffu, excl, L);
+            return s0 + L;
+        }
+        base += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    *base_out = base;
+    return p.num_seqs;
+}
+
+// CTA of a G-CTA grid whose stage range contains stream stage x.
+__device__ __forceinline__ long long cta_of(long long x, long long total, long long G)
+{
+    return ((x + 1) * G - 1) / total;
+}
+
+template <class Prod>
+__device__ __forceinline__ void walk_balanced(const DecodeParams &p, int bs, int bps, Prod &pr,
+                                              int lane)
+{
+    const long long G = gridDim.x;
+    const long long cta = blockIdx.x;
+    const bool last = cta == G - 1;
+    const long long units = (long long)p.num_kv_heads * p.head_groups;
+    const long long total = stream_total(p, bs, bps, lane);
+    const long long s_c = cta * total / G;
+    const long long e_c = (cta + 1) * total / G;
+    long long base = 0;
+    int s = find_seq_at(p, bs, bps, s_c, &base, lane);
+    for (; s < p.num_seqs && !*pr.c.abort; ++s) {
+        if (base >= e_c && !last)
+            break;
+        const int len = clamp_len(p, s, bs);
+        const int nb = (len + bs - 1) / bs;
+        const long long ns = (nb + bps - 1) / bps;
+        Item it;
+        it.seq = s;
+        it.len = len;
+        if (ns == 0) {
+            // an empty sequence belongs to the CTA whose range holds its offset
+            if (base >= s_c && (base < e_c || last)) {
+                for (long long u = 0; u < units; ++u) {
+                    it.kvh = (int)(u / p.head_groups);
+                    it.hg = (int)(u % p.head_groups);
+                    it.j0 = it.j1 = 0;
+                    it.qrow0 = it.kvh * p.group + it.hg * kHeadsPerItem;
+                    it.rows = min(kHeadsPerItem, p.group - it.hg * kHeadsPerItem);
+                    it.partial = 0;
+                    it.prow0 = 0;
+                    if (!pr.emit(it))
+                        return;
+                }
+            }
+            continue;
+        }
+        const long long u_lo = s_c > base ? (s_c - base) / ns : 0;
+        const long long u_hi = min(units - 1, (e_c - 1 - base) / ns);
+        for (long long u = u_lo; u <= u_hi; ++u) {
+            const long long a = base + u * ns;
+            const long long lo = max(a, s_c), hi = min(a + ns, e_c);
+            if (lo >= hi)
+                continue;
+            it.kvh = (int)(u / p.head_groups);
+            it.hg = (int)(u % p.head_groups);
+            it.j0 = (int)((lo - a) * bps);
+            it.j1 = (int)min((hi - a) * bps, (long long)nb);
+            it.qrow0 = it.kvh * p.group + it.hg * kHeadsPerItem;
+            it.rows = min(kHeadsPerItem, p.group - it.hg * kHeadsPerItem);
+            it.partial = (lo == a && hi == a + ns) ? 0 : 1;
+            // slot 2c: the unit began in an earlier CTA; slot 2c + 1: it goes on after
+            it.prow0 = (int)((2 * cta + (a < s_c ? 0 : 1)) * kHeadsPerItem);
+            if (!pr.emit(it))
+                return;
+        }
+        base += units * ns;
+    }
+}
+
+template <class Prod>
+__device__ __forceinline__ void walk_fixed(const DecodeParams &p, int bs, Prod &pr, int lane)
+{
+    int seq = 0;
+    long long base = 0;
+    for (long long w = blockIdx.x;; w += gridDim.x) {
+        if (!find_item(p, bs, w, seq, base, lane) || *pr.c.abort)
+            break;
+        if (!pr.emit(decode_item(p, bs, w, seq, base)))
+            return;
+    }
+}
+
+template <typename T, int D, int BS, int kBPS, int kChunks, int kTileBytes, int kStages>
+__device__ __forceinline__ void producer_loop(const DecodeParams &p, const CUtensorMap *tk,
+                                              const CUtensorMap *tv, const CtaState &c, int lane)
+{
+    Producer<T, D, BS, kBPS, kChunks, kTileBytes, kStages> pr(p, tk, tv, c, lane);
+    if (p.balanced)
+        walk_balanced(p, BS, kBPS, pr, lane);
+    else
+        walk_fixed(p, BS, pr, lane);
+    pr.finish();
 }
 
 // ---------------------------------------------------------------------------
@@ -244,12 +668,12 @@ __device__ __forceinline__ void finalize_item(const DecodeParams &p, const Item 
             }
         }
         const float o = (L > 0.f) ? O / L : 0.f;
-        const size_t h = (size_t)it.qrow0 + r;
-        if (it.single) {
+        if (!it.partial) {
+            const size_t h = (size_t)it.qrow0 + r;
             reinterpret_cast<T *>(p.out)[((size_t)it.seq * p.num_q_heads + h) * D + col] =
                 dev::from_float<T>(o);
         } else {
-            const size_t pr = ((size_t)it.seq * p.max_parts + it.part) * p.num_q_heads + h;
+            const size_t pr = (size_t)it.prow0 + r;
             p.part_o[pr * D + col] = o;
             if (col == 0)
                 p.part_lse[pr] = (L > 0.f) ? M + log2f(L) : -INFINITY;
@@ -268,38 +692,26 @@ __global__ void __launch_bounds__(kThreads, 2)
 {
     using C = Cfg<T, D, BS>;
     constexpr int kCE = C::kChunkElems;
-    constexpr int NT = BS / 8;   // score n-tiles of 8 tokens
+    constexpr int TS = C::kStageTokens;  // token rows per stage tile
+    constexpr int NT = TS / 8;   // score n-tiles of 8 tokens
     constexpr int KS = D / 16;   // k-steps of Q K^T
     constexpr int DT = D / 8;    // output n-tiles of 8 dims
     constexpr int SA = D + kAccPad;
+    constexpr uint32_t kQSlotBytes = kHeadsPerItem * D * sizeof(T);
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int rows_cap = min(kHeadsPerItem, p.group);
-    const SmemLayout lay = make_layout(C::kStages, C::kStageBytes, rows_cap, D, false);
-    uint8_t *ring = smem;
-    float *macc = reinterpret_cast<float *>(smem + lay.acc);
-    float *mml = reinterpret_cast<float *>(smem + lay.ml);
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + lay.bars);
-    uint64_t *empty = full + C::kStages;
-    volatile int *abort = reinterpret_cast<volatile int *>(smem + lay.flag);
+    const SmemLayout lay = make_layout(C::kStages, C::kStageBytes, rows_cap, D, sizeof(T));
+    const CtaState c = cta_state(smem, lay, C::kStages);
+    init_cta(c, C::kStages);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < C::kStages; ++s) {
-            dev::mbar_init(dev::smem_addr(&full[s]), 1);
-            dev::mbar_init(dev::smem_addr(&empty[s]), 1);
-        }
-        *abort = 0;
-        dev::fence_mbar_init();
-    }
-    __syncthreads();
-
     if (warp == kConsumerWarps) {
-        producer_loop<D, BS, C::kChunks, C::kTileBytes, C::kStages>(p, &tmap_k, &tmap_v, ring, full,
-                                                                   empty, abort, lane);
+        producer_loop<T, D, BS, C::kBPS, C::kChunks, C::kTileBytes, C::kStages>(p, &tmap_k, &tmap_v,
+                                                                              c, lane);
         return;
     }
 
@@ -308,52 +720,85 @@ __global__ void __launch_bounds__(kThreads, 2)
     const int cq = (lane & 3) * 2;   // fragment column pair
     const int mi = lane >> 3;        // ldmatrix: which 8x8 matrix this lane addresses
     const int swz = lane & 7;        // 128-byte swizzle: 16-byte unit ^= row % 8
-    int seq = 0;
-    long long base = 0;
-    uint32_t g = 0;
-    for (long long w = blockIdx.x;; w += gridDim.x) {
-        if (!find_item(p, BS, w, seq, base, lane))
+    uint32_t g = 0;                  // stages consumed (same count in every warp)
+    uint32_t sph = 0;                // consumer barrier phase
+#ifdef PA_TRACE
+    if (threadIdx.x == 0) {
+        unsigned int smid;
+        asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+        PA_TRACE_SET(0, dev::global_timer_ns());
+        PA_TRACE_SET(8, smid);
+    }
+    bool first_tile = true;
+#endif
+    for (uint32_t n = 0;; ++n) {
+        const uint32_t slot = n % kItemSlots;
+        if (!warp_wait(&c.item_full[slot], (n / kItemSlots) & 1u)) {
+            if (lane == 0)
+                raise_error(p, c.abort, PA_DEVERR_TIMEOUT_FULL);
             break;
-        const Item it = decode_item(p, BS, w, seq, base);
+        }
+        const Item it = load_item(&c.items[slot]);
+        if (it.seq < 0)
+            break;
+        const bool live0 = r0 < it.rows, live1 = r0 + 8 < it.rows;
 
-        // Query fragments (A operand of Q K^T); rows past the group are zero.
+        // Query fragments (A operand of Q K^T) from the item slot; rows past the
+        // group are zero.
         uint32_t qa[KS][4];
         {
-            const uint32_t *qw = reinterpret_cast<const uint32_t *>(
-                reinterpret_cast<const T *>(p.q) + ((size_t)it.seq * p.num_q_heads + it.qrow0) * D);
-            const bool v0 = r0 < it.rows, v1 = r0 + 8 < it.rows;
+            const uint32_t qb = dev::smem_addr(c.qslots + slot * kQSlotBytes) +
+                                (uint32_t)(((mi & 1) * 8 + (lane & 7)) * D * sizeof(T));
 #pragma unroll
             for (int ks = 0; ks < KS; ++ks) {
-                const int c0 = (ks * 16 + cq) >> 1;
-                qa[ks][0] = v0 ? __ldg(qw + r0 * (D / 2) + c0) : 0u;
-                qa[ks][1] = v1 ? __ldg(qw + (r0 + 8) * (D / 2) + c0) : 0u;
-                qa[ks][2] = v0 ? __ldg(qw + r0 * (D / 2) + c0 + 4) : 0u;
-                qa[ks][3] = v1 ? __ldg(qw + (r0 + 8) * (D / 2) + c0 + 4) : 0u;
+                dev::ldsm_x4(qb + (uint32_t)((ks * 16 + (mi >> 1) * 8) * sizeof(T)), qa[ks][0],
+                             qa[ks][1], qa[ks][2], qa[ks][3]);
+                qa[ks][0] = live0 ? qa[ks][0] : 0u;
+                qa[ks][2] = live0 ? qa[ks][2] : 0u;
+                qa[ks][1] = live1 ? qa[ks][1] : 0u;
+                qa[ks][3] = live1 ? qa[ks][3] : 0u;
             }
+            // every read of the slot (query rows, descriptor) must have completed
+            // before the slot is handed back to the producer
+            uint32_t all = (uint32_t)(it.seq ^ it.kvh ^ it.hg ^ it.len ^ it.j0 ^ it.j1 ^ it.qrow0 ^
+                                      it.rows ^ it.partial ^ it.prow0);
+#pragma unroll
+            for (int ks = 0; ks < KS; ++ks)
+                all ^= qa[ks][0] ^ qa[ks][1] ^ qa[ks][2] ^ qa[ks][3];
+            all = __reduce_xor_sync(0xffffffffu, all);
+            if (lane == 0)
+                dev::settle_loads(&c.sink[warp], all);
+            __syncwarp();
+            if (lane == 0)
+                dev::mbar_arrive(dev::smem_addr(&c.item_empty[slot]));
         }
-        const bool live0 = r0 < it.rows, live1 = r0 + 8 < it.rows;
 
         float acc[DT][4];
 #pragma unroll
         for (int i = 0; i < DT; ++i)
             acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
         float mrow0 = -INFINITY, mrow1 = -INFINITY, lrow0 = 0.f, lrow1 = 0.f;
-        bool failed = false;
+        bool alive = true;
 
-        for (int j = it.j0; j < it.j1; ++j, ++g) {
+        for (int j = it.j0; j < it.j1; j += C::kBPS, ++g) {
             if ((int)(g % kConsumerWarps) != warp)
                 continue;
             const uint32_t st = g % C::kStages;
-            if (!dev::mbar_wait(dev::smem_addr(&full[st]), (g / C::kStages) & 1u, kWaitTimeoutNs)) {
-                if (lane == 0) {
-                    atomicOr(p.errors, PA_DEVERR_TIMEOUT_FULL);
-                    *abort = 1;
-                }
-                failed = true;
+            if (!warp_wait(&c.full[st], (g / C::kStages) & 1u)) {
+                if (lane == 0)
+                    raise_error(p, c.abort, PA_DEVERR_TIMEOUT_FULL);
+                alive = false;
                 break;
             }
-            const int valid = min(BS, it.len - j * BS);
-            const uint32_t kb = dev::smem_addr(ring + (size_t)st * C::kStageBytes);
+#ifdef PA_TRACE
+            if (threadIdx.x == 0 && first_tile) {
+                PA_TRACE_SET(1, dev::global_timer_ns());
+                first_tile = false;
+            }
+#endif
+            // tokens of this stage that count: the loaded blocks, up to the context
+            const int valid = min(min(C::kBPS, it.j1 - j) * BS, it.len - j * BS);
+            const uint32_t kb = dev::smem_addr(c.ring + (size_t)st * C::kStageBytes);
             const uint32_t vb = kb + C::kTileBytes;
 
             // S = Q K^T: K tile rows are tokens, so plain ldmatrix yields the
@@ -365,7 +810,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
             for (int ks = 0; ks < KS; ++ks) {
                 const int d = ks * 16 + (mi & 1) * 8;
-                const uint32_t colpart = (uint32_t)(d / kCE) * (BS * 128) +
+                const uint32_t colpart = (uint32_t)(d / kCE) * (TS * 128) +
                                          (uint32_t)((((d % kCE) >> 3) ^ swz) << 4);
 #pragma unroll
                 for (int np = 0; np < NT / 2; ++np) {
@@ -425,9 +870,9 @@ __global__ void __launch_bounds__(kThreads, 2)
 
             // O += P V: V tile rows are tokens, so ldmatrix.trans yields the
             // "col" B fragment (k = token, n = head dim).
-            const bool partial = valid < BS;
+            const bool partial = valid < TS;
 #pragma unroll
-            for (int kt = 0; kt < BS / 16; ++kt) {
+            for (int kt = 0; kt < TS / 16; ++kt) {
                 uint32_t pa[4];
                 pa[0] = dev::Mma<T>::pack(sc[2 * kt][0], sc[2 * kt][1]);
                 pa[1] = dev::Mma<T>::pack(sc[2 * kt][2], sc[2 * kt][3]);
@@ -444,7 +889,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
                 for (int dp = 0; dp < D / 16; ++dp) {
                     const int d = dp * 16 + (mi >> 1) * 8;
-                    const uint32_t addr = vb + (uint32_t)(d / kCE) * (BS * 128) + tok * 128 +
+                    const uint32_t addr = vb + (uint32_t)(d / kCE) * (TS * 128) + tok * 128 +
                                           (uint32_t)((((d % kCE) >> 3) ^ swz) << 4);
                     uint32_t v0, v1, v2, v3;
                     dev::ldsm_x4_trans(addr, v0, v1, v2, v3);
@@ -454,16 +899,17 @@ __global__ void __launch_bounds__(kThreads, 2)
             }
             __syncwarp();
             if (lane == 0)
-                dev::mbar_arrive(dev::smem_addr(&empty[st]));
+                dev::mbar_arrive(dev::smem_addr(&c.empty[st]));
         }
-        (void)failed;  // a failed warp has set *abort: the CTA stops after this merge
+        if (!alive)
+            break;
 
         // ---- merge the four consumer warps ----
         lrow0 += __shfl_xor_sync(0xffffffffu, lrow0, 1);
         lrow0 += __shfl_xor_sync(0xffffffffu, lrow0, 2);
         lrow1 += __shfl_xor_sync(0xffffffffu, lrow1, 1);
         lrow1 += __shfl_xor_sync(0xffffffffu, lrow1, 2);
-        float *mine = macc + warp * rows_cap * SA;
+        float *mine = c.macc + warp * rows_cap * SA;
         if (live0) {
 #pragma unroll
             for (int i = 0; i < DT; ++i)
@@ -477,17 +923,29 @@ __global__ void __launch_bounds__(kThreads, 2)
                     make_float2(acc[i][2], acc[i][3]);
         }
         if ((lane & 3) == 0) {
-            mml[(warp * kHeadsPerItem + r0) * 2] = (live0 && lrow0 > 0.f) ? mrow0 : -INFINITY;
-            mml[(warp * kHeadsPerItem + r0) * 2 + 1] = lrow0;
-            mml[(warp * kHeadsPerItem + r0 + 8) * 2] = (live1 && lrow1 > 0.f) ? mrow1 : -INFINITY;
-            mml[(warp * kHeadsPerItem + r0 + 8) * 2 + 1] = lrow1;
+            c.mml[(warp * kHeadsPerItem + r0) * 2] = (live0 && lrow0 > 0.f) ? mrow0 : -INFINITY;
+            c.mml[(warp * kHeadsPerItem + r0) * 2 + 1] = lrow0;
+            c.mml[(warp * kHeadsPerItem + r0 + 8) * 2] = (live1 && lrow1 > 0.f) ? mrow1 : -INFINITY;
+            c.mml[(warp * kHeadsPerItem + r0 + 8) * 2 + 1] = lrow1;
         }
-        dev::consumer_sync(32 * kConsumerWarps);
-        finalize_item<T, D>(p, it, macc, mml, rows_cap, threadIdx.x);
-        dev::consumer_sync(32 * kConsumerWarps);
-        if (*abort)
+        if (!consumer_sync(c, sph)) {
+            if (lane == 0)
+                raise_error(p, c.abort, PA_DEVERR_TIMEOUT_FULL);
+            break;
+        }
+        finalize_item<T, D>(p, it, c.macc, c.mml, rows_cap, threadIdx.x);
+        if (!consumer_sync(c, sph)) {
+            if (lane == 0)
+                raise_error(p, c.abort, PA_DEVERR_TIMEOUT_FULL);
+            break;
+        }
+        if (*c.abort)
             break;
     }
+#ifdef PA_TRACE
+    if (threadIdx.x == 0)
+        PA_TRACE_SET(2, dev::global_timer_ns());
+#endif
 }
 
 // ---------------------------------------------------------------------------
@@ -511,49 +969,33 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int rows_cap = min(kHeadsPerItem, p.group);
-    const SmemLayout lay = make_layout(C::kStages, C::kStageBytes, rows_cap, D, true);
-    uint8_t *ring = smem;
-    float *macc = reinterpret_cast<float *>(smem + lay.acc);
-    float *mml = reinterpret_cast<float *>(smem + lay.ml);
-    float *qsm = reinterpret_cast<float *>(smem + lay.q);
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + lay.bars);
-    uint64_t *empty = full + C::kStages;
-    volatile int *abort = reinterpret_cast<volatile int *>(smem + lay.flag);
+    const SmemLayout lay = make_layout(C::kStages, C::kStageBytes, rows_cap, D, sizeof(float));
+    const CtaState c = cta_state(smem, lay, C::kStages);
+    init_cta(c, C::kStages);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < C::kStages; ++s) {
-            dev::mbar_init(dev::smem_addr(&full[s]), 1);
-            dev::mbar_init(dev::smem_addr(&empty[s]), 1);
-        }
-        *abort = 0;
-        dev::fence_mbar_init();
-    }
-    __syncthreads();
-
     if (warp == kConsumerWarps) {
-        producer_loop<D, BS, C::kChunks, C::kTileBytes, C::kStages>(p, &tmap_k, &tmap_v, ring, full,
-                                                                   empty, abort, lane);
+        producer_loop<float, D, BS, C::kBPS, C::kChunks, C::kTileBytes, C::kStages>(p, &tmap_k,
+                                                                                  &tmap_v, c, lane);
         return;
     }
 
     const int t = lane % BS;
     const int part = lane / BS;
-    float *qs = qsm + warp * H * D;
-    int seq = 0;
-    long long base = 0;
     uint32_t g = 0;
-    for (long long w = blockIdx.x;; w += gridDim.x) {
-        if (!find_item(p, BS, w, seq, base, lane))
+    uint32_t sph = 0;
+    for (uint32_t n = 0;; ++n) {
+        const uint32_t slot = n % kItemSlots;
+        if (!warp_wait(&c.item_full[slot], (n / kItemSlots) & 1u)) {
+            if (lane == 0)
+                raise_error(p, c.abort, PA_DEVERR_TIMEOUT_FULL);
             break;
-        const Item it = decode_item(p, BS, w, seq, base);
-        const float *qg = reinterpret_cast<const float *>(p.q) +
-                          ((size_t)it.seq * p.num_q_heads + it.qrow0) * D;
-        __syncwarp();
-        for (int i = lane; i < H * D; i += 32)
-            qs[i] = (i / D < it.rows) ? __ldg(qg + i) : 0.f;
-        __syncwarp();
+        }
+        const Item it = load_item(&c.items[slot]);
+        if (it.seq < 0)
+            break;
+        const float *qs = reinterpret_cast<const float *>(c.qslots) + slot * H * D;
 
         float acc[H][VEC];
         float mr[H], lr[H];
@@ -565,21 +1007,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int e = 0; e < VEC; ++e)
                 acc[r][e] = 0.f;
         }
-        bool failed = false;
+        bool alive = true;
         for (int j = it.j0; j < it.j1; ++j, ++g) {
             if ((int)(g % kConsumerWarps) != warp)
                 continue;
             const uint32_t st = g % C::kStages;
-            if (!dev::mbar_wait(dev::smem_addr(&full[st]), (g / C::kStages) & 1u, kWaitTimeoutNs)) {
-                if (lane == 0) {
-                    atomicOr(p.errors, PA_DEVERR_TIMEOUT_FULL);
-                    *abort = 1;
-                }
-                failed = true;
+            if (!warp_wait(&c.full[st], (g / C::kStages) & 1u)) {
+                if (lane == 0)
+                    raise_error(p, c.abort, PA_DEVERR_TIMEOUT_FULL);
+                alive = false;
                 break;
             }
             const int valid = min(BS, it.len - j * BS);
-            const uint8_t *kt = ring + (size_t)st * C::kStageBytes;
+            const uint8_t *kt = c.ring + (size_t)st * C::kStageBytes;
             const uint8_t *vt = kt + C::kTileBytes;
 
             float sc[H];
@@ -658,11 +1098,24 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             __syncwarp();
             if (lane == 0)
-                dev::mbar_arrive(dev::smem_addr(&empty[st]));
+                dev::mbar_arrive(dev::smem_addr(&c.empty[st]));
         }
-        (void)failed;
+        // the query rows of this slot are no longer read (every read of them fed an
+        // FMA above); the descriptor fields are settled like the fp16/bf16 path's
+        {
+            const uint32_t all = __reduce_xor_sync(
+                0xffffffffu, (uint32_t)(it.seq ^ it.kvh ^ it.hg ^ it.len ^ it.j0 ^ it.j1 ^
+                                        it.qrow0 ^ it.rows ^ it.partial ^ it.prow0));
+            if (lane == 0)
+                dev::settle_loads(&c.sink[warp], all);
+        }
+        __syncwarp();
+        if (lane == 0)
+            dev::mbar_arrive(dev::smem_addr(&c.item_empty[slot]));
+        if (!alive)
+            break;
 
-        float *mine = macc + warp * rows_cap * SA;
+        float *mine = c.macc + warp * rows_cap * SA;
 #pragma unroll
         for (int r = 0; r < H; ++r) {
             if (r < it.rows) {
@@ -670,19 +1123,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int e = 0; e < VEC; ++e)
                     mine[r * SA + lane * VEC + e] = acc[r][e];
                 if (lane == 0) {
-                    mml[(warp * H + r) * 2] = lr[r] > 0.f ? mr[r] : -INFINITY;
-                    mml[(warp * H + r) * 2 + 1] = lr[r];
+                    c.mml[(warp * H + r) * 2] = lr[r] > 0.f ? mr[r] : -INFINITY;
+                    c.mml[(warp * H + r) * 2 + 1] = lr[r];
                 }
             }
         }
-        dev::consumer_sync(32 * kConsumerWarps);
-        finalize_item<float, D>(p, it, macc, mml, rows_cap, threadIdx.x);
-        dev::consumer_sync(32 * kConsumerWarps);
-        if (*abort)
+        if (!consumer_sync(c, sph)) {
+            if (lane == 0)
+                raise_error(p, c.abort, PA_DEVERR_TIMEOUT_FULL);
+            break;
+        }
+        finalize_item<float, D>(p, it, c.macc, c.mml, rows_cap, threadIdx.x);
+        if (!consumer_sync(c, sph)) {
+            if (lane == 0)
+                raise_error(p, c.abort, PA_DEVERR_TIMEOUT_FULL);
+            break;
+        }
+        if (*c.abort)
             break;
     }
 }
-
 // ---------------------------------------------------------------------------
 // Split-KV merge: out[s][h] = sum_p 2^(lse_p - M) o_p / sum_p 2^(lse_p - M).
 // One warp per (sequence, query head); sequences with one partition were
@@ -697,6 +1157,9 @@ __global__ void __launch_bounds__(128)
     const int lane = threadIdx.x & 31;
     const int s = blockIdx.y;
     const int h = blockIdx.x * 4 + warp;
+    // launched as a programmatic dependent of the partition kernel: its partials
+    // are complete and visible only after this wait
+    dev::grid_dependency_wait();
     if (h >= p.num_q_heads)
         return;
     const int np = num_parts(p, s, block_size);
@@ -746,17 +1209,92 @@ __global__ void __launch_bounds__(128)
 }
 
 // ---------------------------------------------------------------------------
+// Balanced-split merge: one CTA per boundary b between CTAs b-1 and b of the
+// partition grid (G CTAs).  The unit that straddles boundary b is merged by the CTA
+// of its first boundary, from the partials of CTAs c_first .. c_last: slot
+// 2 c_first + 1 (where the unit began), then slot 2 c of every later CTA.
+// ---------------------------------------------------------------------------
+template <typename T, int D>
+__global__ void __launch_bounds__(128)
+    pa_merge_balanced_kernel(const __grid_constant__ DecodeParams p, int block_size, int bps, int G)
+{
+    constexpr int VEC = D / 32;
+    // launched as a programmatic dependent of the partition kernel
+    dev::grid_dependency_wait();
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const long long b = (long long)blockIdx.x + 1;
+    const long long total = stream_total(p, block_size, bps, lane);
+    if (total == 0)
+        return;
+    const long long x = b * total / G;  // first stage of CTA b
+    long long base = 0;
+    int s = find_seq_at(p, block_size, bps, x, &base, lane);
+    while (s < p.num_seqs && seq_stages(p, s, block_size, bps) == 0)
+        ++s;  // empty sequences sit at x without covering it
+    if (s >= p.num_seqs)
+        return;
+    const long long ns = seq_stages(p, s, block_size, bps);
+    const long long u = (x - base) / ns;
+    const long long a = base + u * ns;
+    if (a == x || cta_of(a, total, G) != b - 1)
+        return;  // not cut here, or cut first at an earlier boundary
+    const long long c_first = b - 1;
+    const int nparts = (int)(cta_of(a + ns - 1, total, G) - c_first + 1);
+    const int kvh = (int)(u / p.head_groups);
+    const int hg = (int)(u % p.head_groups);
+    const int qrow0 = kvh * p.group + hg * kHeadsPerItem;
+    const int rows = min(kHeadsPerItem, p.group - hg * kHeadsPerItem);
+    // CTAs with an empty stage range (more CTAs than stages) wrote nothing
+    auto holds = [&](int i) -> bool {
+        const long long cc = c_first + i;
+        return i == 0 || cc * total / G < (cc + 1) * total / G;
+    };
+    for (int r = warp; r < rows; r += 4) {
+        auto prow = [&](int i) -> size_t {
+            const long long slot = i == 0 ? 2 * c_first + 1 : 2 * (c_first + i);
+            return (size_t)(slot * kHeadsPerItem + r);
+        };
+        float M = -INFINITY;
+        for (int i = lane; i < nparts; i += 32)
+            if (holds(i))
+                M = fmaxf(M, p.part_lse[prow(i)]);
+        M = dev::warp_max(M);
+        float W = 0.f;
+        for (int i = lane; i < nparts; i += 32)
+            if (holds(i))
+                W += exp2f(p.part_lse[prow(i)] - M);
+        W = dev::warp_sum(W);
+        float acc[VEC];
+#pragma unroll
+        for (int e = 0; e < VEC; ++e)
+            acc[e] = 0.f;
+        for (int i = 0; i < nparts; ++i) {
+            if (!holds(i))
+                continue;
+            const float wgt = exp2f(p.part_lse[prow(i)] - M);
+            const float *po = p.part_o + prow(i) * D + lane * VEC;
+#pragma unroll
+            for (int e = 0; e < VEC; ++e)
+                acc[e] = fmaf(wgt, po[e], acc[e]);
+        }
+        T *o = reinterpret_cast<T *>(p.out) + ((size_t)s * p.num_q_heads + qrow0 + r) * D + lane * VEC;
+#pragma unroll
+        for (int e = 0; e < VEC; ++e)
+            o[e] = dev::from_float<T>(acc[e] / W);
+    }
+}
+
+// ---------------------------------------------------------------------------
 // Launch helpers
 // ---------------------------------------------------------------------------
 template <typename T, int D, int BS>
 struct KernelOf {
     static void *get() { return reinterpret_cast<void *>(&pa_decode_mma_kernel<T, D, BS>); }
-    static constexpr bool kQSmem = false;
 };
 template <int D, int BS>
 struct KernelOf<float, D, BS> {
     static void *get() { return reinterpret_cast<void *>(&pa_decode_f32_kernel<D, BS>); }
-    static constexpr bool kQSmem = true;
 };
 
 template <typename T, int D, int BS>
@@ -764,7 +1302,7 @@ inline size_t smem_bytes_for(int group)
 {
     using C = Cfg<T, D, BS>;
     const int rows = group < kHeadsPerItem ? group : kHeadsPerItem;
-    return make_layout(C::kStages, C::kStageBytes, rows, D, KernelOf<T, D, BS>::kQSmem).total;
+    return make_layout(C::kStages, C::kStageBytes, rows, D, sizeof(T)).total;
 }
 
 int cached_occupancy(void *kernel, int device, size_t smem, size_t max_smem);
@@ -783,23 +1321,52 @@ cudaError_t launch_decode_impl(const DecodeLaunch &L, cudaStream_t stream)
     const int per_sm = cached_occupancy(kern, dev, smem, smem_max);
     if (per_sm <= 0)
         return cudaErrorInvalidConfiguration;
-    const long long items = (long long)p.num_seqs * p.max_parts * p.num_kv_heads * p.head_groups;
-    long long grid = (long long)per_sm * L.sm_count;
-    if (L.grid > 0)
+    long long grid = (long long)min(per_sm, kMaxCtasPerSm) * L.sm_count;
+    if (L.grid > 0 && L.grid < grid)
         grid = L.grid;
-    if (grid > items)
-        grid = items;
+    if (!p.balanced) {
+        const long long items =
+            (long long)p.num_seqs * p.max_parts * p.num_kv_heads * p.head_groups;
+        if (grid > items)
+            grid = items;
+    }
     if (grid < 1)
         grid = 1;
     void *args[] = {const_cast<DecodeParams *>(&L.p), const_cast<CUtensorMap *>(&L.tmap_k),
                     const_cast<CUtensorMap *>(&L.tmap_v)};
-    e = cudaLaunchKernel(kern, dim3((unsigned)grid), dim3(kThreads), args, smem, stream);
+    // Both kernels are programmatic dependents of whatever precedes them in the
+    // stream: their launch and prologue overlap the previous kernel's tail, and
+    // griddepcontrol.wait orders every read of the previous kernel's results.
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    #ifdef PA_NO_PDL
+    attr[0].val.programmaticStreamSerializationAllowed = 0;
+#else
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+#endif
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelExC(&cfg, kern, args);
     if (e != cudaSuccess)
         return e;
-    if (p.max_parts > 1) {
-        dim3 mg((unsigned)((p.num_q_heads + 3) / 4), (unsigned)p.num_seqs);
-        pa_merge_kernel<T, D><<<mg, 128, 0, stream>>>(p, BS);
-        e = cudaGetLastError();
+    cudaLaunchConfig_t mcfg = {};
+    mcfg.blockDim = dim3(128);
+    mcfg.dynamicSmemBytes = 0;
+    mcfg.stream = stream;
+    mcfg.attrs = attr;
+    mcfg.numAttrs = 1;
+    if (p.balanced && grid > 1) {
+        mcfg.gridDim = dim3((unsigned)(grid - 1));
+        e = cudaLaunchKernelEx(&mcfg, pa_merge_balanced_kernel<T, D>, p, (int)BS,
+                               (int)Cfg<T, D, BS>::kBPS, (int)grid);
+    } else if (!p.balanced && p.max_parts > 1) {
+        mcfg.gridDim = dim3((unsigned)((p.num_q_heads + 3) / 4), (unsigned)p.num_seqs);
+        e = cudaLaunchKernelEx(&mcfg, pa_merge_kernel<T, D>, p, (int)BS);
     }
     return e;
 }

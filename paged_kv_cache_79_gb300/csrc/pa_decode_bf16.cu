@@ -14,3 +14,5 @@ size_t decode_smem_bytes_bf16(int head_dim, int block_size, int group)
 }
 
 }  // namespace pagedkv
+
+PA_TRACE_DEFINE_READER(bf16)

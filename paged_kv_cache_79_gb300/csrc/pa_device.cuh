@@ -89,6 +89,39 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap *map
         : "memory");
 }
 
+// Contiguous bulk copy global -> this CTA's shared memory (16-byte aligned
+// addresses, size a multiple of 16); completion counted on `bar`.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            dst),
+        "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+        : "memory");
+}
+
+// Complete the shared-memory loads that produced `v` before this call returns: a
+// load whose register result is first used much later may still be in flight
+// when the warp moves on, so storing a value derived from every such result to a
+// scratch word (the store must wait for its data) pins them before a release of
+// the memory they were read from.
+__device__ __forceinline__ void settle_loads(volatile uint32_t *sink, uint32_t v) { *sink = v; }
+
+// ---- programmatic dependent launch ------------------------------------------------
+// Block until the grids this one depends on have completed and their writes are
+// visible (returns at once when the launch had no programmatic dependency).
+__device__ __forceinline__ void grid_dependency_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Allow the next grid in the stream (launched with programmatic serialization) to
+// start; it still waits for this grid's completion before reading its results.
+__device__ __forceinline__ void grid_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---- named barrier among the consumer warps ------------------------------------
 __device__ __forceinline__ void consumer_sync(int nthreads)
 {

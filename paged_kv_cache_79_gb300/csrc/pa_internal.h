@@ -25,8 +25,10 @@ struct DecodeParams {
     const void *q;                // [S][Hq][D] storage dtype
     const int32_t *block_tables;  // [S][max_blocks]
     const int32_t *context_lens;  // [S]
-    float *part_o;                // [S][max_parts][Hq][D] fp32 (null if max_parts == 1)
-    float *part_lse;              // [S][max_parts][Hq]    fp32 log2-sum-exp
+    // Partial results (fp32 output rows and their log2-sum-exp), null when unused:
+    //   fixed partitions: rows [S][max_parts][Hq];  balanced split: rows [2*grid][16]
+    float *part_o;
+    float *part_lse;
     unsigned int *errors;         // device error flags (PA_DEVERR_*)
     float scale_log2;             // softmax scale * log2(e)
     int num_seqs;
@@ -36,9 +38,13 @@ struct DecodeParams {
     int num_kv_heads;
     int group;                    // num_q_heads / num_kv_heads
     int head_groups;              // ceil(group / kHeadsPerItem)
-    int partition_blocks;         // blocks per partition
-    int max_parts;                // ceil(max_blocks / partition_blocks)
+    int partition_blocks;         // fixed partitions: blocks per partition
+    int max_parts;                // fixed partitions: ceil(max_blocks / partition_blocks)
+    int balanced;                 // 1: balanced split over the persistent grid
 };
+
+// Balanced split: partial slots are reserved for at most this many CTAs per SM.
+constexpr int kMaxCtasPerSm = 4;
 
 struct DecodeLaunch {
     DecodeParams p;

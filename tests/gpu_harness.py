@@ -2,8 +2,12 @@
 
 Tolerances (stated for the attention output, fp32 accumulation):
   fp32 storage:        max |gpu - oracle| <= 1e-5
-  fp16 / bf16 storage: max |gpu - oracle| <= 1e-2  and
-                       max |gpu - oracle| / max |oracle| <= 1e-2   (normwise relative)
+  fp16 / bf16 storage: "1e-2 (relative 1e-2)", read elementwise as
+                       |gpu - oracle| <= 1e-2 * max(1, |oracle|)      and
+                       max |gpu - oracle| / max |oracle| <= 1e-2      (normwise relative)
+  A plain max-abs bound of 1e-2 would be finer than the output format: half a bf16
+  ulp is 2^-9 |x|, more than 1e-2 once |x| > 2.56 (short contexts, where the output
+  is an average of a few N(0,1) rows, reach |x| ~ 4).
 """
 from __future__ import annotations
 
@@ -29,19 +33,25 @@ def dtype_name(t: torch.Tensor) -> str:
 
 
 def errors(got: torch.Tensor, want: np.ndarray):
+    """(max abs error, normwise relative error, max of |error| / max(1, |ref|))."""
     g = got.detach().float().cpu().double().numpy()
-    err = float(np.max(np.abs(g - want))) if want.size else 0.0
-    scale = float(np.max(np.abs(want))) if want.size else 0.0
-    return err, (err / scale if scale > 0 else err)
+    if not want.size:
+        return 0.0, 0.0, 0.0
+    d = np.abs(g - want)
+    err = float(np.max(d))
+    scale = float(np.max(np.abs(want)))
+    mixed = float(np.max(d / np.maximum(1.0, np.abs(want))))
+    return err, (err / scale if scale > 0 else err), mixed
 
 
 def assert_close(got: torch.Tensor, want: np.ndarray, dtype: str, what: str = ""):
     assert np.all(np.isfinite(got.detach().float().cpu().numpy())), f"{what}: non-finite output"
-    err, rel = errors(got, want)
+    err, rel, mixed = errors(got, want)
     if dtype == "f32":
         assert err <= TOL_F32, f"{what}: max abs err {err:.3e} > {TOL_F32}"
     else:
-        assert err <= TOL_16 and rel <= TOL_16, f"{what}: max abs err {err:.3e}, normwise rel {rel:.3e}"
+        assert mixed <= TOL_16 and rel <= TOL_16, \
+            f"{what}: max abs err {err:.3e}, elementwise {mixed:.3e}, normwise rel {rel:.3e}"
     return err, rel
 
 

@@ -99,11 +99,18 @@ def test_workspace_size_formula():
         P.pa_decode_workspace_size(4, 8, 3, 64, 16, 10, 64)
 
 
-def test_auto_partition_is_block_multiple_and_bounded():
-    for (S, hq, hkv, b, w) in [(8, 40, 40, 16, 128), (64, 64, 8, 16, 2048), (1, 8, 8, 16, 4), (256, 32, 8, 32, 4096)]:
-        p = P.pa_decode_partition_size(S, hq, hkv, 128, b, w, 0)
-        assert p > 0 and p % b == 0
-        assert p <= max(1024, b) or p >= w * b
+def test_partition_size_resolution():
+    # 0 selects the balanced split; a fixed size is capped at the table capacity
+    assert P.pa_decode_partition_size(8, 40, 40, 128, 16, 128, 0) == 0
+    assert P.pa_decode_partition_size(8, 40, 40, 128, 16, 128, 512) == 512
+    assert P.pa_decode_partition_size(8, 40, 40, 128, 16, 4, 512) == 64
+    assert P.pa_decode_partition_size(8, 40, 40, 128, 16, 4, 24) == -1
+
+
+def test_balanced_workspace_does_not_depend_on_lengths():
+    a = P.pa_decode_workspace_size(8, 40, 40, 128, 16, 128, 0)
+    b = P.pa_decode_workspace_size(256, 32, 8, 128, 32, 4096, 0)
+    assert a == b > 0
 
 
 # ---------------------------------------------------------------------------

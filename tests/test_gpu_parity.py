@@ -49,6 +49,23 @@ def test_decode_matches_oracle(dtype, D, B, Hq, Hkv, lens, part):
     assert_close(got, want, dtype, f"{dtype} D{D} B{B} G{Hq // Hkv} {lens} part{part}")
 
 
+BALANCED_EDGES = [
+    ("bf16", 128, 16, 40, 2, [1 + (i * 7) % 20 for i in range(500)]),   # many tiny sequences, G=20
+    ("f16", 128, 32, 8, 8, [0, 0, 0]),                                    # nothing to read
+    ("bf16", 128, 16, 8, 1, [60000]),                                     # one unit over every CTA
+    ("f32", 64, 16, 4, 2, [0, 3000, 0, 1, 0]),                            # empty sequences between
+    ("f16", 64, 32, 16, 16, [5, 70, 4097, 2, 33]),
+]
+
+
+@pytest.mark.parametrize("dtype,D,B,Hq,Hkv,lens", BALANCED_EDGES, ids=lambda v: str(v)[:40])
+def test_balanced_split_edges(dtype, D, B, Hq, Hkv, lens):
+    q, kc, vc, bt, cl = small_case(sum(lens) % 997, dtype, D, B, Hq, Hkv, lens)
+    got = run_decode(q, kc, vc, bt, cl, 0.07, Hq, Hkv, D, B, part=0)
+    want = oracle_decode(q, kc, vc, bt, cl, 0.07, dtype, Hq, Hkv, D, B)
+    assert_close(got, want, dtype)
+
+
 @pytest.mark.parametrize("dtype", ["f32", "f16", "bf16"])
 def test_single_token_returns_value_row(dtype):
     q, kc, vc, bt, cl = small_case(5, dtype, 128, 16, 8, 2, [1, 1, 1])

@@ -14,7 +14,7 @@ import torch
 
 import paged_kv_cache_79_gb300 as P
 from paged_kv_cache_79_gb300 import _lib
-from tests.gpu_harness import assert_close, errors, small_case
+from tests.gpu_harness import assert_close, small_case
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"

@@ -239,8 +239,9 @@ def run_ours(args):
     import paged_kv_cache_79_gb300 as P
     parts = P.pa_decode_partition_size(S, w.num_q_heads, w.num_kv_heads, w.head_dim, w.block_size,
                                        bt.shape[1], w.partition_size)
-    # balanced split (0): partition + merge kernels; fixed: merge only if a table spans partitions
-    merge = parts == 0 or -(-bt.shape[1] // (parts // w.block_size)) > 1
+    # balanced split (0): one partition kernel (split units merge in it); fixed
+    # partitions: plus the merge kernel when a table spans several partitions
+    merge = parts > 0 and -(-bt.shape[1] // (parts // w.block_size)) > 1
     launches_per_step = (1 if n_pairs else 0) + (1 if n_tok else 0) + 1 + (1 if merge else 0)
 
     with torch.cuda.stream(stream):
@@ -318,7 +319,7 @@ def run_ours(args):
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_kind": f"{peak_kind} copy bandwidth",
                      "traffic": profiled_traffic(w.name),
-                     "kernel": "pa_decode (partition kernel + split-KV merge)"},
+                     "kernel": "pa_decode (partition kernel; split-KV merge fused or second kernel)"},
         "e2e": e2e,
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk,

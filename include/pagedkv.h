@@ -84,13 +84,17 @@ int pa_last_cuda_error(void);
  * to [0, max_blocks_per_seq * block_size].
  *
  * Long contexts are split so that several CTAs share one sequence; their partial
- * (max, exp-sum, weighted V) results are merged by a second kernel with the same
- * rule.  partition_size selects the split:
+ * (max, exp-sum, weighted V) results are merged with the same rule.
+ * partition_size selects the split:
  *   0      balanced split: the K/V of all (sequence, kv head) pairs is cut into
- *          equal shares, one per CTA of a persistent grid, so every CTA streams the
- *          same number of bytes whatever the length mix;
- *   > 0    fixed partitions of partition_size tokens (a multiple of block_size).
- * Both give the same result up to fp32 rounding order.
+ *          equal shares, one per CTA of a persistent grid, so every CTA streams
+ *          about the same number of bytes whatever the length mix; the CTA that
+ *          completes a split pair's partials merges them (one kernel launch);
+ *   > 0    fixed partitions of partition_size tokens (a multiple of block_size),
+ *          merged by a second kernel.
+ * Both give the same result up to fp32 rounding order.  The workspace needs no
+ * initialisation: the balanced split's merge counters are tagged with a
+ * per-call epoch.
  *
  * Arguments
  *   out            device, [S][Hq][d], dtype `dtype`, written
@@ -128,9 +132,10 @@ int pa_decode_partition_size(int num_seqs, int num_q_heads, int num_kv_heads, in
  * Bytes of workspace pa_decode needs for these arguments.  Fixed partitions: 0
  * when one partition covers the table, else fp32 partial outputs [S][P][Hq][d]
  * (256-byte aligned end) followed by fp32 log2-sum-exp values [S][P][Hq], P =
- * ceil(max_blocks_per_seq * block_size / partition_size).  Balanced split: the
- * same two arrays with 2 * 4 * (SMs of the current device) * 16 rows, whatever the
- * lengths.  Returns (size_t)-1 for invalid arguments.
+ * ceil(max_blocks_per_seq * block_size / partition_size).  Balanced split: C =
+ * 4 * (SMs of the current device) 64-bit merge counters (256-byte aligned end),
+ * then the same two arrays with 2 * C * 16 rows, whatever the lengths.  Returns
+ * (size_t)-1 for invalid arguments.
  */
 size_t pa_decode_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
                                 int block_size, int max_blocks_per_seq, int partition_size);

@@ -1,6 +1,7 @@
 // extern "C" entry points of libpagedkv.so: argument validation, tensor-map
 // encoding, partition sizing and kernel dispatch.  Declarations and the contract
 // of every function are in include/pagedkv.h.
+#include <atomic>
 #include <cmath>
 #include <cstring>
 #include <map>
@@ -126,8 +127,21 @@ int resolve_partition(int B, int max_blocks, int part)
     return part >= max_ctx ? (int)(((max_ctx + B - 1) / B) * B) : part;
 }
 
-// Balanced split: partial rows reserved for 2 slots x 16 query heads per CTA.
-size_t balanced_rows(int sms) { return (size_t)2 * kMaxCtasPerSm * (size_t)sms * kHeadsPerItem; }
+// Balanced split workspace: one merge counter per CTA, then partial rows for
+// 2 slots x 16 query heads per CTA.
+size_t balanced_ctas(int sms) { return (size_t)kMaxCtasPerSm * (size_t)sms; }
+size_t balanced_rows(int sms) { return 2 * balanced_ctas(sms) * kHeadsPerItem; }
+size_t counter_bytes(int sms) { return (balanced_ctas(sms) * 8 + 255) & ~size_t(255); }
+
+std::atomic<unsigned int> g_epoch{0};
+
+unsigned int next_epoch()
+{
+    unsigned int e = ++g_epoch;
+    if (e == 0)  // a zeroed counter must never match
+        e = ++g_epoch;
+    return e;
+}
 
 int current_sms()
 {
@@ -221,9 +235,10 @@ size_t pa_decode_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads,
     if (part < 0)
         return (size_t)-1;
     if (part == 0) {
-        const int sms = current_sms();
-        const size_t rows = balanced_rows(sms > 0 ? sms : 160);
-        return ((rows * (size_t)head_dim * 4 + 255) & ~size_t(255)) + rows * 4;
+        int sms = current_sms();
+        sms = sms > 0 ? sms : 160;
+        const size_t rows = balanced_rows(sms);
+        return counter_bytes(sms) + ((rows * (size_t)head_dim * 4 + 255) & ~size_t(255)) + rows * 4;
     }
     const long long pb = part / block_size;
     const long long parts = (max_blocks_per_seq + pb - 1) / pb;
@@ -291,6 +306,11 @@ pa_status pa_decode(void *out, const void *q, const void *k_cache, const void *v
     if (balanced || parts > 1) {
         const size_t rows =
             balanced ? balanced_rows(sms) : (size_t)num_seqs * parts * num_q_heads;
+        if (balanced) {
+            p.counters = static_cast<unsigned long long *>(workspace);
+            p.epoch = next_epoch();
+            workspace = static_cast<char *>(workspace) + counter_bytes(sms);
+        }
         p.part_o = static_cast<float *>(workspace);
         p.part_lse = reinterpret_cast<float *>(static_cast<char *>(workspace) +
                                                ((rows * head_dim * 4 + 255) & ~size_t(255)));

@@ -12,9 +12,10 @@
 // sharing that kv head); a work item is a range of a unit's blocks.  A persistent
 // grid of CTAs takes the items in one of two ways:
 //   balanced split (partition_size 0): the units' K/V streams are concatenated and
-//               each CTA takes an equal contiguous range of ring stages, so every CTA
-//               moves the same number of bytes; a unit cut by CTA boundaries leaves
-//               partials that pa_merge_balanced_kernel combines;
+//               each CTA takes an equal contiguous range of ring stages (each unit
+//               also charged a fixed cost), so every CTA moves about the same number
+//               of bytes; a unit cut by CTA boundaries leaves partials that the CTA
+//               completing the set merges;
 //   fixed partitions (partition_size > 0): units are cut every partition_size
 //               tokens and CTA c takes items c, c + grid, ...; pa_merge_kernel
 //               combines the partitions of multi-partition sequences.
@@ -131,7 +132,7 @@ __host__ __device__ inline SmemLayout make_layout(int stages, int stage_bytes, i
     o = (o + 15u) & ~15u;
     L.bars = o;
     o += (2u * (uint32_t)stages + 2u * kItemSlots + 1u) * 8u;
-    L.flag = o;  // abort flag, then one scratch word per consumer warp
+    L.flag = o;  // abort flag, merge flag, then one scratch word per consumer warp
     o += 16u + 4u * kConsumerWarps;
     L.total = o + 1024u;  // slack to align the base to 1024 bytes (128-byte swizzle)
     return L;
@@ -187,7 +188,11 @@ struct Item {
     int qrow0, rows;        // query heads qrow0 .. qrow0 + rows - 1
     int partial;            // 0: write the output; 1: write partial row prow0 + r
     int prow0;
-    int pad[6];             // 64 bytes: one shared-memory descriptor slot
+    // balanced split, partial items: the unit's partials come from the non-empty
+    // CTAs c_first ... (nparts of them); the CTA that writes the last one merges
+    int c_first, nparts;
+    unsigned int total_lo, total_hi;  // stream length (to tell empty CTA ranges)
+    int pad[2];             // 64 bytes: one shared-memory descriptor slot
 };
 
 __device__ __forceinline__ Item decode_item(const DecodeParams &p, int bs, long long w, int seq,
@@ -217,6 +222,9 @@ __device__ __forceinline__ Item decode_item(const DecodeParams &p, int bs, long 
     it.rows = min(kHeadsPerItem, p.group - it.hg * kHeadsPerItem);
     it.partial = num_parts(p, seq, bs) == 1 ? 0 : 1;
     it.prow0 = (int)(((long long)seq * p.max_parts + part) * p.num_q_heads + it.qrow0);
+    it.c_first = -1;  // merged by pa_merge_kernel
+    it.nparts = 0;
+    it.total_lo = it.total_hi = 0;
     return it;
 }
 
@@ -233,6 +241,7 @@ struct CtaState {
     uint64_t *item_full, *item_empty;  // per item slot
     uint64_t *csync;                   // consumer-only barrier (all consumer threads arrive)
     volatile int *abort;
+    volatile int *merge;               // this CTA completes the current split unit
     volatile uint32_t *sink;           // per consumer warp: see dev::settle_loads
 };
 
@@ -250,6 +259,7 @@ __device__ __forceinline__ CtaState cta_state(uint8_t *smem, const SmemLayout &l
     c.item_empty = c.item_full + kItemSlots;
     c.csync = c.item_empty + kItemSlots;
     c.abort = reinterpret_cast<volatile int *>(smem + lay.flag);
+    c.merge = reinterpret_cast<volatile int *>(smem + lay.flag + 4);
     c.sink = reinterpret_cast<volatile uint32_t *>(smem + lay.flag + 16);
     return c;
 }
@@ -292,6 +302,10 @@ __device__ __forceinline__ Item load_item(const Item *slot)
     it.rows = v[7];
     it.partial = v[8];
     it.prow0 = v[9];
+    it.c_first = v[10];
+    it.nparts = v[11];
+    it.total_lo = (unsigned int)v[12];
+    it.total_hi = (unsigned int)v[13];
     return it;
 }
 
@@ -478,10 +492,17 @@ struct Producer {
 
 // ---------------------------------------------------------------------------
 // Balanced split helpers.  Work is measured in ring stages: a unit of a sequence
-// with nb blocks is ceil(nb / bps) stages; all units of all sequences, in order
-// (sequence, kv head, head group), form one stream of `total` stages.  CTA c of G
-// takes stages [c * total / G, (c + 1) * total / G).
+// with nb blocks costs kUnitCost + ceil(nb / bps) positions -- the fixed cost of an
+// item (descriptor, query rows, block-table lookup latency, merge) counted as
+// kUnitCost stages, then its real stages.  All units of all sequences, in order
+// (sequence, kv head, head group), form one stream of `total` positions; CTA c of
+// G takes positions [c * total / G, (c + 1) * total / G).
 // ---------------------------------------------------------------------------
+#ifndef PA_UNIT_COST
+#define PA_UNIT_COST 2
+#endif
+constexpr int kUnitCost = PA_UNIT_COST;
+static_assert(kUnitCost >= 1, "every unit needs a start position");
 __device__ __forceinline__ int seq_stages(const DecodeParams &p, int s, int bs, int bps)
 {
     const int nb = (clamp_len(p, s, bs) + bs - 1) / bs;
@@ -496,21 +517,21 @@ __device__ __forceinline__ long long warp_sum_ll(long long v)
     return v;
 }
 
-// Stages of the whole stream (every lane gets the value).
+// Positions of the whole stream (every lane gets the value).
 __device__ __forceinline__ long long stream_total(const DecodeParams &p, int bs, int bps, int lane)
 {
     long long t = 0;
     for (int s0 = 0; s0 < p.num_seqs; s0 += 32) {
         const int s = s0 + lane;
         if (s < p.num_seqs)
-            t += seq_stages(p, s, bs, bps);
+            t += kUnitCost + seq_stages(p, s, bs, bps);
     }
     return warp_sum_ll(t) * ((long long)p.num_kv_heads * p.head_groups);
 }
 
-// First sequence s with prefix(s) >= x or prefix(s + 1) > x, where prefix(s) is
-// the stream offset of sequence s.  Returns num_seqs if there is none; *base gets
-// prefix(s).  Warp-cooperative.
+// The sequence whose positions contain x (every unit has at least one position);
+// num_seqs if x >= total.  *base_out gets the sequence's first position.
+// Warp-cooperative.
 __device__ __forceinline__ int find_seq_at(const DecodeParams &p, int bs, int bps, long long x,
                                            long long *base_out, int lane)
 {
@@ -518,7 +539,7 @@ __device__ __forceinline__ int find_seq_at(const DecodeParams &p, int bs, int bp
     long long base = 0;
     for (int s0 = 0; s0 < p.num_seqs; s0 += 32) {
         const int s = s0 + lane;
-        const long long w = (s < p.num_seqs) ? units * seq_stages(p, s, bs, bps) : 0;
+        const long long w = (s < p.num_seqs) ? units * (kUnitCost + seq_stages(p, s, bs, bps)) : 0;
         long long incl = w;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -527,8 +548,7 @@ __device__ __forceinline__ int find_seq_at(const DecodeParams &p, int bs, int bp
                 incl += v;
         }
         const long long excl = incl - w;
-        const unsigned hit =
-            __ballot_sync(0xffffffffu, s < p.num_seqs && (base + excl >= x || base + incl > x));
+        const unsigned hit = __ballot_sync(0xffffffffu, s < p.num_seqs && base + incl > x);
         if (hit) {
             const int L = __ffs(hit) - 1;
             *base_out = base + __shfl_sync(0xffffffffu, excl, L);
@@ -552,59 +572,66 @@ __device__ __forceinline__ void walk_balanced(const DecodeParams &p, int bs, int
 {
     const long long G = gridDim.x;
     const long long cta = blockIdx.x;
-    const bool last = cta == G - 1;
     const long long units = (long long)p.num_kv_heads * p.head_groups;
     const long long total = stream_total(p, bs, bps, lane);
     const long long s_c = cta * total / G;
     const long long e_c = (cta + 1) * total / G;
+    if (s_c >= e_c)
+        return;
     long long base = 0;
     int s = find_seq_at(p, bs, bps, s_c, &base, lane);
-    for (; s < p.num_seqs && !*pr.c.abort; ++s) {
-        if (base >= e_c && !last)
-            break;
+    for (; s < p.num_seqs && base < e_c && !*pr.c.abort; ++s) {
         const int len = clamp_len(p, s, bs);
         const int nb = (len + bs - 1) / bs;
         const long long ns = (nb + bps - 1) / bps;
+        const long long span = kUnitCost + ns;
         Item it;
         it.seq = s;
         it.len = len;
-        if (ns == 0) {
-            // an empty sequence belongs to the CTA whose range holds its offset
-            if (base >= s_c && (base < e_c || last)) {
-                for (long long u = 0; u < units; ++u) {
-                    it.kvh = (int)(u / p.head_groups);
-                    it.hg = (int)(u % p.head_groups);
-                    it.j0 = it.j1 = 0;
-                    it.qrow0 = it.kvh * p.group + it.hg * kHeadsPerItem;
-                    it.rows = min(kHeadsPerItem, p.group - it.hg * kHeadsPerItem);
-                    it.partial = 0;
-                    it.prow0 = 0;
-                    if (!pr.emit(it))
-                        return;
-                }
-            }
-            continue;
-        }
-        const long long u_lo = s_c > base ? (s_c - base) / ns : 0;
-        const long long u_hi = min(units - 1, (e_c - 1 - base) / ns);
+        it.total_lo = (unsigned int)(total & 0xffffffffll);
+        it.total_hi = (unsigned int)(total >> 32);
+        const long long u_lo = s_c > base ? (s_c - base) / span : 0;
+        const long long u_hi = min(units - 1, (e_c - 1 - base) / span);
         for (long long u = u_lo; u <= u_hi; ++u) {
-            const long long a = base + u * ns;
-            const long long lo = max(a, s_c), hi = min(a + ns, e_c);
-            if (lo >= hi)
-                continue;
+            const long long a = base + u * span;  // unit start (its cost positions)
+            const long long ra = a + kUnitCost;   // first real stage
+            const long long rb = ra + ns;
             it.kvh = (int)(u / p.head_groups);
             it.hg = (int)(u % p.head_groups);
-            it.j0 = (int)((lo - a) * bps);
-            it.j1 = (int)min((hi - a) * bps, (long long)nb);
             it.qrow0 = it.kvh * p.group + it.hg * kHeadsPerItem;
             it.rows = min(kHeadsPerItem, p.group - it.hg * kHeadsPerItem);
-            it.partial = (lo == a && hi == a + ns) ? 0 : 1;
-            // slot 2c: the unit began in an earlier CTA; slot 2c + 1: it goes on after
-            it.prow0 = (int)((2 * cta + (a < s_c ? 0 : 1)) * kHeadsPerItem);
+            it.c_first = -1;
+            it.nparts = 0;
+            if (ns == 0) {
+                // an empty unit belongs to the CTA holding its start: zero output
+                if (a < s_c)
+                    continue;
+                it.j0 = it.j1 = 0;
+                it.partial = 0;
+                it.prow0 = 0;
+            } else {
+                const long long lo = max(ra, s_c), hi = min(rb, e_c);
+                if (lo >= hi)
+                    continue;
+                it.j0 = (int)((lo - ra) * bps);
+                it.j1 = (int)min((hi - ra) * bps, (long long)nb);
+                it.partial = (lo == ra && hi == rb) ? 0 : 1;
+                // slot 2c: the unit's stages began in an earlier CTA; 2c + 1: they go on
+                it.prow0 = (int)((2 * cta + (ra < s_c ? 0 : 1)) * kHeadsPerItem);
+                if (it.partial) {
+                    const long long cf = cta_of(ra, total, G);
+                    const long long cl = cta_of(rb - 1, total, G);
+                    int np = 1;
+                    for (long long cc = cf + 1; cc <= cl; ++cc)
+                        np += (cc * total / G < (cc + 1) * total / G) ? 1 : 0;
+                    it.c_first = (int)cf;
+                    it.nparts = np;
+                }
+            }
             if (!pr.emit(it))
                 return;
         }
-        base += units * ns;
+        base += units * span;
     }
 }
 
@@ -679,6 +706,89 @@ __device__ __forceinline__ void finalize_item(const DecodeParams &p, const Item 
                 p.part_lse[pr] = (L > 0.f) ? M + log2f(L) : -INFINITY;
         }
     }
+}
+
+// ---------------------------------------------------------------------------
+// Balanced split: merge of a unit whose stages several CTAs shared.  Each CTA
+// writes its partial (fp32 output rows + log2-sum-exp), makes it visible
+// (__threadfence) and counts it on the unit's counter; the CTA whose count
+// completes the set merges every partial with the log-sum-exp rule.  No CTA waits
+// for another.  Counters hold (epoch << 32 | count): a value left by an earlier call
+// carries another epoch and counts as zero, so they never need clearing.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ bool count_partial(const DecodeParams &p, const Item &it)
+{
+    unsigned long long *ctr = p.counters + it.c_first;
+    unsigned long long old = *reinterpret_cast<volatile unsigned long long *>(ctr);
+    unsigned int cnt;
+    for (;;) {  // each failed exchange means another CTA counted: at most nparts rounds
+        cnt = (unsigned int)(old >> 32) == p.epoch ? (unsigned int)old : 0u;
+        const unsigned long long want = ((unsigned long long)p.epoch << 32) | (cnt + 1u);
+        const unsigned long long prev = atomicCAS(ctr, old, want);
+        if (prev == old)
+            break;
+        old = prev;
+    }
+    return cnt + 1u == (unsigned int)it.nparts;
+}
+
+template <typename T, int D>
+__device__ __forceinline__ void merge_split_unit(const DecodeParams &p, const Item &it, int tid)
+{
+    const long long total = ((long long)it.total_hi << 32) | (long long)it.total_lo;
+    const long long G = gridDim.x;
+    for (int idx = tid; idx < it.rows * D; idx += 32 * kConsumerWarps) {
+        const int r = idx / D;
+        const int col = idx - r * D;
+        float M = -INFINITY;
+        long long cc = it.c_first;
+        for (int i = 0; i < it.nparts; ++i) {
+            if (i > 0)  // next CTA with a non-empty range
+                do {
+                    ++cc;
+                } while (cc * total / G >= (cc + 1) * total / G);
+            const long long slot = i == 0 ? 2 * cc + 1 : 2 * cc;
+            M = fmaxf(M, __ldcg(p.part_lse + slot * kHeadsPerItem + r));
+        }
+        float W = 0.f, O = 0.f;
+        cc = it.c_first;
+        for (int i = 0; i < it.nparts; ++i) {
+            if (i > 0)
+                do {
+                    ++cc;
+                } while (cc * total / G >= (cc + 1) * total / G);
+            const long long row = (i == 0 ? 2 * cc + 1 : 2 * cc) * kHeadsPerItem + r;
+            const float wgt = exp2f(__ldcg(p.part_lse + row) - M);
+            W += wgt;
+            O = fmaf(wgt, __ldcg(p.part_o + row * D + col), O);
+        }
+        reinterpret_cast<T *>(p.out)[((size_t)it.seq * p.num_q_heads + it.qrow0 + r) * D + col] =
+            dev::from_float<T>(O / W);
+    }
+}
+
+// End of an item for the consumer warps: smem reuse barrier and, for a split unit
+// of the balanced schedule, the count-and-merge step.  False on a timeout.
+template <typename T, int D>
+__device__ __forceinline__ bool finish_item(const DecodeParams &p, const Item &it, const CtaState &c,
+                                            uint32_t &sph)
+{
+    const bool split = p.balanced && it.partial;
+    if (split)
+        __threadfence();  // this thread's partial rows, device-wide, before the count
+    if (!consumer_sync(c, sph))
+        return false;
+    if (!split)
+        return true;
+    if (threadIdx.x == 0)
+        *c.merge = count_partial(p, it) ? 1 : 0;
+    if (!consumer_sync(c, sph))
+        return false;
+    if (*c.merge) {
+        __threadfence();
+        merge_split_unit<T, D>(p, it, threadIdx.x);
+    }
+    return true;
 }
 
 // ---------------------------------------------------------------------------
@@ -934,7 +1044,7 @@ __global__ void __launch_bounds__(kThreads, 2)
             break;
         }
         finalize_item<T, D>(p, it, c.macc, c.mml, rows_cap, threadIdx.x);
-        if (!consumer_sync(c, sph)) {
+        if (!finish_item<T, D>(p, it, c, sph)) {
             if (lane == 0)
                 raise_error(p, c.abort, PA_DEVERR_TIMEOUT_FULL);
             break;
@@ -1134,7 +1244,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
         }
         finalize_item<float, D>(p, it, c.macc, c.mml, rows_cap, threadIdx.x);
-        if (!consumer_sync(c, sph)) {
+        if (!finish_item<float, D>(p, it, c, sph)) {
             if (lane == 0)
                 raise_error(p, c.abort, PA_DEVERR_TIMEOUT_FULL);
             break;
@@ -1206,83 +1316,6 @@ __global__ void __launch_bounds__(128)
 #pragma unroll
     for (int e = 0; e < VEC; ++e)
         o[e] = dev::from_float<T>(acc[e] / W);
-}
-
-// ---------------------------------------------------------------------------
-// Balanced-split merge: one CTA per boundary b between CTAs b-1 and b of the
-// partition grid (G CTAs).  The unit that straddles boundary b is merged by the CTA
-// of its first boundary, from the partials of CTAs c_first .. c_last: slot
-// 2 c_first + 1 (where the unit began), then slot 2 c of every later CTA.
-// ---------------------------------------------------------------------------
-template <typename T, int D>
-__global__ void __launch_bounds__(128)
-    pa_merge_balanced_kernel(const __grid_constant__ DecodeParams p, int block_size, int bps, int G)
-{
-    constexpr int VEC = D / 32;
-    // launched as a programmatic dependent of the partition kernel
-    dev::grid_dependency_wait();
-    const int warp = threadIdx.x >> 5;
-    const int lane = threadIdx.x & 31;
-    const long long b = (long long)blockIdx.x + 1;
-    const long long total = stream_total(p, block_size, bps, lane);
-    if (total == 0)
-        return;
-    const long long x = b * total / G;  // first stage of CTA b
-    long long base = 0;
-    int s = find_seq_at(p, block_size, bps, x, &base, lane);
-    while (s < p.num_seqs && seq_stages(p, s, block_size, bps) == 0)
-        ++s;  // empty sequences sit at x without covering it
-    if (s >= p.num_seqs)
-        return;
-    const long long ns = seq_stages(p, s, block_size, bps);
-    const long long u = (x - base) / ns;
-    const long long a = base + u * ns;
-    if (a == x || cta_of(a, total, G) != b - 1)
-        return;  // not cut here, or cut first at an earlier boundary
-    const long long c_first = b - 1;
-    const int nparts = (int)(cta_of(a + ns - 1, total, G) - c_first + 1);
-    const int kvh = (int)(u / p.head_groups);
-    const int hg = (int)(u % p.head_groups);
-    const int qrow0 = kvh * p.group + hg * kHeadsPerItem;
-    const int rows = min(kHeadsPerItem, p.group - hg * kHeadsPerItem);
-    // CTAs with an empty stage range (more CTAs than stages) wrote nothing
-    auto holds = [&](int i) -> bool {
-        const long long cc = c_first + i;
-        return i == 0 || cc * total / G < (cc + 1) * total / G;
-    };
-    for (int r = warp; r < rows; r += 4) {
-        auto prow = [&](int i) -> size_t {
-            const long long slot = i == 0 ? 2 * c_first + 1 : 2 * (c_first + i);
-            return (size_t)(slot * kHeadsPerItem + r);
-        };
-        float M = -INFINITY;
-        for (int i = lane; i < nparts; i += 32)
-            if (holds(i))
-                M = fmaxf(M, p.part_lse[prow(i)]);
-        M = dev::warp_max(M);
-        float W = 0.f;
-        for (int i = lane; i < nparts; i += 32)
-            if (holds(i))
-                W += exp2f(p.part_lse[prow(i)] - M);
-        W = dev::warp_sum(W);
-        float acc[VEC];
-#pragma unroll
-        for (int e = 0; e < VEC; ++e)
-            acc[e] = 0.f;
-        for (int i = 0; i < nparts; ++i) {
-            if (!holds(i))
-                continue;
-            const float wgt = exp2f(p.part_lse[prow(i)] - M);
-            const float *po = p.part_o + prow(i) * D + lane * VEC;
-#pragma unroll
-            for (int e = 0; e < VEC; ++e)
-                acc[e] = fmaf(wgt, po[e], acc[e]);
-        }
-        T *o = reinterpret_cast<T *>(p.out) + ((size_t)s * p.num_q_heads + qrow0 + r) * D + lane * VEC;
-#pragma unroll
-        for (int e = 0; e < VEC; ++e)
-            o[e] = dev::from_float<T>(acc[e] / W);
-    }
 }
 
 // ---------------------------------------------------------------------------
@@ -1360,11 +1393,7 @@ cudaError_t launch_decode_impl(const DecodeLaunch &L, cudaStream_t stream)
     mcfg.stream = stream;
     mcfg.attrs = attr;
     mcfg.numAttrs = 1;
-    if (p.balanced && grid > 1) {
-        mcfg.gridDim = dim3((unsigned)(grid - 1));
-        e = cudaLaunchKernelEx(&mcfg, pa_merge_balanced_kernel<T, D>, p, (int)BS,
-                               (int)Cfg<T, D, BS>::kBPS, (int)grid);
-    } else if (!p.balanced && p.max_parts > 1) {
+    if (!p.balanced && p.max_parts > 1) {
         mcfg.gridDim = dim3((unsigned)((p.num_q_heads + 3) / 4), (unsigned)p.num_seqs);
         e = cudaLaunchKernelEx(&mcfg, pa_merge_kernel<T, D>, p, (int)BS);
     }

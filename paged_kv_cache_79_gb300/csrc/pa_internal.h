@@ -41,6 +41,8 @@ struct DecodeParams {
     int partition_blocks;         // fixed partitions: blocks per partition
     int max_parts;                // fixed partitions: ceil(max_blocks / partition_blocks)
     int balanced;                 // 1: balanced split over the persistent grid
+    unsigned int epoch;           // balanced split: tag of this call's merge counters
+    unsigned long long *counters; // balanced split: [grid] (epoch << 32 | partials written)
 };
 
 // Balanced split: partial slots are reserved for at most this many CTAs per SM.

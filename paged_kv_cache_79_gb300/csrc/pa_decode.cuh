@@ -732,62 +732,107 @@ __device__ __forceinline__ bool count_partial(const DecodeParams &p, const Item 
     return cnt + 1u == (unsigned int)it.nparts;
 }
 
-template <typename T, int D>
-__device__ __forceinline__ void merge_split_unit(const DecodeParams &p, const Item &it, int tid)
+// Partial row i (0-based) of a split unit: slot 2 c_first + 1, then slot 2 c of the
+// next CTAs that hold stages (a CTA range is empty only when the stream has fewer
+// positions than the grid has CTAs; otherwise the CTAs are consecutive).
+__device__ __forceinline__ long long split_slot(const Item &it, int i, long long total, long long G)
 {
+    if (i == 0)
+        return 2ll * it.c_first + 1;
+    if (total >= G)
+        return 2ll * (it.c_first + i);
+    long long cc = it.c_first;
+    for (int k = 0; k < i; ++k)
+        do {
+            ++cc;
+        } while (cc * total / G >= (cc + 1) * total / G);
+    return 2 * cc;
+}
+
+// Merge the nparts partials of a split unit into its output rows: one warp per
+// query head; lane i holds partial i's log2-sum-exp.
+template <typename T, int D>
+__device__ __forceinline__ void merge_split_unit(const DecodeParams &p, const Item &it, int warp,
+                                                 int lane)
+{
+    constexpr int VEC = D / 32;
     const long long total = ((long long)it.total_hi << 32) | (long long)it.total_lo;
     const long long G = gridDim.x;
-    for (int idx = tid; idx < it.rows * D; idx += 32 * kConsumerWarps) {
-        const int r = idx / D;
-        const int col = idx - r * D;
+    for (int r = warp; r < it.rows; r += kConsumerWarps) {
         float M = -INFINITY;
-        long long cc = it.c_first;
-        for (int i = 0; i < it.nparts; ++i) {
-            if (i > 0)  // next CTA with a non-empty range
-                do {
-                    ++cc;
-                } while (cc * total / G >= (cc + 1) * total / G);
-            const long long slot = i == 0 ? 2 * cc + 1 : 2 * cc;
-            M = fmaxf(M, __ldcg(p.part_lse + slot * kHeadsPerItem + r));
+        for (int i0 = 0; i0 < it.nparts; i0 += 32) {
+            const int i = i0 + lane;
+            if (i < it.nparts)
+                M = fmaxf(M, __ldcg(p.part_lse + split_slot(it, i, total, G) * kHeadsPerItem + r));
         }
-        float W = 0.f, O = 0.f;
-        cc = it.c_first;
-        for (int i = 0; i < it.nparts; ++i) {
-            if (i > 0)
-                do {
-                    ++cc;
-                } while (cc * total / G >= (cc + 1) * total / G);
-            const long long row = (i == 0 ? 2 * cc + 1 : 2 * cc) * kHeadsPerItem + r;
-            const float wgt = exp2f(__ldcg(p.part_lse + row) - M);
+        M = dev::warp_max(M);
+        float W = 0.f;
+        float acc[VEC];
+#pragma unroll
+        for (int e = 0; e < VEC; ++e)
+            acc[e] = 0.f;
+        for (int i0 = 0; i0 < it.nparts; i0 += 32) {
+            const int i = i0 + lane;
+            long long row = 0;
+            float wgt = 0.f;
+            if (i < it.nparts) {
+                row = split_slot(it, i, total, G) * kHeadsPerItem + r;
+                wgt = exp2f(__ldcg(p.part_lse + row) - M);
+            }
             W += wgt;
-            O = fmaf(wgt, __ldcg(p.part_o + row * D + col), O);
+            const int n = min(32, it.nparts - i0);
+            for (int k0 = 0; k0 < n; k0 += 4) {
+                float v[4][VEC], wk[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int k = min(k0 + u, n - 1);
+                    const long long rk = __shfl_sync(0xffffffffu, row, k);
+                    wk[u] = (k0 + u < n) ? __shfl_sync(0xffffffffu, wgt, k) : 0.f;
+                    const float *po = p.part_o + rk * D + lane * VEC;
+#pragma unroll
+                    for (int e = 0; e < VEC; ++e)
+                        v[u][e] = __ldcg(po + e);
+                }
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+#pragma unroll
+                    for (int e = 0; e < VEC; ++e)
+                        acc[e] = fmaf(wk[u], v[u][e], acc[e]);
+            }
         }
-        reinterpret_cast<T *>(p.out)[((size_t)it.seq * p.num_q_heads + it.qrow0 + r) * D + col] =
-            dev::from_float<T>(O / W);
+        W = dev::warp_sum(W);
+        T *o = reinterpret_cast<T *>(p.out) + ((size_t)it.seq * p.num_q_heads + it.qrow0 + r) * D +
+               lane * VEC;
+#pragma unroll
+        for (int e = 0; e < VEC; ++e)
+            o[e] = dev::from_float<T>(acc[e] / W);
     }
 }
 
-// End of an item for the consumer warps: smem reuse barrier and, for a split unit
-// of the balanced schedule, the count-and-merge step.  False on a timeout.
+// End of an item for the consumer warps: shared-memory reuse barrier and, for a
+// split unit of the balanced schedule, the count-and-merge step.  The barrier
+// orders every consumer thread's partial stores before thread 0's GPU-scope fence
+// and count (fences are cumulative); the merging CTA fences again before reading.
+// False on a timeout.
 template <typename T, int D>
 __device__ __forceinline__ bool finish_item(const DecodeParams &p, const Item &it, const CtaState &c,
-                                            uint32_t &sph)
+                                            uint32_t &sph, int warp, int lane)
 {
     const bool split = p.balanced && it.partial;
-    if (split)
-        __threadfence();  // this thread's partial rows, device-wide, before the count
     if (!consumer_sync(c, sph))
         return false;
     if (!split)
         return true;
-    if (threadIdx.x == 0)
-        *c.merge = count_partial(p, it) ? 1 : 0;
+    if (threadIdx.x == 0) {
+        dev::fence_acq_rel_gpu();
+        const bool last = count_partial(p, it);
+        dev::fence_acq_rel_gpu();
+        *c.merge = last ? 1 : 0;
+    }
     if (!consumer_sync(c, sph))
         return false;
-    if (*c.merge) {
-        __threadfence();
-        merge_split_unit<T, D>(p, it, threadIdx.x);
-    }
+    if (*c.merge)
+        merge_split_unit<T, D>(p, it, warp, lane);
     return true;
 }
 
@@ -843,11 +888,18 @@ __global__ void __launch_bounds__(kThreads, 2)
 #endif
     for (uint32_t n = 0;; ++n) {
         const uint32_t slot = n % kItemSlots;
+#ifdef PA_TRACE
+        const unsigned long long t_iw = dev::global_timer_ns();
+#endif
         if (!warp_wait(&c.item_full[slot], (n / kItemSlots) & 1u)) {
             if (lane == 0)
                 raise_error(p, c.abort, PA_DEVERR_TIMEOUT_FULL);
             break;
         }
+#ifdef PA_TRACE
+        if (threadIdx.x == 0)
+            PA_TRACE_ADD(12, dev::global_timer_ns() - t_iw);
+#endif
         const Item it = load_item(&c.items[slot]);
         if (it.seq < 0)
             break;
@@ -894,6 +946,9 @@ __global__ void __launch_bounds__(kThreads, 2)
             if ((int)(g % kConsumerWarps) != warp)
                 continue;
             const uint32_t st = g % C::kStages;
+#ifdef PA_TRACE
+            const unsigned long long t_sw = dev::global_timer_ns();
+#endif
             if (!warp_wait(&c.full[st], (g / C::kStages) & 1u)) {
                 if (lane == 0)
                     raise_error(p, c.abort, PA_DEVERR_TIMEOUT_FULL);
@@ -901,9 +956,14 @@ __global__ void __launch_bounds__(kThreads, 2)
                 break;
             }
 #ifdef PA_TRACE
-            if (threadIdx.x == 0 && first_tile) {
-                PA_TRACE_SET(1, dev::global_timer_ns());
-                first_tile = false;
+            if (threadIdx.x == 0) {
+                const unsigned long long t_now = dev::global_timer_ns();
+                PA_TRACE_ADD(13, t_now - t_sw);
+                PA_TRACE_SET(11, t_now);
+                if (first_tile) {
+                    PA_TRACE_SET(1, t_now);
+                    first_tile = false;
+                }
             }
 #endif
             // tokens of this stage that count: the loaded blocks, up to the context
@@ -1013,6 +1073,9 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
         if (!alive)
             break;
+#ifdef PA_TRACE
+        const unsigned long long t_m0 = dev::global_timer_ns();
+#endif
 
         // ---- merge the four consumer warps ----
         lrow0 += __shfl_xor_sync(0xffffffffu, lrow0, 1);
@@ -1044,11 +1107,18 @@ __global__ void __launch_bounds__(kThreads, 2)
             break;
         }
         finalize_item<T, D>(p, it, c.macc, c.mml, rows_cap, threadIdx.x);
-        if (!finish_item<T, D>(p, it, c, sph)) {
+        if (!finish_item<T, D>(p, it, c, sph, warp, lane)) {
             if (lane == 0)
                 raise_error(p, c.abort, PA_DEVERR_TIMEOUT_FULL);
             break;
         }
+#ifdef PA_TRACE
+        if (threadIdx.x == 0) {
+            PA_TRACE_ADD(9, dev::global_timer_ns() - t_m0);
+            if (p.balanced && it.partial && *c.merge)
+                PA_TRACE_ADD(10, 1);
+        }
+#endif
         if (*c.abort)
             break;
     }
@@ -1244,7 +1314,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
         }
         finalize_item<float, D>(p, it, c.macc, c.mml, rows_cap, threadIdx.x);
-        if (!finish_item<float, D>(p, it, c, sph)) {
+        if (!finish_item<float, D>(p, it, c, sph, warp, lane)) {
             if (lane == 0)
                 raise_error(p, c.abort, PA_DEVERR_TIMEOUT_FULL);
             break;

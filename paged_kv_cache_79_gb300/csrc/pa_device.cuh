@@ -107,6 +107,11 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_
 // the memory they were read from.
 __device__ __forceinline__ void settle_loads(volatile uint32_t *sink, uint32_t v) { *sink = v; }
 
+// GPU-scope acquire-release fence: orders this thread's earlier memory operations
+// (and, cumulatively, those it has observed through a CTA barrier) before its later
+// ones, as seen by any thread of the GPU.
+__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+
 // ---- programmatic dependent launch ------------------------------------------------
 // Block until the grids this one depends on have completed and their writes are
 // visible (returns at once when the launch had no programmatic dependency).

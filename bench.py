@@ -2,10 +2,12 @@
 """Paged decode attention benchmark: one JSON line on rank 0.
 
 A step is one decode iteration of the whole hot path over one batch: the
-copy-on-write block copies (pa_copy_blocks), the new tokens' K/V append
-(pa_reshape_and_cache) and the decode attention (pa_decode: partition kernel +
-split-KV merge kernel), on inputs already resident in HBM.  The workload's
-allocator script (untimed) prepares the caches and tables.
+copy-on-write block copies (pa_copy_blocks, when the step has any), then the new
+tokens' K/V append fused with the decode attention (pa_decode_append: append +
+partition kernel with the split-KV merge inside), on inputs already resident in
+HBM.  The workload's allocator script (untimed) prepares the caches and tables.
+The split is the balanced one (partition_size 0) unless --partition-size says
+otherwise.
 
 Metric: KV GB/s (algorithmic bytes of the step / device time of the step); the
 line also carries seq*layers/s (one pa_decode call = one layer), the roofline of
@@ -174,10 +176,12 @@ class ClockSampler:
 # ----------------------------------------------------------------------------
 # our arm
 # ----------------------------------------------------------------------------
-def prepare(name, device, seed_offset=0):
+def prepare(name, device, seed_offset=0, partition_size=None):
     import workloads as W
     from paged_kv_cache_79_gb300 import runner
     w = W.by_name(name)
+    if partition_size is not None:
+        w.partition_size = partition_size
     if seed_offset:
         w.data_seed += 97 * seed_offset
     kc, vc = W.pool_tensors(w, device)
@@ -246,7 +250,7 @@ def run_ours(args):
 
     from paged_kv_cache_79_gb300 import build as libbuild
     libbuild.build()
-    w, ds, bt, cl = prepare(args.workload, device, seed_offset=rank)
+    w, ds, bt, cl = prepare(args.workload, device, seed_offset=rank, partition_size=args.partition_size)
     n_tok = int(ds.slots.shape[0])
     n_pairs = int(ds.pairs.shape[0])
     by = step_bytes(w, bt, cl, n_tok, n_pairs)
@@ -259,11 +263,14 @@ def run_ours(args):
     # balanced split (0): one partition kernel (split units merge in it); fixed
     # partitions: plus the merge kernel when a table spans several partitions
     merge = parts > 0 and -(-bt.shape[1] // (parts // w.block_size)) > 1
-    launches_per_step = (1 if n_pairs else 0) + (1 if n_tok else 0) + 1 + (1 if merge else 0)
+    fused = ds.fusable
+    launches_per_step = ((1 if n_pairs else 0) + (0 if fused or not n_tok else 1) + 1 +
+                         (1 if merge else 0))
 
     with torch.cuda.stream(stream):
+        step = ds.run_fused if fused else ds.run
         for _ in range(args.warmup):
-            ds.run(stream)
+            step(stream)
         torch.cuda.synchronize(device)
         if world > 1:
             dist.barrier()
@@ -281,9 +288,16 @@ def run_ours(args):
             e0.record(stream)
             if n_pairs:
                 P.pa_copy_blocks(ds.k_cache, ds.v_cache, ds.pairs, stream)
-            P.pa_reshape_and_cache(ds.step_k, ds.step_v, ds.k_cache, ds.v_cache, ds.slots, stream)
+            if not fused:
+                P.pa_reshape_and_cache(ds.step_k, ds.step_v, ds.k_cache, ds.v_cache, ds.slots, stream)
             e1.record(stream)
-            ds.decode(stream)
+            if fused:
+                P.pa_decode_append(ds.out, ds.q, ds.k_cache, ds.v_cache, ds.step_k, ds.step_v,
+                                   ds.block_tables, ds.context_lens, ds.scale, ds.num_q_heads,
+                                   ds.num_kv_heads, ds.head_dim, ds.block_size, ds.partition_size,
+                                   ds.workspace, stream)
+            else:
+                ds.decode(stream)
             e2.record(stream)
         torch.cuda.synchronize(device)
         wall = time.perf_counter() - t_wall
@@ -307,7 +321,8 @@ def run_ours(args):
         return None
     value = world * by["step"] / (t_step * 1e-3) / 1e9
     peak, peak_kind = measured_peak()
-    achieved = by["decode"] / (t_dec * 1e-3) / 1e9
+    dec_bytes = by["decode"] + (by["append"] if fused else 0)
+    achieved = dec_bytes / (t_dec * 1e-3) / 1e9
     line = {
         "metric": METRIC,
         "value": round(value, 2),
@@ -326,6 +341,7 @@ def run_ours(args):
                    "num_blocks": w.num_blocks, "context_tokens": int(np.sum(cl)),
                    "max_context": int(np.max(cl)),
                    "split": "balanced" if parts == 0 else f"fixed partitions of {parts} tokens",
+                   "append": "fused into the decode launch" if fused else "separate launch",
                    "appended_tokens": n_tok,
                    "cow_pairs": n_pairs,
                    "l2": "flushed before every timed step (512 MB write, then 1 GB read)",
@@ -337,7 +353,8 @@ def run_ours(args):
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_kind": f"{peak_kind} copy bandwidth",
                      "traffic": profiled_traffic(w.name),
-                     "kernel": "pa_decode (partition kernel; split-KV merge fused or second kernel)"},
+                     "kernel": ("pa_decode_append (append + decode partition kernel, merge inside)" if fused
+                                else "pa_decode (partition kernel; split-KV merge fused or second kernel)")},
         "e2e": e2e,
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk,
@@ -374,7 +391,7 @@ def run_e2e(ds, stream, device, args, by):
             a.record(stream)
             for name, t in host.items():
                 getattr(ds, name).copy_(t, non_blocking=True)
-            ds.run(stream)
+            ds.run_fused(stream) if ds.fusable else ds.run(stream)
             out_h.copy_(ds.out, non_blocking=True)
             b.record(stream)
             b.synchronize()
@@ -441,6 +458,8 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--partition-size", type=int, default=0,
+                    help="0: balanced split (default); >0: fixed partitions of that many tokens")
     ap.add_argument("--cpu-budget", type=float, default=10.0)
     args = ap.parse_args()
     if args.warmup < 3:

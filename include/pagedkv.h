@@ -121,6 +121,27 @@ pa_status pa_decode(void *out, const void *q, const void *k_cache, const void *v
                     size_t workspace_bytes, void *stream);
 
 /*
+ * pa_decode_append -- append each sequence's newest token and decode, in one launch.
+ *
+ * Same result as pa_reshape_and_cache of the newest tokens followed by pa_decode
+ * ([T] §3.1 append_kv then §3.2 compute, the per-step loop of [T] §4): for every
+ * sequence s with T = context_lens[s] >= 1, position T - 1 is the new token; its
+ * K and V rows are k_new[s], v_new[s] ([S][Hkv][d], dtype `dtype`).  They are
+ * written into the caches at that position's slot (block_tables[s][(T-1)/B] * B +
+ * (T-1) % B, which the allocator's pa_alloc_append returned), and the attention
+ * over positions 0 .. T-1 uses them.  Copy-on-write pairs of the step must be
+ * applied (pa_copy_blocks) before the call.  Sequences with T = 0 write nothing
+ * and yield zeros.  Other arguments, workspace and errors as pa_decode;
+ * PA_ERR_INVALID also for null or misaligned k_new / v_new.
+ */
+pa_status pa_decode_append(void *out, const void *q, void *k_cache, void *v_cache,
+                           const void *k_new, const void *v_new, const int32_t *block_tables,
+                           int max_blocks_per_seq, const int32_t *context_lens, int num_seqs,
+                           int num_blocks, float scale, int num_q_heads, int num_kv_heads,
+                           int head_dim, int block_size, pa_dtype dtype, int partition_size,
+                           void *workspace, size_t workspace_bytes, void *stream);
+
+/*
  * Partition size pa_decode uses for these arguments: 0 for the balanced split,
  * else the fixed partition size (capped at the table capacity).  Returns -1 for
  * invalid arguments.

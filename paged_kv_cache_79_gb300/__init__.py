@@ -6,6 +6,7 @@ of the computation runs in the library's CUDA kernels.  There is no CPU path:
 calls on tensors that are not CUDA tensors raise.
 
     pa_decode               paged single-query attention (partition + merge kernels)
+    pa_decode_append        the newest tokens' append fused with the decode
     pa_reshape_and_cache    write new tokens' K/V rows through a slot mapping
     pa_copy_blocks          copy-on-write block copies
     BlockAllocator          host ref-counted block allocator (pa_alloc_*)
@@ -114,6 +115,32 @@ def pa_decode(out, q, k_cache, v_cache, block_tables, context_lens, scale: float
                            num_q_heads, num_kv_heads, head_dim, block_size, _dtype_code(q),
                            partition_size, ws_ptr, ws_bytes, _stream(stream))
     _check(st, "pa_decode")
+    return out
+
+
+def pa_decode_append(out, q, k_cache, v_cache, k_new, v_new, block_tables, context_lens,
+                     scale: float, num_q_heads: int, num_kv_heads: int, head_dim: int,
+                     block_size: int, partition_size: int = 0, workspace=None, stream=None):
+    """Append each sequence's newest token (k_new/v_new [S, Hkv, d], position
+    context_lens[s] - 1) to the caches and decode, in one launch; the same result as
+    pa_reshape_and_cache followed by pa_decode."""
+    import torch
+    S = q.shape[0]
+    W = block_tables.shape[1]
+    if workspace is None:
+        workspace = alloc_workspace(S, num_q_heads, num_kv_heads, head_dim, block_size, W,
+                                    partition_size, q.device)
+    ws_ptr = _cuda(workspace, "workspace") if workspace is not None else None
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    if block_tables.dtype != torch.int32 or context_lens.dtype != torch.int32:
+        raise TypeError("block_tables and context_lens must be int32")
+    st = _load().pa_decode_append(_cuda(out, "out"), _cuda(q, "q"), _cuda(k_cache, "k_cache"),
+                                  _cuda(v_cache, "v_cache"), _cuda(k_new, "k_new"),
+                                  _cuda(v_new, "v_new"), _cuda(block_tables, "block_tables"), W,
+                                  _cuda(context_lens, "context_lens"), S, k_cache.shape[0],
+                                  float(scale), num_q_heads, num_kv_heads, head_dim, block_size,
+                                  _dtype_code(q), partition_size, ws_ptr, ws_bytes, _stream(stream))
+    _check(st, "pa_decode_append")
     return out
 
 
@@ -268,6 +295,6 @@ class BlockAllocator:
         return out[:n.value].tolist()
 
 
-__all__ = ["pa_decode", "pa_decode_noalloc", "pa_decode_workspace_size", "pa_decode_partition_size", "alloc_workspace",
+__all__ = ["pa_decode", "pa_decode_append", "pa_decode_noalloc", "pa_decode_workspace_size", "pa_decode_partition_size", "alloc_workspace",
            "pa_reshape_and_cache", "pa_copy_blocks", "pa_device_errors", "pa_status_string",
            "BlockAllocator", "PagedKVError", "OutOfBlocks", "library_path"]

@@ -22,6 +22,9 @@ SIGNATURES = {
     "pa_decode": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_void_p, c_int,
                           c_int, c_float, c_int, c_int, c_int, c_int, c_int, c_int, c_void_p,
                           c_size_t, c_void_p]),
+    "pa_decode_append": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
+                                 c_int, c_void_p, c_int, c_int, c_float, c_int, c_int, c_int, c_int,
+                                 c_int, c_int, c_void_p, c_size_t, c_void_p]),
     "pa_decode_noalloc": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_void_p,
                                   c_int, c_int, c_float, c_int, c_int, c_int, c_int, c_int, c_int,
                                   c_void_p]),

@@ -250,12 +250,17 @@ size_t pa_decode_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads,
     return bytes + rows * 4;
 }
 
-pa_status pa_decode(void *out, const void *q, const void *k_cache, const void *v_cache,
-                    const int32_t *block_tables, int max_blocks_per_seq,
-                    const int32_t *context_lens, int num_seqs, int num_blocks, float scale,
-                    int num_q_heads, int num_kv_heads, int head_dim, int block_size,
-                    pa_dtype dtype, int partition_size, void *workspace, size_t workspace_bytes,
-                    void *stream)
+}  // extern "C"
+
+namespace {
+
+// pa_decode and pa_decode_append: k_new/v_new null for a plain decode.
+pa_status decode_impl(void *out, const void *q, const void *k_cache, const void *v_cache,
+                      const int32_t *block_tables, int max_blocks_per_seq,
+                      const int32_t *context_lens, int num_seqs, int num_blocks, float scale,
+                      int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                      pa_dtype dtype, int partition_size, void *workspace, size_t workspace_bytes,
+                      const void *k_new, const void *v_new, void *stream)
 {
     if (num_seqs == 0)
         return PA_OK;
@@ -329,6 +334,10 @@ pa_status pa_decode(void *out, const void *q, const void *k_cache, const void *v
     p.partition_blocks = pb;
     p.max_parts = parts;
     p.balanced = balanced ? 1 : 0;
+    p.k_new = k_new;
+    p.v_new = v_new;
+    p.k_cache = const_cast<void *>(k_cache);
+    p.v_cache = const_cast<void *>(v_cache);
     L.head_dim = head_dim;
     L.block_size = block_size;
     L.sm_count = sms;
@@ -348,6 +357,36 @@ pa_status pa_decode(void *out, const void *q, const void *k_cache, const void *v
     if (e != cudaSuccess)
         return cuda_fail(e);
     return PA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+pa_status pa_decode(void *out, const void *q, const void *k_cache, const void *v_cache,
+                    const int32_t *block_tables, int max_blocks_per_seq,
+                    const int32_t *context_lens, int num_seqs, int num_blocks, float scale,
+                    int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                    pa_dtype dtype, int partition_size, void *workspace, size_t workspace_bytes,
+                    void *stream)
+{
+    return decode_impl(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
+                       num_seqs, num_blocks, scale, num_q_heads, num_kv_heads, head_dim, block_size,
+                       dtype, partition_size, workspace, workspace_bytes, nullptr, nullptr, stream);
+}
+
+pa_status pa_decode_append(void *out, const void *q, void *k_cache, void *v_cache,
+                           const void *k_new, const void *v_new, const int32_t *block_tables,
+                           int max_blocks_per_seq, const int32_t *context_lens, int num_seqs,
+                           int num_blocks, float scale, int num_q_heads, int num_kv_heads,
+                           int head_dim, int block_size, pa_dtype dtype, int partition_size,
+                           void *workspace, size_t workspace_bytes, void *stream)
+{
+    if (num_seqs != 0 && (!k_new || !v_new || !aligned(k_new, 16) || !aligned(v_new, 16)))
+        return PA_ERR_INVALID;
+    return decode_impl(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
+                       num_seqs, num_blocks, scale, num_q_heads, num_kv_heads, head_dim, block_size,
+                       dtype, partition_size, workspace, workspace_bytes, k_new, v_new, stream);
 }
 
 pa_status pa_reshape_and_cache(const void *k, const void *v, void *k_cache, void *v_cache,

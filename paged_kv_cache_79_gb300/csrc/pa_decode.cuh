@@ -108,7 +108,7 @@ __device__ __forceinline__ void trace_add(int slot, unsigned long long v)
 #endif
 
 struct SmemLayout {
-    uint32_t acc, ml, items, q, bars, flag, total;
+    uint32_t acc, ml, items, q, newrow, newinfo, bars, flag, total;
 };
 
 constexpr int kItemSlots = 2;  // work-item descriptors (and their query rows) in flight
@@ -129,6 +129,10 @@ __host__ __device__ inline SmemLayout make_layout(int stages, int stage_bytes, i
     o += kItemSlots * 64u;
     L.q = o;
     o += (uint32_t)(kItemSlots * kHeadsPerItem * D * elem_bytes);
+    L.newrow = o;  // per stage: the newest token's K row then V row (fused append)
+    o += (uint32_t)(stages * 2 * D * elem_bytes);
+    L.newinfo = o;  // per stage: {row in the stage tile or -1, physical block}
+    o += (uint32_t)(stages * 8);
     o = (o + 15u) & ~15u;
     L.bars = o;
     o += (2u * (uint32_t)stages + 2u * kItemSlots + 1u) * 8u;
@@ -237,6 +241,8 @@ struct CtaState {
     float *mml;
     Item *items;
     uint8_t *qslots;
+    uint8_t *newrow;                   // per ring stage: fused-append K/V rows
+    volatile int *newinfo;             // per ring stage: {row or -1, physical block}
     uint64_t *full, *empty;            // per ring stage
     uint64_t *item_full, *item_empty;  // per item slot
     uint64_t *csync;                   // consumer-only barrier (all consumer threads arrive)
@@ -253,6 +259,8 @@ __device__ __forceinline__ CtaState cta_state(uint8_t *smem, const SmemLayout &l
     c.mml = reinterpret_cast<float *>(smem + lay.ml);
     c.items = reinterpret_cast<Item *>(smem + lay.items);
     c.qslots = smem + lay.q;
+    c.newrow = smem + lay.newrow;
+    c.newinfo = reinterpret_cast<volatile int *>(smem + lay.newinfo);
     c.full = reinterpret_cast<uint64_t *>(smem + lay.bars);
     c.empty = c.full + stages;
     c.item_full = c.empty + stages;
@@ -429,7 +437,22 @@ struct Producer {
                 if (lane == 0) {
                     constexpr int kRowsPerStage = kTileBytes / (kChunks * 128);
                     const uint32_t fb = dev::smem_addr(&c.full[st]);
-                    dev::mbar_arrive_expect_tx(fb, 2u * (uint32_t)nbs * (kTileBytes / kBPS));
+                    // fused append: does this stage hold the sequence's newest token?
+                    const int newest = it.len - 1 - (jb + i) * BS;
+                    const bool has_new = p.k_new != nullptr && newest >= 0 && newest < nbs * BS;
+                    c.newinfo[2 * st] = has_new ? newest : -1;
+                    if (has_new)
+                        c.newinfo[2 * st + 1] = ph[newest / BS];
+                    constexpr uint32_t kRowBytes = D * sizeof(T);
+                    dev::mbar_arrive_expect_tx(
+                        fb, 2u * (uint32_t)nbs * (kTileBytes / kBPS) + (has_new ? 2u * kRowBytes : 0u));
+                    if (has_new) {
+                        const size_t src = ((size_t)it.seq * p.num_kv_heads + it.kvh) * D;
+                        const uint32_t nr = dev::smem_addr(c.newrow + (size_t)st * 2 * kRowBytes);
+                        dev::bulk_load(nr, reinterpret_cast<const T *>(p.k_new) + src, kRowBytes, fb);
+                        dev::bulk_load(nr + kRowBytes, reinterpret_cast<const T *>(p.v_new) + src,
+                                       kRowBytes, fb);
+                    }
                     const uint32_t kd = dev::smem_addr(c.ring + (size_t)st * 2 * kTileBytes);
                     const uint32_t vd = kd + kTileBytes;
 #pragma unroll
@@ -753,7 +776,7 @@ __device__ __forceinline__ long long split_slot(const Item &it, int i, long long
 // query head; lane i holds partial i's log2-sum-exp.
 template <typename T, int D>
 __device__ __forceinline__ void merge_split_unit(const DecodeParams &p, const Item &it, int warp,
-                                                 int lane)
+                                              int lane)
 {
     constexpr int VEC = D / 32;
     const long long total = ((long long)it.total_hi << 32) | (long long)it.total_lo;
@@ -834,6 +857,42 @@ __device__ __forceinline__ bool finish_item(const DecodeParams &p, const Item &i
     if (*c.merge)
         merge_split_unit<T, D>(p, it, warp, lane);
     return true;
+}
+
+// ---------------------------------------------------------------------------
+// Fused append: copy the newest token's K and V rows (staged by the producer next
+// to the stage) into row `r` of the stage's swizzled tiles, and store them into the
+// cache at (physical block, r % block_size).  Nothing else in the launch reads those
+// cache bytes: only this (sequence, kv head) unit covers them, and it uses the
+// staged copy.  One 16-byte unit per lane per pass.
+// ---------------------------------------------------------------------------
+template <typename T, int D, int TS, int BS>
+__device__ __forceinline__ void patch_newest_row(const DecodeParams &p, const Item &it,
+                                              const CtaState &c, uint32_t st, uint8_t *ktile,
+                                              uint8_t *vtile, int lane)
+{
+    constexpr int kUnits = D * (int)sizeof(T) / 16;  // 16-byte units per row
+    constexpr int kUnitElems = 16 / (int)sizeof(T);
+    constexpr int kCE = 128 / (int)sizeof(T);
+    const int r = c.newinfo[2 * st];
+    const int blk = c.newinfo[2 * st + 1];
+    const uint8_t *staged = c.newrow + (size_t)st * 2 * D * sizeof(T);
+    const size_t dst = (((size_t)blk * BS + r % BS) * p.num_kv_heads + it.kvh) * D;
+    const bool store = it.hg == 0 && blk >= 0 && blk < p.num_blocks;
+    for (int idx = lane; idx < 2 * kUnits; idx += 32) {
+        const bool isv = idx >= kUnits;
+        const int u = isv ? idx - kUnits : idx;
+        const uint4 val = *reinterpret_cast<const uint4 *>(staged + (isv ? D * sizeof(T) : 0) + u * 16);
+        const int d0 = u * kUnitElems;
+        const int ch = d0 / kCE;
+        const int uc = (d0 % kCE) / kUnitElems;
+        *reinterpret_cast<uint4 *>((isv ? vtile : ktile) + ch * (TS * 128) + r * 128 +
+                                   ((uc ^ (r & 7)) << 4)) = val;
+        if (store)
+            *reinterpret_cast<uint4 *>(reinterpret_cast<T *>(isv ? p.v_cache : p.k_cache) + dst + d0) =
+                val;
+    }
+    __syncwarp();
 }
 
 // ---------------------------------------------------------------------------
@@ -970,6 +1029,10 @@ __global__ void __launch_bounds__(kThreads, 2)
             const int valid = min(min(C::kBPS, it.j1 - j) * BS, it.len - j * BS);
             const uint32_t kb = dev::smem_addr(c.ring + (size_t)st * C::kStageBytes);
             const uint32_t vb = kb + C::kTileBytes;
+            if (c.newinfo[2 * st] >= 0)
+                patch_newest_row<T, D, TS, BS>(p, it, c, st, c.ring + (size_t)st * C::kStageBytes,
+                                               c.ring + (size_t)st * C::kStageBytes + C::kTileBytes,
+                                               lane);
 
             // S = Q K^T: K tile rows are tokens, so plain ldmatrix yields the
             // "col" B fragment (k = head dim, n = token).
@@ -1201,6 +1264,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int valid = min(BS, it.len - j * BS);
             const uint8_t *kt = c.ring + (size_t)st * C::kStageBytes;
             const uint8_t *vt = kt + C::kTileBytes;
+            if (c.newinfo[2 * st] >= 0)
+                patch_newest_row<float, D, BS, BS>(p, it, c, st, c.ring + (size_t)st * C::kStageBytes,
+                                                   c.ring + (size_t)st * C::kStageBytes +
+                                                       C::kTileBytes,
+                                                   lane);
 
             float sc[H];
 #pragma unroll

@@ -43,6 +43,13 @@ struct DecodeParams {
     int balanced;                 // 1: balanced split over the persistent grid
     unsigned int epoch;           // balanced split: tag of this call's merge counters
     unsigned long long *counters; // balanced split: [grid] (epoch << 32 | partials written)
+    // Fused append (null when off): the newest token of every sequence (position
+    // context_len - 1) takes its K/V rows from k_new/v_new [S][Hkv][D] instead of the
+    // cache, and the kernel writes them into the cache at that position's slot.
+    const void *k_new;
+    const void *v_new;
+    void *k_cache;
+    void *v_cache;
 };
 
 // Balanced split: partial slots are reserved for at most this many CTAs per SM.

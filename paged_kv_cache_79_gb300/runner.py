@@ -13,7 +13,8 @@ from typing import Callable, List, Optional
 
 import numpy as np
 
-from . import BlockAllocator, alloc_workspace, pa_copy_blocks, pa_decode, pa_reshape_and_cache
+from . import (BlockAllocator, alloc_workspace, pa_copy_blocks, pa_decode, pa_decode_append,
+               pa_reshape_and_cache)
 
 
 def _kind(ev) -> str:
@@ -51,6 +52,7 @@ class DecodeStep:
     head_dim: int
     block_size: int
     partition_size: int = 0
+    fusable: bool = True        # step rows are the batch's newest tokens, in batch order
 
     def run(self, stream=None):
         """copy-on-write pairs, then the new tokens' K/V, then decode."""
@@ -58,6 +60,16 @@ class DecodeStep:
             pa_copy_blocks(self.k_cache, self.v_cache, self.pairs, stream)
         pa_reshape_and_cache(self.step_k, self.step_v, self.k_cache, self.v_cache, self.slots, stream)
         return self.decode(stream)
+
+    def run_fused(self, stream=None):
+        """copy-on-write pairs, then one launch that appends the new tokens and decodes
+        (step_k/step_v rows are the decoded sequences' newest tokens, in batch order)."""
+        if self.pairs.shape[0]:
+            pa_copy_blocks(self.k_cache, self.v_cache, self.pairs, stream)
+        return pa_decode_append(self.out, self.q, self.k_cache, self.v_cache, self.step_k, self.step_v,
+                                self.block_tables, self.context_lens, self.scale, self.num_q_heads,
+                                self.num_kv_heads, self.head_dim, self.block_size, self.partition_size,
+                                self.workspace, stream)
 
     def decode(self, stream=None):
         return pa_decode(self.out, self.q, self.k_cache, self.v_cache, self.block_tables,
@@ -100,6 +112,8 @@ def execute(w, k_cache, v_cache, step_kv: Callable, query: Callable,
                 if cow is not None:
                     pairs.append(cow)
             k, v = step_kv(ev)
+            # the fused append pairs row i of the step's K/V with batch sequence i
+            fusable = list(ev.seqs) == list(w.decode_seqs)
             bt, cl = tables_for(alloc, w.decode_seqs, width)
             S = len(w.decode_seqs)
             q = query(ev)
@@ -112,7 +126,8 @@ def execute(w, k_cache, v_cache, step_kv: Callable, query: Callable,
                 workspace=alloc_workspace(S, w.num_q_heads, w.num_kv_heads, w.head_dim, w.block_size,
                                           bt.shape[1], w.partition_size, dev),
                 scale=w.softmax_scale, num_q_heads=w.num_q_heads, num_kv_heads=w.num_kv_heads,
-                head_dim=w.head_dim, block_size=w.block_size, partition_size=w.partition_size)
+                head_dim=w.head_dim, block_size=w.block_size, partition_size=w.partition_size,
+                fusable=fusable)
             if ds.pairs.shape[0]:
                 pa_copy_blocks(k_cache, v_cache, ds.pairs, stream)
             pa_reshape_and_cache(k, v, k_cache, v_cache, ds.slots, stream)

@@ -139,3 +139,23 @@ def test_long_multiturn_bf16():
     del kc, vc
     torch.cuda.empty_cache()
     assert P.pa_device_errors() == 0
+
+
+@pytest.mark.parametrize("name", ["mha_fp16", "shared_prefix_fp16_p1032"])
+def test_fused_step_equals_separate_step(name):
+    """Replaying a workload's last step with the fused append (one launch) gives the
+    same caches and output, bit for bit, as append then decode."""
+    w = W.by_name(name, **({"prompts": 4} if name.startswith("shared") else {}))
+    kc, vc = _gpu_tensors(w)
+    alloc, ds = runner.execute(w, kc, vc, _step_kv(w), _query(w))
+    assert ds.fusable
+    k0, v0 = kc.clone(), vc.clone()
+    ds.run()
+    torch.cuda.synchronize()
+    out1, k1, v1 = ds.out.clone(), kc.clone(), vc.clone()
+    kc.copy_(k0)
+    vc.copy_(v0)
+    ds.run_fused()
+    torch.cuda.synchronize()
+    assert torch.equal(kc, k1) and torch.equal(vc, v1)
+    assert torch.equal(ds.out, out1)

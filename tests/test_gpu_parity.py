@@ -196,3 +196,51 @@ def test_copy_blocks_bit_exact(dtype):
 
 def test_no_device_errors_raised():
     assert P.pa_device_errors() == 0
+
+
+# ---------------------------------------------------------------------------
+# fused append + decode
+# ---------------------------------------------------------------------------
+FUSED = [
+    ("bf16", 128, 16, 8, 2, [1, 16, 17, 31, 32, 33, 500], 0),
+    ("f16", 128, 32, 40, 40, [7, 64, 65, 1000], 0),
+    ("f32", 64, 16, 4, 2, [1, 2, 40, 300], 0),
+    ("bf16", 64, 16, 40, 2, [18, 257, 1024], 128),
+    ("f16", 128, 16, 12, 3, [0, 5, 3000, 0], 0),
+]
+
+
+@pytest.mark.parametrize("dtype,D,B,Hq,Hkv,lens,part", FUSED, ids=lambda v: str(v).replace(" ", ""))
+def test_decode_append_equals_append_then_decode(dtype, D, B, Hq, Hkv, lens, part):
+    """pa_decode_append == pa_reshape_and_cache(newest tokens) + pa_decode, bit for bit
+    (caches and output), and both match the oracle."""
+    seed = sum(lens) % 1000 + D
+    q, kc, vc, bt, cl = small_case(seed, dtype, D, B, Hq, Hkv, lens, stale=0.0)
+    td = q.dtype
+    g = torch.Generator().manual_seed(seed)
+    k_new = torch.randn(len(lens), Hkv, D, generator=g).to(td)
+    v_new = torch.randn(len(lens), Hkv, D, generator=g).to(td)
+    slots = []
+    for s, T in enumerate(lens):
+        slots.append(int(bt[s, (T - 1) // B]) * B + (T - 1) % B if T > 0 else -1)
+    slots_t = torch.tensor(slots, dtype=torch.int64)
+    dev = {n: t.to(DEV) for n, t in dict(q=q, kc=kc, vc=vc, bt=bt, cl=cl, kn=k_new, vn=v_new, sl=slots_t).items()}
+    # two-launch path
+    k1, v1 = dev["kc"].clone(), dev["vc"].clone()
+    P.pa_reshape_and_cache(dev["kn"], dev["vn"], k1, v1, dev["sl"])
+    out1 = torch.empty_like(dev["q"])
+    P.pa_decode(out1, dev["q"], k1, v1, dev["bt"], dev["cl"], 0.11, Hq, Hkv, D, B, part)
+    # fused path
+    k2, v2 = dev["kc"].clone(), dev["vc"].clone()
+    out2 = torch.empty_like(dev["q"])
+    P.pa_decode_append(out2, dev["q"], k2, v2, dev["kn"], dev["vn"], dev["bt"], dev["cl"], 0.11, Hq, Hkv,
+                       D, B, part)
+    torch.cuda.synchronize()
+    assert torch.equal(k1, k2) and torch.equal(v1, v2)
+    assert torch.equal(out1, out2)
+    kh, vh = raw(kc).copy(), raw(vc).copy()
+    oracle.reshape_and_cache(raw(k_new), raw(v_new), kh, vh, np.array(slots), B)
+    assert np.array_equal(raw(k2), kh) and np.array_equal(raw(v2), vh)
+    want = oracle.decode(raw(q), kh, vh, bt.numpy(), cl.numpy(), 0.11, dtype, Hq, Hkv, D, B)
+    assert_close(out2, want, dtype)
+    assert P.pa_device_errors() == 0

@@ -264,11 +264,15 @@ def run_ours(args):
     # partitions: plus the merge kernel when a table spans several partitions
     merge = parts > 0 and -(-bt.shape[1] // (parts // w.block_size)) > 1
     fused = ds.fusable
-    launches_per_step = ((1 if n_pairs else 0) + (0 if fused or not n_tok else 1) + 1 +
-                         (1 if merge else 0))
+    shared = ds.share is not None and not args.no_share
+    if shared:
+        merge = False
+        parts = 0
+    launches_per_step = ((1 if n_pairs else 0) + (0 if fused or not n_tok else 1) +
+                         (2 if shared else 1) + (1 if merge else 0))
 
     with torch.cuda.stream(stream):
-        step = ds.run_fused if fused else ds.run
+        step = ds.run_shared if shared else (ds.run_fused if fused else ds.run)
         for _ in range(args.warmup):
             step(stream)
         torch.cuda.synchronize(device)
@@ -291,7 +295,9 @@ def run_ours(args):
             if not fused:
                 P.pa_reshape_and_cache(ds.step_k, ds.step_v, ds.k_cache, ds.v_cache, ds.slots, stream)
             e1.record(stream)
-            if fused:
+            if shared:
+                ds.decode_shared(stream, append=fused)
+            elif fused:
                 P.pa_decode_append(ds.out, ds.q, ds.k_cache, ds.v_cache, ds.step_k, ds.step_v,
                                    ds.block_tables, ds.context_lens, ds.scale, ds.num_q_heads,
                                    ds.num_kv_heads, ds.head_dim, ds.block_size, ds.partition_size,
@@ -315,7 +321,7 @@ def run_ours(args):
         t_step, t_dec = t.tolist()
 
     # end to end through the public API with host buffers
-    e2e = run_e2e(ds, stream, device, args, by)
+    e2e = run_e2e(ds, stream, device, args, by, shared)
 
     if rank != 0:
         return None
@@ -342,6 +348,9 @@ def run_ours(args):
                    "max_context": int(np.max(cl)),
                    "split": "balanced" if parts == 0 else f"fixed partitions of {parts} tokens",
                    "append": "fused into the decode launch" if fused else "separate launch",
+                   "prefix_sharing": (f"{int((ds.share[:, 0] >= 0).sum())} sequences in groups that "
+                                      "read their shared leading blocks once (two-pass decode)"
+                                      if shared else "none"),
                    "appended_tokens": n_tok,
                    "cow_pairs": n_pairs,
                    "l2": "flushed before every timed step (512 MB write, then 1 GB read)",
@@ -353,8 +362,11 @@ def run_ours(args):
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_kind": f"{peak_kind} copy bandwidth",
                      "traffic": profiled_traffic(w.name),
-                     "kernel": ("pa_decode_append (append + decode partition kernel, merge inside)" if fused
-                                else "pa_decode (partition kernel; split-KV merge fused or second kernel)")},
+                     "kernel": ("pa_decode_shared (partition kernel twice: shared prefixes, then own "
+                                "blocks" + (" + append" if fused else "") + ", merges inside)" if shared
+                                else "pa_decode_append (append + decode partition kernel, merge inside)"
+                                if fused else
+                                "pa_decode (partition kernel; split-KV merge fused or second kernel)")},
         "e2e": e2e,
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk,
@@ -369,12 +381,15 @@ def run_ours(args):
     return line
 
 
-def run_e2e(ds, stream, device, args, by):
+def run_e2e(ds, stream, device, args, by, shared=False):
     """Same step through the public API with inputs in pinned host memory: H2D of
     the step's inputs, the step, D2H of the output -- all inside the timed region."""
     import torch
     host = {}
-    for name in ("q", "step_k", "step_v", "slots", "pairs", "block_tables", "context_lens"):
+    names = ["q", "step_k", "step_v", "slots", "pairs", "block_tables", "context_lens"]
+    if shared:
+        names.append("share")
+    for name in names:
         t = getattr(ds, name)
         host[name] = t.cpu().pin_memory()
     out_h = torch.empty(ds.out.shape, dtype=ds.out.dtype).pin_memory()
@@ -391,7 +406,10 @@ def run_e2e(ds, stream, device, args, by):
             a.record(stream)
             for name, t in host.items():
                 getattr(ds, name).copy_(t, non_blocking=True)
-            ds.run_fused(stream) if ds.fusable else ds.run(stream)
+            if shared:
+                ds.run_shared(stream)
+            else:
+                ds.run_fused(stream) if ds.fusable else ds.run(stream)
             out_h.copy_(ds.out, non_blocking=True)
             b.record(stream)
             b.synchronize()
@@ -461,6 +479,8 @@ def main():
     ap.add_argument("--partition-size", type=int, default=0,
                     help="0: balanced split (default); >0: fixed partitions of that many tokens")
     ap.add_argument("--cpu-budget", type=float, default=10.0)
+    ap.add_argument("--no-share", action="store_true",
+                    help="decode every sequence's blocks separately even where groups share a prefix")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

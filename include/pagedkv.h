@@ -142,6 +142,42 @@ pa_status pa_decode_append(void *out, const void *q, void *k_cache, void *v_cach
                            void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * pa_decode_shared -- decode a batch whose sequences share prefix blocks.
+ *
+ * Same result as pa_decode (or, with k_new/v_new, pa_decode_append), but each
+ * block shared by a group of sequences is read once for the whole group ([S]
+ * "Memory sharing": parallel samples point at the same physical prompt blocks).
+ * The decode runs in two launches: the shared blocks of every group, with the
+ * query rows of all its members against each kv head, then every sequence's own
+ * blocks; the two partial results are merged by the log-sum-exp rule of [S]'s
+ * block-wise attention equation.
+ *
+ *   share   device int32 [S][2]: share[s][0] = batch index of the first member of
+ *           s's group, or -1 when s shares nothing; share[s][1] = number of leading
+ *           blocks the group shares.  Preconditions (not checked on the device):
+ *           members are consecutive in the batch; all have the same share[s][1] =
+ *           P; their block-table rows agree on entries 0 .. P-1; and every member's
+ *           context is longer than P * block_size (the newest token is never in a
+ *           shared block: the allocator copies such a block on write).
+ *   k_new, v_new   both null (plain decode) or as in pa_decode_append.
+ * Requires num_q_heads / num_kv_heads <= 16 (PA_ERR_UNSUPPORTED otherwise).  Always
+ * uses the balanced split.  Workspace: pa_decode_shared_workspace_size bytes.
+ * Errors as pa_decode; PA_ERR_INVALID also for a null or misaligned share.
+ */
+pa_status pa_decode_shared(void *out, const void *q, void *k_cache, void *v_cache,
+                           const void *k_new, const void *v_new, const int32_t *block_tables,
+                           int max_blocks_per_seq, const int32_t *context_lens,
+                           const int32_t *share, int num_seqs, int num_blocks, float scale,
+                           int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                           pa_dtype dtype, void *workspace, size_t workspace_bytes, void *stream);
+
+/* Workspace bytes of pa_decode_shared: pa_decode_workspace_size(..., 0) plus fp32
+ * shared-prefix rows [S][Hq][d] and their log2-sum-exp [S][Hq] (each 256-byte
+ * aligned).  (size_t)-1 for invalid arguments. */
+size_t pa_decode_shared_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads,
+                                       int head_dim, int block_size, int max_blocks_per_seq);
+
+/*
  * Partition size pa_decode uses for these arguments: 0 for the balanced split,
  * else the fixed partition size (capped at the table capacity).  Returns -1 for
  * invalid arguments.
@@ -297,6 +333,19 @@ int pa_alloc_refcount(const pa_alloc *a, int block);     /* -1 if out of range *
 int pa_alloc_num_free(const pa_alloc *a);
 /* Copy up to `cap` free-list entries (bottom to top: the next pop is the last). */
 pa_status pa_alloc_free_list(const pa_alloc *a, int32_t *out, int cap, int *n);
+
+/*
+ * Host helper: the share argument of pa_decode_shared, derived from the block
+ * tables (host int32 [S][W], -1 padded) and context lengths (host int32 [S]).
+ * A group is a maximal run of consecutive rows whose entry 0 is the same physical
+ * block (>= 0); its P is the number of leading entries equal in all its rows,
+ * capped at floor((T - 1) / block_size) for every member T.  Groups with fewer
+ * than two rows or P < min_shared_blocks get {-1, 0}.  share: host int32 [S][2],
+ * written for every row.  PA_ERR_INVALID for bad sizes or null pointers.
+ */
+pa_status pa_share_groups(const int32_t *block_tables, int num_seqs, int max_blocks_per_seq,
+                          const int32_t *context_lens, int block_size, int min_shared_blocks,
+                          int32_t *share);
 
 #ifdef __cplusplus
 }

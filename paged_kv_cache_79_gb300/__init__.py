@@ -7,6 +7,7 @@ calls on tensors that are not CUDA tensors raise.
 
     pa_decode               paged single-query attention (partition + merge kernels)
     pa_decode_append        the newest tokens' append fused with the decode
+    pa_decode_shared        decode reading each shared prefix block once per group
     pa_reshape_and_cache    write new tokens' K/V rows through a slot mapping
     pa_copy_blocks          copy-on-write block copies
     BlockAllocator          host ref-counted block allocator (pa_alloc_*)
@@ -142,6 +143,57 @@ def pa_decode_append(out, q, k_cache, v_cache, k_new, v_new, block_tables, conte
                                   _dtype_code(q), partition_size, ws_ptr, ws_bytes, _stream(stream))
     _check(st, "pa_decode_append")
     return out
+
+
+def pa_decode_shared_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+                                    max_blocks_per_seq) -> int:
+    n = _load().pa_decode_shared_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim,
+                                                block_size, max_blocks_per_seq)
+    if n == ctypes.c_size_t(-1).value:
+        raise PagedKVError(PA_ERR_INVALID, "pa_decode_shared_workspace_size")
+    return n
+
+
+def pa_decode_shared(out, q, k_cache, v_cache, block_tables, context_lens, share, scale: float,
+                     num_q_heads: int, num_kv_heads: int, head_dim: int, block_size: int,
+                     k_new=None, v_new=None, workspace=None, stream=None):
+    """Decode a batch whose sequence groups share leading blocks, reading each shared
+    block once per group; share: int32 [S, 2] = (first member of the group or -1,
+    shared leading blocks).  With k_new/v_new, also appends the newest tokens."""
+    import torch
+    S = q.shape[0]
+    W = block_tables.shape[1]
+    if workspace is None:
+        n = pa_decode_shared_workspace_size(S, num_q_heads, num_kv_heads, head_dim, block_size, W)
+        workspace = torch.empty(n, dtype=torch.uint8, device=q.device)
+    if share.dtype != torch.int32 or block_tables.dtype != torch.int32 or context_lens.dtype != torch.int32:
+        raise TypeError("share, block_tables and context_lens must be int32")
+    st = _load().pa_decode_shared(_cuda(out, "out"), _cuda(q, "q"), _cuda(k_cache, "k_cache"),
+                                  _cuda(v_cache, "v_cache"),
+                                  _cuda(k_new, "k_new") if k_new is not None else None,
+                                  _cuda(v_new, "v_new") if v_new is not None else None,
+                                  _cuda(block_tables, "block_tables"), W,
+                                  _cuda(context_lens, "context_lens"), _cuda(share, "share"), S,
+                                  k_cache.shape[0], float(scale), num_q_heads, num_kv_heads, head_dim,
+                                  block_size, _dtype_code(q), _cuda(workspace, "workspace"),
+                                  workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(st, "pa_decode_shared")
+    return out
+
+
+def share_groups(block_tables, context_lens, block_size: int, min_shared_blocks: int = 1):
+    """share int32 [S, 2] for pa_decode_shared, from host block tables [S, W] and
+    context lengths [S] (numpy or CPU tensors); see pa_share_groups."""
+    import numpy as np
+    bt = np.ascontiguousarray(np.asarray(block_tables, dtype=np.int32))
+    cl = np.ascontiguousarray(np.asarray(context_lens, dtype=np.int32))
+    S = cl.shape[0]
+    share = np.empty((S, 2), dtype=np.int32)
+    W = bt.shape[1] if bt.ndim == 2 else 0
+    st = _load().pa_share_groups(bt.ctypes.data if S else None, S, W, cl.ctypes.data if S else None,
+                                 block_size, min_shared_blocks, share.ctypes.data if S else None)
+    _check(st, "pa_share_groups")
+    return share
 
 
 def pa_decode_noalloc(out, q, k_cache, v_cache, block_tables, context_lens, scale: float,
@@ -295,6 +347,7 @@ class BlockAllocator:
         return out[:n.value].tolist()
 
 
-__all__ = ["pa_decode", "pa_decode_append", "pa_decode_noalloc", "pa_decode_workspace_size", "pa_decode_partition_size", "alloc_workspace",
+__all__ = ["pa_decode", "pa_decode_append", "pa_decode_shared", "pa_decode_shared_workspace_size",
+           "share_groups", "pa_decode_noalloc", "pa_decode_workspace_size", "pa_decode_partition_size", "alloc_workspace",
            "pa_reshape_and_cache", "pa_copy_blocks", "pa_device_errors", "pa_status_string",
            "BlockAllocator", "PagedKVError", "OutOfBlocks", "library_path"]

@@ -255,3 +255,45 @@ pa_status pa_alloc_free_list(const pa_alloc *a, int32_t *out, int cap, int *n)
 }
 
 }  // extern "C"
+
+// Shared-prefix groups for pa_decode_shared, from the block tables alone: a group
+// is a maximal run of consecutive batch rows whose first entries name the same
+// physical block; it shares the leading entries common to all its rows, capped so
+// that every member's newest token stays outside the shared part.
+pa_status pa_share_groups(const int32_t *block_tables, int num_seqs, int max_blocks_per_seq,
+                          const int32_t *context_lens, int block_size, int min_shared_blocks,
+                          int32_t *share)
+{
+    if (num_seqs < 0 || max_blocks_per_seq < 0 || block_size <= 0 || min_shared_blocks < 1)
+        return PA_ERR_INVALID;
+    if (num_seqs > 0 && (!block_tables || !context_lens || !share || max_blocks_per_seq == 0))
+        return PA_ERR_INVALID;
+    const size_t W = (size_t)max_blocks_per_seq;
+    auto cap = [&](int s) {     // blocks of s that hold no newest token: floor((T-1)/B)
+        const int T = context_lens[s];
+        return T <= 0 ? 0 : std::min((T - 1) / block_size, max_blocks_per_seq);
+    };
+    int g = 0;
+    while (g < num_seqs) {
+        const int32_t *row0 = block_tables + (size_t)g * W;
+        int e = g + 1;
+        while (e < num_seqs && row0[0] >= 0 && block_tables[(size_t)e * W] == row0[0])
+            ++e;
+        int P = cap(g);
+        for (int m = g + 1; m < e; ++m) {
+            const int32_t *row = block_tables + (size_t)m * W;
+            int j = 0;
+            const int lim = std::min(P, cap(m));
+            while (j < lim && row[j] == row0[j] && row[j] >= 0)
+                ++j;
+            P = j;
+        }
+        const bool ok = e - g >= 2 && P >= min_shared_blocks;
+        for (int m = g; m < e; ++m) {
+            share[2 * m] = ok ? g : -1;
+            share[2 * m + 1] = ok ? P : 0;
+        }
+        g = e;
+    }
+    return PA_OK;
+}

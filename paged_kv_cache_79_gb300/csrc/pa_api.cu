@@ -254,13 +254,21 @@ size_t pa_decode_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads,
 
 namespace {
 
-// pa_decode and pa_decode_append: k_new/v_new null for a plain decode.
+size_t prefix_buffer_bytes(int num_seqs, int num_q_heads, int head_dim)
+{
+    const size_t rows = (size_t)num_seqs * num_q_heads;
+    return ((rows * head_dim * 4 + 255) & ~size_t(255)) + ((rows * 4 + 255) & ~size_t(255));
+}
+
+// pa_decode, pa_decode_append and pa_decode_shared: k_new/v_new null for a plain
+// decode; share null unless the batch declares shared-prefix groups.
 pa_status decode_impl(void *out, const void *q, const void *k_cache, const void *v_cache,
                       const int32_t *block_tables, int max_blocks_per_seq,
                       const int32_t *context_lens, int num_seqs, int num_blocks, float scale,
                       int num_q_heads, int num_kv_heads, int head_dim, int block_size,
                       pa_dtype dtype, int partition_size, void *workspace, size_t workspace_bytes,
-                      const void *k_new, const void *v_new, void *stream)
+                      const void *k_new, const void *v_new, void *stream,
+                      const int32_t *share = nullptr)
 {
     if (num_seqs == 0)
         return PA_OK;
@@ -294,12 +302,23 @@ pa_status decode_impl(void *out, const void *q, const void *k_cache, const void 
     const int part = balanced ? 0 : resolve_partition(block_size, max_blocks_per_seq, partition_size);
     const int pb = balanced ? max_blocks_per_seq : part / block_size;
     const int parts = balanced ? 1 : (max_blocks_per_seq + pb - 1) / pb;
-    const size_t need = pa_decode_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim,
-                                                 block_size, max_blocks_per_seq, partition_size);
+    size_t need = pa_decode_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+                                           max_blocks_per_seq, partition_size);
     if (need == (size_t)-1)
         return PA_ERR_INVALID;
+    const bool shared = share != nullptr && balanced && num_q_heads / num_kv_heads <= kHeadsPerItem;
+    const size_t pfx_at = need;
+    if (shared)
+        need += prefix_buffer_bytes(num_seqs, num_q_heads, head_dim);
     if (need > 0 && (!workspace || workspace_bytes < need || !aligned(workspace, 16)))
         return PA_ERR_INVALID;
+    float *pfx_o = nullptr, *pfx_lse = nullptr;
+    if (shared) {
+        const size_t rows = (size_t)num_seqs * num_q_heads;
+        pfx_o = reinterpret_cast<float *>(static_cast<char *>(workspace) + pfx_at);
+        pfx_lse = reinterpret_cast<float *>(static_cast<char *>(workspace) + pfx_at +
+                                            ((rows * head_dim * 4 + 255) & ~size_t(255)));
+    }
 
     DecodeLaunch L;
     std::memset(&L, 0, sizeof L);
@@ -351,9 +370,31 @@ pa_status decode_impl(void *out, const void *q, const void *k_cache, const void 
         return cuda_fail(cudaErrorInvalidValue);
 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    cudaError_t e = dtype == PA_F32   ? launch_decode_f32(L, st)
-                    : dtype == PA_F16 ? launch_decode_f16(L, st)
-                                      : launch_decode_bf16(L, st);
+    auto launch = [&](const DecodeLaunch &l) {
+        return dtype == PA_F32   ? launch_decode_f32(l, st)
+               : dtype == PA_F16 ? launch_decode_f16(l, st)
+                                 : launch_decode_bf16(l, st);
+    };
+    if (shared) {
+        // pass 1: every group's shared blocks once, all members' rows at a time
+        DecodeLaunch L1 = L;
+        L1.p.pass = 1;
+        L1.p.share = share;
+        L1.p.pfx_o = pfx_o;
+        L1.p.pfx_lse = pfx_lse;
+        L1.p.k_new = nullptr;
+        L1.p.v_new = nullptr;
+        cudaError_t e = launch(L1);
+        if (e != cudaSuccess)
+            return cuda_fail(e);
+        // pass 0: each sequence's own blocks (and newest token), merged with pass 1
+        L.p.pass = 0;
+        L.p.share = share;
+        L.p.pfx_o = pfx_o;
+        L.p.pfx_lse = pfx_lse;
+        L.p.epoch = next_epoch();
+    }
+    cudaError_t e = launch(L);
     if (e != cudaSuccess)
         return cuda_fail(e);
     return PA_OK;
@@ -387,6 +428,35 @@ pa_status pa_decode_append(void *out, const void *q, void *k_cache, void *v_cach
     return decode_impl(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
                        num_seqs, num_blocks, scale, num_q_heads, num_kv_heads, head_dim, block_size,
                        dtype, partition_size, workspace, workspace_bytes, k_new, v_new, stream);
+}
+
+size_t pa_decode_shared_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads,
+                                       int head_dim, int block_size, int max_blocks_per_seq)
+{
+    const size_t base = pa_decode_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim,
+                                                 block_size, max_blocks_per_seq, 0);
+    if (base == (size_t)-1)
+        return base;
+    return base + prefix_buffer_bytes(num_seqs, num_q_heads, head_dim);
+}
+
+pa_status pa_decode_shared(void *out, const void *q, void *k_cache, void *v_cache,
+                           const void *k_new, const void *v_new, const int32_t *block_tables,
+                           int max_blocks_per_seq, const int32_t *context_lens,
+                           const int32_t *share, int num_seqs, int num_blocks, float scale,
+                           int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                           pa_dtype dtype, void *workspace, size_t workspace_bytes, void *stream)
+{
+    if (num_seqs != 0 && (!share || !aligned(share, 8)))
+        return PA_ERR_INVALID;
+    if (num_seqs != 0 && ((k_new == nullptr) != (v_new == nullptr) ||
+                          (k_new && (!aligned(k_new, 16) || !aligned(v_new, 16)))))
+        return PA_ERR_INVALID;
+    if (num_kv_heads > 0 && num_q_heads / num_kv_heads > kHeadsPerItem)
+        return PA_ERR_UNSUPPORTED;
+    return decode_impl(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
+                       num_seqs, num_blocks, scale, num_q_heads, num_kv_heads, head_dim, block_size,
+                       dtype, 0, workspace, workspace_bytes, k_new, v_new, stream, share);
 }
 
 pa_status pa_reshape_and_cache(const void *k, const void *v, void *k_cache, void *v_cache,

@@ -113,6 +113,14 @@ struct SmemLayout {
 
 constexpr int kItemSlots = 2;  // work-item descriptors (and their query rows) in flight
 
+// Most query rows one item of this launch carries: the heads of one head group,
+// or, in the shared-prefix pass, the rows of up to kHeadsPerItem / group member
+// sequences.  Sizes the merge accumulators in shared memory.
+__host__ __device__ inline int item_rows_cap(const DecodeParams &p)
+{
+    return p.pass == 1 ? kHeadsPerItem : (p.group < kHeadsPerItem ? p.group : kHeadsPerItem);
+}
+
 // Shared memory: stage ring | merge accumulators | merge (max, sum) | item
 // descriptors | query rows per item slot | mbarriers | abort flag.
 __host__ __device__ inline SmemLayout make_layout(int stages, int stage_bytes, int rows, int D,
@@ -186,18 +194,34 @@ __device__ __forceinline__ bool find_item(const DecodeParams &p, int bs, long lo
     return false;
 }
 
+constexpr int kToPrefix = 1;     // result rows go to the shared-prefix buffer
+constexpr int kMergePrefix = 2;  // result rows are merged with the shared-prefix buffer
+
+// A work item: blocks [j0, j1) of one unit.  Row r of the item is query head
+// qrow0 + r % rpm of sequence seq + r / rpm (several sequences only in the
+// shared-prefix pass, where the rows of `members` sequences share one kv head).
 struct Item {
-    int seq, kvh, hg, len;  // unit and its context length
-    int j0, j1;             // blocks [j0, j1) of the unit
-    int qrow0, rows;        // query heads qrow0 .. qrow0 + rows - 1
-    int partial;            // 0: write the output; 1: write partial row prow0 + r
+    int seq, kvh, hg, len;  // first sequence, kv head, head group, context length
+    int j0, j1;             // blocks [j0, j1) of the unit (absolute block indices)
+    int qrow0, rows;        // query heads qrow0 .. of each sequence; rows in all
+    int partial;            // 0: write the result; 1: write partial row prow0 + r
     int prow0;
     // balanced split, partial items: the unit's partials come from the non-empty
     // CTAs c_first ... (nparts of them); the CTA that writes the last one merges
     int c_first, nparts;
     unsigned int total_lo, total_hi;  // stream length (to tell empty CTA ranges)
-    int pad[2];             // 64 bytes: one shared-memory descriptor slot
+    int tseq;               // sequence whose block-table row gives the blocks
+    int packed;             // members << 16 | rows per member << 8 | kToPrefix/kMergePrefix
+    __device__ int members() const { return packed >> 16; }
+    __device__ int rpm() const { return (packed >> 8) & 0xff; }
+    __device__ int flags() const { return packed & 0xff; }
 };
+static_assert(sizeof(Item) == 64, "one 64-byte descriptor slot");
+
+__device__ __forceinline__ int pack_rows(int members, int rpm, int flags)
+{
+    return (members << 16) | (rpm << 8) | flags;
+}
 
 __device__ __forceinline__ Item decode_item(const DecodeParams &p, int bs, long long w, int seq,
                                             long long base)
@@ -229,6 +253,8 @@ __device__ __forceinline__ Item decode_item(const DecodeParams &p, int bs, long 
     it.c_first = -1;  // merged by pa_merge_kernel
     it.nparts = 0;
     it.total_lo = it.total_hi = 0;
+    it.tseq = seq;
+    it.packed = pack_rows(1, it.rows, 0);
     return it;
 }
 
@@ -314,6 +340,8 @@ __device__ __forceinline__ Item load_item(const Item *slot)
     it.nparts = v[11];
     it.total_lo = (unsigned int)v[12];
     it.total_hi = (unsigned int)v[13];
+    it.tseq = v[14];
+    it.packed = v[15];
     return it;
 }
 
@@ -384,13 +412,15 @@ struct Producer {
                                     ((n / kItemSlots) & 1u) ^ 1u, kWaitTimeoutNs);
                 if (ok) {
                     c.items[slot] = it;
-                    const uint32_t qbytes = (uint32_t)it.rows * D * sizeof(T);
+                    // query rows: rpm contiguous heads of each member sequence
+                    const uint32_t mbytes = (uint32_t)it.rpm() * D * sizeof(T);
                     const uint32_t fb = dev::smem_addr(&c.item_full[slot]);
-                    dev::mbar_arrive_expect_tx(fb, qbytes);
-                    dev::bulk_load(dev::smem_addr(c.qslots + slot * kQSlotBytes),
-                                   reinterpret_cast<const T *>(p.q) +
-                                       ((size_t)it.seq * p.num_q_heads + it.qrow0) * D,
-                                   qbytes, fb);
+                    dev::mbar_arrive_expect_tx(fb, mbytes * (uint32_t)it.members());
+                    for (int m = 0; m < it.members(); ++m)
+                        dev::bulk_load(dev::smem_addr(c.qslots + slot * kQSlotBytes) + m * mbytes,
+                                       reinterpret_cast<const T *>(p.q) +
+                                           ((size_t)(it.seq + m) * p.num_q_heads + it.qrow0) * D,
+                                       mbytes, fb);
                 }
             }
             if (!__shfl_sync(0xffffffffu, ok, 0)) {
@@ -401,7 +431,7 @@ struct Producer {
             }
             ++n;
         }
-        const int32_t *row = p.block_tables + (size_t)it.seq * p.max_blocks;
+        const int32_t *row = p.block_tables + (size_t)it.tseq * p.max_blocks;
         for (int jb = it.j0; jb < it.j1; jb += 32) {
             const int j = jb + lane;
             const int phys = (j < it.j1) ? row[j] : 0;  // one coalesced read per 32 blocks
@@ -526,10 +556,68 @@ struct Producer {
 #endif
 constexpr int kUnitCost = PA_UNIT_COST;
 static_assert(kUnitCost >= 1, "every unit needs a start position");
-__device__ __forceinline__ int seq_stages(const DecodeParams &p, int s, int bs, int bps)
+// The units a sequence contributes to the stream of the current pass.
+//   pass 0: (kv head, head group) units over blocks [start, nb) -- start is the
+//           shared prefix length of a grouped sequence (its rows then merge with the
+//           prefix pass's), else 0;
+//   pass 1: only the first member of a group has units: (kv head, member group)
+//           over the group's shared blocks [0, nb = prefix), each unit holding the
+//           query rows of up to 16 / G member sequences.
+struct SeqUnits {
+    int nunits;   // units of this sequence in the stream
+    int ns;       // ring stages per unit
+    int start;    // first block
+    int nb;       // end block
+    int len;      // context length the unit's blocks belong to
+    int members;  // pass 1: group size
+    int mgroups;  // pass 1: member groups per kv head
+};
+
+__device__ __forceinline__ int shared_blocks(const DecodeParams &p, int s)
 {
-    const int nb = (clamp_len(p, s, bs) + bs - 1) / bs;
-    return (nb + bps - 1) / bps;
+    if (!p.share || p.group > kHeadsPerItem || p.share[2 * s] < 0)
+        return 0;
+    const int v = p.share[2 * s + 1];
+    return v > 0 ? min(v, p.max_blocks) : 0;
+}
+
+__device__ __forceinline__ SeqUnits seq_units(const DecodeParams &p, int s, int bs, int bps)
+{
+    SeqUnits u;
+    const int len = clamp_len(p, s, bs);
+    const int nb = (len + bs - 1) / bs;
+    u.members = 1;
+    u.mgroups = 1;
+    if (p.pass == 1) {
+        u.nunits = 0;
+        u.ns = 0;
+        u.start = 0;
+        u.nb = 0;
+        u.len = 0;
+        if (p.share && p.share[2 * s] == s) {
+            const int P = shared_blocks(p, s);
+            if (P > 0) {
+                int m = 1;
+                while (s + m < p.num_seqs && p.share[2 * (s + m)] == s)
+                    ++m;
+                const int mpi = kHeadsPerItem / p.group;
+                u.members = m;
+                u.mgroups = (m + mpi - 1) / mpi;
+                u.nunits = p.num_kv_heads * u.mgroups;
+                u.ns = (P + bps - 1) / bps;
+                u.nb = P;
+                u.len = P * bs;
+            }
+        }
+        return u;
+    }
+    const int P = min(shared_blocks(p, s), nb);
+    u.nunits = p.num_kv_heads * p.head_groups;
+    u.ns = (nb - P + bps - 1) / bps;
+    u.start = P;
+    u.nb = nb;
+    u.len = len;
+    return u;
 }
 
 __device__ __forceinline__ long long warp_sum_ll(long long v)
@@ -540,6 +628,12 @@ __device__ __forceinline__ long long warp_sum_ll(long long v)
     return v;
 }
 
+__device__ __forceinline__ long long seq_weight(const DecodeParams &p, int s, int bs, int bps)
+{
+    const SeqUnits u = seq_units(p, s, bs, bps);
+    return (long long)u.nunits * (kUnitCost + u.ns);
+}
+
 // Positions of the whole stream (every lane gets the value).
 __device__ __forceinline__ long long stream_total(const DecodeParams &p, int bs, int bps, int lane)
 {
@@ -547,22 +641,21 @@ __device__ __forceinline__ long long stream_total(const DecodeParams &p, int bs,
     for (int s0 = 0; s0 < p.num_seqs; s0 += 32) {
         const int s = s0 + lane;
         if (s < p.num_seqs)
-            t += kUnitCost + seq_stages(p, s, bs, bps);
+            t += seq_weight(p, s, bs, bps);
     }
-    return warp_sum_ll(t) * ((long long)p.num_kv_heads * p.head_groups);
+    return warp_sum_ll(t);
 }
 
-// The sequence whose positions contain x (every unit has at least one position);
+// The sequence whose positions contain x (sequences without units have none);
 // num_seqs if x >= total.  *base_out gets the sequence's first position.
 // Warp-cooperative.
 __device__ __forceinline__ int find_seq_at(const DecodeParams &p, int bs, int bps, long long x,
                                            long long *base_out, int lane)
 {
-    const long long units = (long long)p.num_kv_heads * p.head_groups;
     long long base = 0;
     for (int s0 = 0; s0 < p.num_seqs; s0 += 32) {
         const int s = s0 + lane;
-        const long long w = (s < p.num_seqs) ? units * (kUnitCost + seq_stages(p, s, bs, bps)) : 0;
+        const long long w = (s < p.num_seqs) ? seq_weight(p, s, bs, bps) : 0;
         long long incl = w;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -595,7 +688,6 @@ __device__ __forceinline__ void walk_balanced(const DecodeParams &p, int bs, int
 {
     const long long G = gridDim.x;
     const long long cta = blockIdx.x;
-    const long long units = (long long)p.num_kv_heads * p.head_groups;
     const long long total = stream_total(p, bs, bps, lane);
     const long long s_c = cta * total / G;
     const long long e_c = (cta + 1) * total / G;
@@ -604,40 +696,56 @@ __device__ __forceinline__ void walk_balanced(const DecodeParams &p, int bs, int
     long long base = 0;
     int s = find_seq_at(p, bs, bps, s_c, &base, lane);
     for (; s < p.num_seqs && base < e_c && !*pr.c.abort; ++s) {
-        const int len = clamp_len(p, s, bs);
-        const int nb = (len + bs - 1) / bs;
-        const long long ns = (nb + bps - 1) / bps;
+        const SeqUnits su = seq_units(p, s, bs, bps);
+        if (su.nunits == 0)
+            continue;
+        const long long ns = su.ns;
         const long long span = kUnitCost + ns;
         Item it;
-        it.seq = s;
-        it.len = len;
+        it.len = su.len;
         it.total_lo = (unsigned int)(total & 0xffffffffll);
         it.total_hi = (unsigned int)(total >> 32);
+        it.tseq = s;
         const long long u_lo = s_c > base ? (s_c - base) / span : 0;
-        const long long u_hi = min(units - 1, (e_c - 1 - base) / span);
+        const long long u_hi = min((long long)su.nunits - 1, (e_c - 1 - base) / span);
         for (long long u = u_lo; u <= u_hi; ++u) {
             const long long a = base + u * span;  // unit start (its cost positions)
             const long long ra = a + kUnitCost;   // first real stage
             const long long rb = ra + ns;
-            it.kvh = (int)(u / p.head_groups);
-            it.hg = (int)(u % p.head_groups);
-            it.qrow0 = it.kvh * p.group + it.hg * kHeadsPerItem;
-            it.rows = min(kHeadsPerItem, p.group - it.hg * kHeadsPerItem);
+            if (p.pass == 1) {
+                const int mpi = kHeadsPerItem / p.group;
+                const int mg = (int)(u % su.mgroups);
+                const int members = min(mpi, su.members - mg * mpi);
+                it.seq = s + mg * mpi;
+                it.kvh = (int)(u / su.mgroups);
+                it.hg = 0;
+                it.qrow0 = it.kvh * p.group;
+                it.rows = members * p.group;
+                it.packed = pack_rows(members, p.group, kToPrefix);
+            } else {
+                it.seq = s;
+                it.kvh = (int)(u / p.head_groups);
+                it.hg = (int)(u % p.head_groups);
+                it.qrow0 = it.kvh * p.group + it.hg * kHeadsPerItem;
+                it.rows = min(kHeadsPerItem, p.group - it.hg * kHeadsPerItem);
+                it.packed = pack_rows(1, it.rows, su.start > 0 ? kMergePrefix : 0);
+            }
             it.c_first = -1;
             it.nparts = 0;
             if (ns == 0) {
-                // an empty unit belongs to the CTA holding its start: zero output
+                // an empty unit belongs to the CTA holding its start: zero rows (or the
+                // shared-prefix rows alone)
                 if (a < s_c)
                     continue;
-                it.j0 = it.j1 = 0;
+                it.j0 = it.j1 = su.start;
                 it.partial = 0;
                 it.prow0 = 0;
             } else {
                 const long long lo = max(ra, s_c), hi = min(rb, e_c);
                 if (lo >= hi)
                     continue;
-                it.j0 = (int)((lo - ra) * bps);
-                it.j1 = (int)min((hi - ra) * bps, (long long)nb);
+                it.j0 = su.start + (int)((lo - ra) * bps);
+                it.j1 = (int)min(su.start + (hi - ra) * bps, (long long)su.nb);
                 it.partial = (lo == ra && hi == rb) ? 0 : 1;
                 // slot 2c: the unit's stages began in an earlier CTA; 2c + 1: they go on
                 it.prow0 = (int)((2 * cta + (ra < s_c ? 0 : 1)) * kHeadsPerItem);
@@ -654,7 +762,7 @@ __device__ __forceinline__ void walk_balanced(const DecodeParams &p, int bs, int
             if (!pr.emit(it))
                 return;
         }
-        base += units * span;
+        base += (long long)su.nunits * span;
     }
 }
 
@@ -681,6 +789,36 @@ __device__ __forceinline__ void producer_loop(const DecodeParams &p, const CUten
     else
         walk_fixed(p, BS, pr, lane);
     pr.finish();
+}
+
+// ---------------------------------------------------------------------------
+// Final value of element `col` of item row r: normalised output o and the row's
+// log2-sum-exp.  Goes to the output (cast to T), to the shared-prefix buffer
+// (prefix pass), or is first merged with the shared-prefix row by the
+// log-sum-exp rule (own blocks of a grouped sequence).
+// ---------------------------------------------------------------------------
+template <typename T, int D>
+__device__ __forceinline__ void store_result(const DecodeParams &p, const Item &it, int r, int col,
+                                             float o, float lse)
+{
+    const int rpm = it.rpm();
+    const size_t row = (size_t)(it.seq + r / rpm) * p.num_q_heads + it.qrow0 + r % rpm;
+    const int f = it.flags();
+    if (f & kToPrefix) {
+        p.pfx_o[row * D + col] = o;
+        if (col == 0)
+            p.pfx_lse[row] = lse;
+        return;
+    }
+    if (f & kMergePrefix) {
+        const float lp = __ldcg(p.pfx_lse + row);
+        const float m2 = fmaxf(lse, lp);
+        if (m2 != -INFINITY) {
+            const float wa = exp2f(lse - m2), wb = exp2f(lp - m2);
+            o = (wa * o + wb * __ldcg(p.pfx_o + row * D + col)) / (wa + wb);
+        }
+    }
+    reinterpret_cast<T *>(p.out)[row * D + col] = dev::from_float<T>(o);
 }
 
 // ---------------------------------------------------------------------------
@@ -719,9 +857,7 @@ __device__ __forceinline__ void finalize_item(const DecodeParams &p, const Item 
         }
         const float o = (L > 0.f) ? O / L : 0.f;
         if (!it.partial) {
-            const size_t h = (size_t)it.qrow0 + r;
-            reinterpret_cast<T *>(p.out)[((size_t)it.seq * p.num_q_heads + h) * D + col] =
-                dev::from_float<T>(o);
+            store_result<T, D>(p, it, r, col, o, (L > 0.f) ? M + log2f(L) : -INFINITY);
         } else {
             const size_t pr = (size_t)it.prow0 + r;
             p.part_o[pr * D + col] = o;
@@ -824,11 +960,10 @@ __device__ __forceinline__ void merge_split_unit(const DecodeParams &p, const It
             }
         }
         W = dev::warp_sum(W);
-        T *o = reinterpret_cast<T *>(p.out) + ((size_t)it.seq * p.num_q_heads + it.qrow0 + r) * D +
-               lane * VEC;
+        const float lse = M + log2f(W);
 #pragma unroll
         for (int e = 0; e < VEC; ++e)
-            o[e] = dev::from_float<T>(acc[e] / W);
+            store_result<T, D>(p, it, r, lane * VEC + e, acc[e] / W, lse);
     }
 }
 
@@ -916,7 +1051,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    const int rows_cap = min(kHeadsPerItem, p.group);
+    const int rows_cap = item_rows_cap(p);
     const SmemLayout lay = make_layout(C::kStages, C::kStageBytes, rows_cap, D, sizeof(T));
     const CtaState c = cta_state(smem, lay, C::kStages);
     init_cta(c, C::kStages);
@@ -982,7 +1117,9 @@ __global__ void __launch_bounds__(kThreads, 2)
             // every read of the slot (query rows, descriptor) must have completed
             // before the slot is handed back to the producer
             uint32_t all = (uint32_t)(it.seq ^ it.kvh ^ it.hg ^ it.len ^ it.j0 ^ it.j1 ^ it.qrow0 ^
-                                      it.rows ^ it.partial ^ it.prow0);
+                                      it.rows ^ it.partial ^ it.prow0 ^ it.tseq ^ it.packed ^
+                                      it.c_first ^ it.nparts) ^
+                           it.total_lo ^ it.total_hi;
 #pragma unroll
             for (int ks = 0; ks < KS; ++ks)
                 all ^= qa[ks][0] ^ qa[ks][1] ^ qa[ks][2] ^ qa[ks][3];
@@ -1211,7 +1348,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    const int rows_cap = min(kHeadsPerItem, p.group);
+    const int rows_cap = item_rows_cap(p);
     const SmemLayout lay = make_layout(C::kStages, C::kStageBytes, rows_cap, D, sizeof(float));
     const CtaState c = cta_state(smem, lay, C::kStages);
     init_cta(c, C::kStages);
@@ -1353,7 +1490,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         {
             const uint32_t all = __reduce_xor_sync(
                 0xffffffffu, (uint32_t)(it.seq ^ it.kvh ^ it.hg ^ it.len ^ it.j0 ^ it.j1 ^
-                                        it.qrow0 ^ it.rows ^ it.partial ^ it.prow0));
+                                        it.qrow0 ^ it.rows ^ it.partial ^ it.prow0 ^ it.tseq ^
+                                        it.packed ^ it.c_first ^ it.nparts) ^
+                                  it.total_lo ^ it.total_hi);
             if (lane == 0)
                 dev::settle_loads(&c.sink[warp], all);
         }
@@ -1469,10 +1608,10 @@ struct KernelOf<float, D, BS> {
 };
 
 template <typename T, int D, int BS>
-inline size_t smem_bytes_for(int group)
+inline size_t smem_bytes_for(int rows)
 {
     using C = Cfg<T, D, BS>;
-    const int rows = group < kHeadsPerItem ? group : kHeadsPerItem;
+    rows = rows < kHeadsPerItem ? rows : kHeadsPerItem;
     return make_layout(C::kStages, C::kStageBytes, rows, D, sizeof(T)).total;
 }
 
@@ -1483,7 +1622,7 @@ cudaError_t launch_decode_impl(const DecodeLaunch &L, cudaStream_t stream)
 {
     const DecodeParams &p = L.p;
     void *kern = KernelOf<T, D, BS>::get();
-    const size_t smem = smem_bytes_for<T, D, BS>(p.group);
+    const size_t smem = smem_bytes_for<T, D, BS>(item_rows_cap(p));
     const size_t smem_max = smem_bytes_for<T, D, BS>(kHeadsPerItem);
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);

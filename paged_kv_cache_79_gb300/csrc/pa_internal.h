@@ -50,6 +50,14 @@ struct DecodeParams {
     const void *v_new;
     void *k_cache;
     void *v_cache;
+    // Shared-prefix decode (null share: off).  share[s] = {first member of s's
+    // group, shared leading blocks}; pass 1 streams each group's shared blocks once
+    // for all members and writes fp32 rows + log2-sum-exp to pfx_o / pfx_lse
+    // ([S][Hq][D], [S][Hq]); pass 0 then covers each sequence's own blocks and merges.
+    const int32_t *share;
+    int pass;
+    float *pfx_o;
+    float *pfx_lse;
 };
 
 // Balanced split: partial slots are reserved for at most this many CTAs per SM.

@@ -14,7 +14,8 @@ from typing import Callable, List, Optional
 import numpy as np
 
 from . import (BlockAllocator, alloc_workspace, pa_copy_blocks, pa_decode, pa_decode_append,
-               pa_reshape_and_cache)
+               pa_decode_shared, pa_decode_shared_workspace_size, pa_reshape_and_cache,
+               share_groups)
 
 
 def _kind(ev) -> str:
@@ -53,6 +54,24 @@ class DecodeStep:
     block_size: int
     partition_size: int = 0
     fusable: bool = True        # step rows are the batch's newest tokens, in batch order
+    share: "object" = None      # int32 [S, 2] shared-prefix groups, None if none share
+
+    def run_shared(self, stream=None):
+        """copy-on-write pairs, then the shared-prefix decode (which also appends the new
+        tokens when the step is fusable)."""
+        if self.pairs.shape[0]:
+            pa_copy_blocks(self.k_cache, self.v_cache, self.pairs, stream)
+        if not self.fusable:
+            pa_reshape_and_cache(self.step_k, self.step_v, self.k_cache, self.v_cache, self.slots, stream)
+        return self.decode_shared(stream, append=self.fusable)
+
+    def decode_shared(self, stream=None, append=False):
+        return pa_decode_shared(self.out, self.q, self.k_cache, self.v_cache, self.block_tables,
+                                self.context_lens, self.share, self.scale, self.num_q_heads,
+                                self.num_kv_heads, self.head_dim, self.block_size,
+                                k_new=self.step_k if append else None,
+                                v_new=self.step_v if append else None,
+                                workspace=self.workspace, stream=stream)
 
     def run(self, stream=None):
         """copy-on-write pairs, then the new tokens' K/V, then decode."""
@@ -117,17 +136,28 @@ def execute(w, k_cache, v_cache, step_kv: Callable, query: Callable,
             bt, cl = tables_for(alloc, w.decode_seqs, width)
             S = len(w.decode_seqs)
             q = query(ev)
+            share = share_groups(bt, cl, w.block_size)
+            has_share = bool(np.any(share[:, 0] >= 0))
+            ws = alloc_workspace(S, w.num_q_heads, w.num_kv_heads, w.head_dim, w.block_size,
+                                 bt.shape[1], w.partition_size, dev)
+            if has_share and w.num_q_heads // w.num_kv_heads <= 16:
+                n = pa_decode_shared_workspace_size(S, w.num_q_heads, w.num_kv_heads, w.head_dim,
+                                                    w.block_size, bt.shape[1])
+                if ws is None or ws.numel() < n:
+                    ws = torch.empty(n, dtype=torch.uint8, device=dev)
+            else:
+                has_share = False
             ds = DecodeStep(
                 q=q, k_cache=k_cache, v_cache=v_cache, step_k=k, step_v=v,
                 slots=torch.tensor(slots, dtype=torch.int64, device=dev),
                 pairs=torch.tensor(np.array(pairs, dtype=np.int32).reshape(-1, 2), device=dev),
                 block_tables=torch.from_numpy(bt).to(dev), context_lens=torch.from_numpy(cl).to(dev),
                 out=torch.empty_like(q),
-                workspace=alloc_workspace(S, w.num_q_heads, w.num_kv_heads, w.head_dim, w.block_size,
-                                          bt.shape[1], w.partition_size, dev),
+                workspace=ws,
                 scale=w.softmax_scale, num_q_heads=w.num_q_heads, num_kv_heads=w.num_kv_heads,
                 head_dim=w.head_dim, block_size=w.block_size, partition_size=w.partition_size,
-                fusable=fusable)
+                fusable=fusable,
+                share=torch.from_numpy(share).to(dev) if has_share else None)
             if ds.pairs.shape[0]:
                 pa_copy_blocks(k_cache, v_cache, ds.pairs, stream)
             pa_reshape_and_cache(k, v, k_cache, v_cache, ds.slots, stream)

@@ -57,12 +57,17 @@ def test_tiny_fifty_appends_each_decoded():
     assert np.array_equal(raw(kc), kh) and np.array_equal(raw(vc), vh)
 
 
-def _check_workload(w, sample=None, min_seqs=0):
-    """Run `w` on both sides; compare allocator state, caches and sampled outputs."""
+def _check_workload(w, sample=None, min_seqs=0, shared=False):
+    """Run `w` on both sides; compare allocator state, caches and sampled outputs
+    (of pa_decode_shared over the groups the tables share, when `shared`)."""
     kc, vc = _gpu_tensors(w)
     kh, vh = raw(kc).copy(), raw(vc).copy()
     alloc, ds = runner.execute(w, kc, vc, _step_kv(w), _query(w))
-    out = ds.decode()
+    if shared:
+        assert ds.share is not None
+        out = ds.decode_shared()
+    else:
+        out = ds.decode()
     torch.cuda.synchronize()
 
     def step_kv_host(ev):
@@ -103,9 +108,10 @@ def test_gqa_bf16():
     _check_workload(W.gqa_bf16(), sample=_sample(16, 3))
 
 
+@pytest.mark.parametrize("shared", [False, True])
 @pytest.mark.parametrize("prompt", [1024, 1032])
-def test_shared_prefix_fp16(prompt):
-    _check_workload(W.shared_prefix_fp16(prompt_len=prompt), sample=_sample(24, 4))
+def test_shared_prefix_fp16(prompt, shared):
+    _check_workload(W.shared_prefix_fp16(prompt_len=prompt), sample=_sample(24, 4), shared=shared)
 
 
 def test_long_multiturn_bf16():
@@ -131,6 +137,11 @@ def test_long_multiturn_bf16():
         sbt[i, :n] = [remap[int(b)] for b in obt[s, :n]]
     want = oracle.decode(raw(ds.q)[seqs], ks, vs, sbt, ocl[seqs], w.softmax_scale, "bf16", 32, 8, 128, 32)
     assert_close(out[seqs], want, "bf16", w.name)
+    # the turns of a group share their leading blocks: the two-pass decode agrees too
+    assert ds.share is not None
+    out_s = ds.decode_shared().clone()
+    torch.cuda.synchronize()
+    assert_close(out_s[seqs], want, "bf16", w.name + " shared")
     # the step's appended rows landed where the oracle's allocator put them
     k_new, v_new = W.step_tensors(w, w.step_events()[-1], DEV)
     slots = ds.slots.cpu().numpy()
@@ -159,3 +170,35 @@ def test_fused_step_equals_separate_step(name):
     torch.cuda.synchronize()
     assert torch.equal(kc, k1) and torch.equal(vc, v1)
     assert torch.equal(ds.out, out1)
+
+
+def test_shared_step_equals_separate_step():
+    """The shared-prefix step (copy-on-write, then one launch per pass with the
+    append fused into the second) leaves the caches bit-identical to append then
+    decode, and its output matches the oracle on every sequence."""
+    w = W.shared_prefix_fp16(prompt_len=1032, prompts=4)
+    kc, vc = _gpu_tensors(w)
+    kh, vh = raw(kc).copy(), raw(vc).copy()
+    alloc, ds = runner.execute(w, kc, vc, _step_kv(w), _query(w))
+    assert ds.fusable and ds.share is not None
+    k0, v0 = kc.clone(), vc.clone()
+    ds.run()
+    torch.cuda.synchronize()
+    k1, v1 = kc.clone(), vc.clone()
+    kc.copy_(k0)
+    vc.copy_(v0)
+    ds.run_shared()
+    torch.cuda.synchronize()
+    assert torch.equal(kc, k1) and torch.equal(vc, v1)
+
+    def step_kv_host(ev):
+        k, v = W.step_tensors(w, ev, DEV)
+        return raw(k), raw(v)
+
+    oalloc, _ = oracle.run_script(w.events, w.num_blocks, w.block_size, w.free_order, kh, vh,
+                                  step_kv=step_kv_host)
+    obt, ocl = oracle.tables_for(oalloc, w.decode_seqs)
+    want = oracle.decode(raw(ds.q), kh, vh, obt, ocl, w.softmax_scale, w.dtype, w.num_q_heads,
+                         w.num_kv_heads, w.head_dim, w.block_size)
+    assert_close(ds.out, want, w.dtype, "shared step")
+    assert P.pa_device_errors() == 0

@@ -25,27 +25,32 @@ def cta_of(x, total, G):
 
 def walk(lens, units, bs, bps, G, cta):
     """Items of CTA `cta`: (seq, unit, j0, j1, partial, slot, c_first, nparts)."""
-    nss = [((t + bs - 1) // bs + bps - 1) // bps for t in lens]
-    total = sum(units * (UNIT_COST + ns) for ns in nss)
+    su = [(units, 0, (t + bs - 1) // bs) for t in lens]
+    return walk_units(su, bps, G, cta)
+
+
+def walk_units(su, bps, G, cta):
+    """Like walk, for per-sequence units: su[s] = (units, first block, end block)."""
+    nss = [(nb - start + bps - 1) // bps if n else 0 for (n, start, nb) in su]
+    total = sum(n * (UNIT_COST + ns) for (n, _, _), ns in zip(su, nss))
     s_c, e_c = cta * total // G, (cta + 1) * total // G
     items = []
     if s_c >= e_c:
         return items, total
     base = 0
-    for s, ns in enumerate(nss):
+    for s, ((units, start, nb), ns) in enumerate(zip(su, nss)):
         span = UNIT_COST + ns
         if base + units * span <= s_c:
             base += units * span
             continue
         if base >= e_c:
             break
-        nb = (lens[s] + bs - 1) // bs
         for u in range(units):
             a = base + u * span
             ra, rb = a + UNIT_COST, a + UNIT_COST + ns
             if ns == 0:
                 if s_c <= a < e_c:
-                    items.append((s, u, 0, 0, False, None, None, None))
+                    items.append((s, u, start, start, False, None, None, None))
                 continue
             lo, hi = max(ra, s_c), min(rb, e_c)
             if lo >= hi:
@@ -57,7 +62,8 @@ def walk(lens, units, bs, bps, G, cta):
                 cf, cl = cta_of(ra, total, G), cta_of(rb - 1, total, G)
                 nparts = 1 + sum(1 for c in range(cf + 1, cl + 1)
                                  if c * total // G < (c + 1) * total // G)
-            items.append((s, u, (lo - ra) * bps, min((hi - ra) * bps, nb), partial, slot, cf, nparts))
+            items.append((s, u, start + (lo - ra) * bps, min(start + (hi - ra) * bps, nb), partial,
+                          slot, cf, nparts))
         base += units * span
     return items, total
 
@@ -120,3 +126,109 @@ def test_single_long_sequence_spreads_over_every_cta():
 
 def test_more_ctas_than_positions():
     check([1, 0, 3], 2, 16, 2, 608)
+
+
+# ---------------------------------------------------------------------------
+# Shared-prefix decode: pass 1 streams each group's P shared blocks once per kv
+# head and member group (up to 16 // group members' query rows at a time), pass 0
+# every sequence's blocks P .. nb.  Together they must cover every (sequence,
+# query head, block) exactly once.
+# ---------------------------------------------------------------------------
+HEADS_PER_ITEM = 16
+
+
+def shared_units(lens, share, Hkv, group, bs, pass_):
+    hg = (group + HEADS_PER_ITEM - 1) // HEADS_PER_ITEM
+    out = []
+    S = len(lens)
+    for s in range(S):
+        nb = (lens[s] + bs - 1) // bs
+        P = share[s][1] if share[s][0] >= 0 else 0
+        if pass_ == 0:
+            out.append((Hkv * hg, min(P, nb), nb))
+            continue
+        if share[s][0] != s or P <= 0:
+            out.append((0, 0, 0))
+            continue
+        m = 1
+        while s + m < S and share[s + m][0] == s:
+            m += 1
+        mpi = HEADS_PER_ITEM // group
+        out.append((Hkv * ((m + mpi - 1) // mpi), 0, P))
+    return out
+
+
+def rows_of(pass_, s, u, share, lens, Hkv, group):
+    """(sequence, query head) pairs of unit u of sequence s."""
+    if pass_ == 1:
+        S = len(lens)
+        m = 1
+        while s + m < S and share[s + m][0] == s:
+            m += 1
+        mpi = HEADS_PER_ITEM // group
+        mgroups = (m + mpi - 1) // mpi
+        kvh, mg = divmod(u, mgroups)
+        members = range(s + mg * mpi, s + min(m, (mg + 1) * mpi))
+        return [(x, kvh * group + r) for x in members for r in range(group)]
+    hg = (group + HEADS_PER_ITEM - 1) // HEADS_PER_ITEM
+    kvh, h = divmod(u, hg)
+    rows = min(HEADS_PER_ITEM, group - h * HEADS_PER_ITEM)
+    return [(s, kvh * group + h * HEADS_PER_ITEM + r) for r in range(rows)]
+
+
+def check_shared(lens, share, Hkv, group, bs, bps, G):
+    cover = {}
+    for pass_ in (1, 0):
+        su = shared_units(lens, share, Hkv, group, bs, pass_)
+        for c in range(G):
+            items, _ = walk_units(su, bps, G, c)
+            for (s, u, j0, j1, _, _, _, _) in items:
+                rows = rows_of(pass_, s, u, share, lens, Hkv, group)
+                assert len(rows) <= HEADS_PER_ITEM
+                for j in range(j0, j1):
+                    for (x, h) in rows:
+                        key = (x, h, j)
+                        assert key not in cover, (pass_, key)
+                        cover[key] = pass_
+    for s, t in enumerate(lens):
+        nb = (t + bs - 1) // bs
+        for h in range(Hkv * group):
+            for j in range(nb):
+                assert (s, h, j) in cover, (s, h, j)
+                P = share[s][1] if share[s][0] >= 0 else 0
+                assert cover[(s, h, j)] == (1 if j < P else 0)
+    assert len(cover) == sum((t + bs - 1) // bs for t in lens) * Hkv * group
+
+
+def random_shared_batch(rng, bs):
+    lens, share = [], []
+    while len(lens) < rng.randint(1, 40):
+        m = rng.choice([1, 1, 2, 3, 8, 17, 33])
+        P = rng.choice([0, 1, 2, 5, 40])
+        first = len(lens)
+        for _ in range(m):
+            lens.append(P * bs + rng.randint(1, 3 * bs))
+            share.append((first, P) if (m > 1 and P > 0) else (-1, 0))
+    return lens, share
+
+
+@pytest.mark.parametrize("seed", range(30))
+def test_shared_prefix_passes_cover_every_block_once(seed):
+    rng = random.Random(1000 + seed)
+    bs = rng.choice([16, 32])
+    bps = 32 // bs
+    group = rng.choice([1, 2, 4, 5, 8, 16])
+    Hkv = rng.choice([1, 2, 3])
+    lens, share = random_shared_batch(rng, bs)
+    G = rng.choice([1, 3, 152, 304])
+    check_shared(lens, share, Hkv, group, bs, bps, G)
+
+
+def test_shared_prefix_workload_shape():
+    # 16 prompts x 8 samples, MHA 40 heads: pass 1 has 16 * 40 units of 16-row items
+    # with 8 rows used; pass 0 has 128 * 40 units of the private blocks
+    lens = [1024 + 1 + (i * 37) % 513 for i in range(128)]
+    share = [(8 * (i // 8), 64) for i in range(128)]
+    su1 = shared_units(lens, share, 40, 1, 16, 1)
+    assert sum(n for n, _, _ in su1) == 16 * 40
+    check_shared(lens[:24], share[:24], 2, 1, 16, 2, 152)

@@ -113,12 +113,23 @@ struct SmemLayout {
 
 constexpr int kItemSlots = 2;  // work-item descriptors (and their query rows) in flight
 
+constexpr int kNarrowRows = 8;  // items of at most this many rows use the transposed form
+
 // Most query rows one item of this launch carries: the heads of one head group,
 // or, in the shared-prefix pass, the rows of up to kHeadsPerItem / group member
 // sequences.  Sizes the merge accumulators in shared memory.
 __host__ __device__ inline int item_rows_cap(const DecodeParams &p)
 {
-    return p.pass == 1 ? kHeadsPerItem : (p.group < kHeadsPerItem ? p.group : kHeadsPerItem);
+    if (p.pass == 1)
+        return p.group <= kNarrowRows ? kNarrowRows : kHeadsPerItem;
+    return p.group < kHeadsPerItem ? p.group : kHeadsPerItem;
+}
+
+// Members of a group whose query rows share one shared-prefix item: the rows
+// fill the 8-row (group <= 8) or 16-row item.
+__host__ __device__ inline int members_per_item(int group)
+{
+    return (group <= kNarrowRows ? kNarrowRows : kHeadsPerItem) / group;
 }
 
 // Shared memory: stage ring | merge accumulators | merge (max, sum) | item
@@ -600,7 +611,7 @@ __device__ __forceinline__ SeqUnits seq_units(const DecodeParams &p, int s, int 
                 int m = 1;
                 while (s + m < p.num_seqs && p.share[2 * (s + m)] == s)
                     ++m;
-                const int mpi = kHeadsPerItem / p.group;
+                const int mpi = members_per_item(p.group);
                 u.members = m;
                 u.mgroups = (m + mpi - 1) / mpi;
                 u.nunits = p.num_kv_heads * u.mgroups;
@@ -713,7 +724,7 @@ __device__ __forceinline__ void walk_balanced(const DecodeParams &p, int bs, int
             const long long ra = a + kUnitCost;   // first real stage
             const long long rb = ra + ns;
             if (p.pass == 1) {
-                const int mpi = kHeadsPerItem / p.group;
+                const int mpi = members_per_item(p.group);
                 const int mg = (int)(u % su.mgroups);
                 const int members = min(mpi, su.members - mg * mpi);
                 it.seq = s + mg * mpi;
@@ -1031,9 +1042,226 @@ __device__ __forceinline__ void patch_newest_row(const DecodeParams &p, const It
 }
 
 // ---------------------------------------------------------------------------
-// fp16 / bf16 partition kernel: tensor-core consumers.
+// One item of at most 8 query rows on one consumer warp (its share of the
+// item's stages), in transposed form: S^T = K Q^T and O^T = V^T P^T.  Tokens
+// (scores) and head dims (output) take the MMA's 16-row side, the query rows
+// its 8-column side, so a 32-token stage costs 16 + 16 MMAs instead of the
+// 32 + 32 that the 16-row form spends on mostly empty rows.  The score
+// fragment turns into the B operand of P V by one movmatrix transpose per
+// 8 x 8 half.  Ends with the warp's partial rows in its merge area.
 // ---------------------------------------------------------------------------
 template <typename T, int D, int BS>
+__device__ __forceinline__ bool consume_item_n8(const DecodeParams &p, const CtaState &c,
+                                                const Item &it, uint32_t slot, uint32_t &g,
+                                                int warp, int lane, int rows_cap)
+{
+    using C = Cfg<T, D, BS>;
+    constexpr int kCE = C::kChunkElems;
+    constexpr int TS = C::kStageTokens;  // token rows per stage tile
+    constexpr int MT = TS / 16;          // 16-token tiles of S^T (= k-steps of P V)
+    constexpr int KS = D / 16;           // k-steps of K Q^T
+    constexpr int DM = D / 16;           // 16-dim tiles of O^T
+    constexpr int SA = D + kAccPad;
+    constexpr uint32_t kQSlotBytes = kHeadsPerItem * D * sizeof(T);
+    const int q4 = lane & 3;             // fragment columns: query rows 2 q4, 2 q4 + 1
+    const int r8 = lane >> 2;            // fragment row: token (S^T) or dim (O^T)
+    const int mi = lane >> 3;            // ldmatrix: which 8x8 matrix this lane addresses
+    const int swz = lane & 7;            // 128-byte swizzle: 16-byte unit ^= row % 8
+    const bool qlive = r8 < it.rows;
+
+    // Q^T as the B operand (k = head dim, n = query row): plain ldmatrix of the
+    // query rows; rows past the item are zero.
+    uint32_t qb[KS][2];
+    {
+        const uint32_t qbase = dev::smem_addr(c.qslots + slot * kQSlotBytes) +
+                               (uint32_t)((lane & 7) * D * sizeof(T));
+#pragma unroll
+        for (int kk = 0; kk < KS / 2; ++kk) {
+            uint32_t x0, x1, x2, x3;
+            dev::ldsm_x4(qbase + (uint32_t)((kk * 32 + mi * 8) * sizeof(T)), x0, x1, x2, x3);
+            qb[2 * kk][0] = qlive ? x0 : 0u;
+            qb[2 * kk][1] = qlive ? x1 : 0u;
+            qb[2 * kk + 1][0] = qlive ? x2 : 0u;
+            qb[2 * kk + 1][1] = qlive ? x3 : 0u;
+        }
+        uint32_t all = (uint32_t)(it.seq ^ it.kvh ^ it.hg ^ it.len ^ it.j0 ^ it.j1 ^ it.qrow0 ^
+                                  it.rows ^ it.partial ^ it.prow0 ^ it.tseq ^ it.packed ^
+                                  it.c_first ^ it.nparts) ^
+                       it.total_lo ^ it.total_hi;
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks)
+            all ^= qb[ks][0] ^ qb[ks][1];
+        all = __reduce_xor_sync(0xffffffffu, all);
+        if (lane == 0)
+            dev::settle_loads(&c.sink[warp], all);
+        __syncwarp();
+        if (lane == 0)
+            dev::mbar_arrive(dev::smem_addr(&c.item_empty[slot]));
+    }
+
+    float o[DM][4];
+#pragma unroll
+    for (int i = 0; i < DM; ++i)
+        o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+    float ma = -INFINITY, mb = -INFINITY;  // running max of rows 2 q4 and 2 q4 + 1
+    float la = 0.f, lb = 0.f;              // this lane's share of their exp sums
+    for (int j = it.j0; j < it.j1; j += C::kBPS, ++g) {
+        if ((int)(g % kConsumerWarps) != warp)
+            continue;
+        const uint32_t st = g % C::kStages;
+        if (!warp_wait(&c.full[st], (g / C::kStages) & 1u)) {
+            if (lane == 0)
+                raise_error(p, c.abort, PA_DEVERR_TIMEOUT_FULL);
+            return false;
+        }
+        const int valid = min(min(C::kBPS, it.j1 - j) * BS, it.len - j * BS);
+        const uint32_t kb = dev::smem_addr(c.ring + (size_t)st * C::kStageBytes);
+        const uint32_t vb = kb + C::kTileBytes;
+        if (c.newinfo[2 * st] >= 0)
+            patch_newest_row<T, D, TS, BS>(p, it, c, st, c.ring + (size_t)st * C::kStageBytes,
+                                           c.ring + (size_t)st * C::kStageBytes + C::kTileBytes,
+                                           lane);
+
+        // S^T = K Q^T: the K tile (rows = tokens) is the row-major A operand.
+        // Two accumulators per token tile (even / odd k-steps) shorten the chains.
+        float s[MT][2][4];
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+                s[mt][h][0] = s[mt][h][1] = s[mt][h][2] = s[mt][h][3] = 0.f;
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks) {
+            const int d = ks * 16 + (mi >> 1) * 8;
+            const uint32_t colpart = (uint32_t)(d / kCE) * (TS * 128) +
+                                     (uint32_t)((((d % kCE) >> 3) ^ swz) << 4);
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt) {
+                const int tok = mt * 16 + (mi & 1) * 8 + (lane & 7);
+                uint32_t a[4];
+                dev::ldsm_x4(kb + colpart + tok * 128, a[0], a[1], a[2], a[3]);
+                dev::Mma<T>::run(s[mt][ks & 1], a, qb[ks][0], qb[ks][1]);
+            }
+        }
+
+        // scores of tokens mt*16 + r8 (+8) for rows 2 q4, 2 q4 + 1: mask, scale, max
+        float mxa = -INFINITY, mxb = -INFINITY;
+        float sc[MT][4];
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                sc[mt][e] = s[mt][0][e] + s[mt][1][e];
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const bool ok = mt * 16 + r8 + 8 * h < valid;
+                sc[mt][2 * h] = ok ? sc[mt][2 * h] * p.scale_log2 : -INFINITY;
+                sc[mt][2 * h + 1] = ok ? sc[mt][2 * h + 1] * p.scale_log2 : -INFINITY;
+                mxa = fmaxf(mxa, sc[mt][2 * h]);
+                mxb = fmaxf(mxb, sc[mt][2 * h + 1]);
+            }
+        }
+#pragma unroll
+        for (int o_ = 4; o_ < 32; o_ <<= 1) {
+            mxa = fmaxf(mxa, __shfl_xor_sync(0xffffffffu, mxa, o_));
+            mxb = fmaxf(mxb, __shfl_xor_sync(0xffffffffu, mxb, o_));
+        }
+        const float na = fmaxf(ma, mxa), nb = fmaxf(mb, mxb);
+        const float ca = exp2f(ma - na), cb = exp2f(mb - nb);
+        ma = na;
+        mb = nb;
+        float pa = 0.f, pb = 0.f;
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) {
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                sc[mt][2 * h] = exp2f(sc[mt][2 * h] - na);
+                sc[mt][2 * h + 1] = exp2f(sc[mt][2 * h + 1] - nb);
+                pa += sc[mt][2 * h];
+                pb += sc[mt][2 * h + 1];
+            }
+        }
+        la = la * ca + pa;
+        lb = lb * cb + pb;
+        if (__any_sync(0xffffffffu, ca != 1.f || cb != 1.f)) {
+#pragma unroll
+            for (int i = 0; i < DM; ++i) {
+                o[i][0] *= ca;
+                o[i][1] *= cb;
+                o[i][2] *= ca;
+                o[i][3] *= cb;
+            }
+        }
+
+        // O^T += V^T P^T: ldmatrix.trans of the V tile (rows = tokens) gives the
+        // row-major A operand (m = head dim, k = token); P^T is the B operand.
+        const bool partial = valid < TS;
+#pragma unroll
+        for (int kt = 0; kt < MT; ++kt) {
+            const uint32_t pb0 = dev::movmatrix_trans(dev::Mma<T>::pack(sc[kt][0], sc[kt][1]));
+            const uint32_t pb1 = dev::movmatrix_trans(dev::Mma<T>::pack(sc[kt][2], sc[kt][3]));
+            // stale rows past the context may hold anything (NaN): zero them
+            uint32_t mk0 = 0xffffffffu, mk1 = 0xffffffffu;
+            if (partial) {
+                const int t0 = kt * 16 + 2 * q4;
+                mk0 = (t0 < valid ? 0x0000ffffu : 0u) | (t0 + 1 < valid ? 0xffff0000u : 0u);
+                mk1 = (t0 + 8 < valid ? 0x0000ffffu : 0u) | (t0 + 9 < valid ? 0xffff0000u : 0u);
+            }
+            const int tok = kt * 16 + (mi >> 1) * 8 + (lane & 7);
+#pragma unroll
+            for (int dm = 0; dm < DM; ++dm) {
+                const int d = dm * 16 + (mi & 1) * 8;
+                const uint32_t addr = vb + (uint32_t)(d / kCE) * (TS * 128) + tok * 128 +
+                                      (uint32_t)((((d % kCE) >> 3) ^ swz) << 4);
+                uint32_t a[4];
+                dev::ldsm_x4_trans(addr, a[0], a[1], a[2], a[3]);
+                a[0] &= mk0;
+                a[1] &= mk0;
+                a[2] &= mk1;
+                a[3] &= mk1;
+                dev::Mma<T>::run(o[dm], a, pb0, pb1);
+            }
+        }
+        __syncwarp();
+        if (lane == 0)
+            dev::mbar_arrive(dev::smem_addr(&c.empty[st]));
+    }
+
+    // partial rows of this warp: O^T fragment (dim dm*16 + r8 (+8), rows 2 q4, 2 q4 + 1)
+#pragma unroll
+    for (int o_ = 4; o_ < 32; o_ <<= 1) {
+        la += __shfl_xor_sync(0xffffffffu, la, o_);
+        lb += __shfl_xor_sync(0xffffffffu, lb, o_);
+    }
+    float *mine = c.macc + warp * rows_cap * SA;
+    const int ra = 2 * q4, rb = 2 * q4 + 1;
+    if (ra < it.rows) {
+#pragma unroll
+        for (int dm = 0; dm < DM; ++dm) {
+            mine[ra * SA + dm * 16 + r8] = o[dm][0];
+            mine[ra * SA + dm * 16 + r8 + 8] = o[dm][2];
+        }
+    }
+    if (rb < it.rows) {
+#pragma unroll
+        for (int dm = 0; dm < DM; ++dm) {
+            mine[rb * SA + dm * 16 + r8] = o[dm][1];
+            mine[rb * SA + dm * 16 + r8 + 8] = o[dm][3];
+        }
+    }
+    if (r8 == 0) {
+        c.mml[(warp * kHeadsPerItem + ra) * 2] = (ra < it.rows && la > 0.f) ? ma : -INFINITY;
+        c.mml[(warp * kHeadsPerItem + ra) * 2 + 1] = la;
+        c.mml[(warp * kHeadsPerItem + rb) * 2] = (rb < it.rows && lb > 0.f) ? mb : -INFINITY;
+        c.mml[(warp * kHeadsPerItem + rb) * 2 + 1] = lb;
+    }
+    return true;
+}
+
+// ---------------------------------------------------------------------------
+// fp16 / bf16 partition kernel: tensor-core consumers.
+// ---------------------------------------------------------------------------
+template <typename T, int D, int BS, bool N8>
 __global__ void __launch_bounds__(kThreads, 2)
     pa_decode_mma_kernel(const __grid_constant__ DecodeParams p,
                          const __grid_constant__ CUtensorMap tmap_k,
@@ -1097,6 +1325,10 @@ __global__ void __launch_bounds__(kThreads, 2)
         const Item it = load_item(&c.items[slot]);
         if (it.seq < 0)
             break;
+        if constexpr (N8) {
+            if (!consume_item_n8<T, D, BS>(p, c, it, slot, g, warp, lane, rows_cap))
+                break;
+        } else {
         const bool live0 = r0 < it.rows, live1 = r0 + 8 < it.rows;
 
         // Query fragments (A operand of Q K^T) from the item slot; rows past the
@@ -1273,9 +1505,6 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
         if (!alive)
             break;
-#ifdef PA_TRACE
-        const unsigned long long t_m0 = dev::global_timer_ns();
-#endif
 
         // ---- merge the four consumer warps ----
         lrow0 += __shfl_xor_sync(0xffffffffu, lrow0, 1);
@@ -1301,6 +1530,10 @@ __global__ void __launch_bounds__(kThreads, 2)
             c.mml[(warp * kHeadsPerItem + r0 + 8) * 2] = (live1 && lrow1 > 0.f) ? mrow1 : -INFINITY;
             c.mml[(warp * kHeadsPerItem + r0 + 8) * 2 + 1] = lrow1;
         }
+        }
+#ifdef PA_TRACE
+        const unsigned long long t_m0 = dev::global_timer_ns();
+#endif
         if (!consumer_sync(c, sph)) {
             if (lane == 0)
                 raise_error(p, c.abort, PA_DEVERR_TIMEOUT_FULL);
@@ -1598,13 +1831,19 @@ __global__ void __launch_bounds__(128)
 // ---------------------------------------------------------------------------
 // Launch helpers
 // ---------------------------------------------------------------------------
+// Items of at most 8 query rows (group <= 8) take the transposed-product
+// consumers; wider items the 16-row form.
 template <typename T, int D, int BS>
 struct KernelOf {
-    static void *get() { return reinterpret_cast<void *>(&pa_decode_mma_kernel<T, D, BS>); }
+    static void *get(bool narrow)
+    {
+        return narrow ? reinterpret_cast<void *>(&pa_decode_mma_kernel<T, D, BS, true>)
+                      : reinterpret_cast<void *>(&pa_decode_mma_kernel<T, D, BS, false>);
+    }
 };
 template <int D, int BS>
 struct KernelOf<float, D, BS> {
-    static void *get() { return reinterpret_cast<void *>(&pa_decode_f32_kernel<D, BS>); }
+    static void *get(bool) { return reinterpret_cast<void *>(&pa_decode_f32_kernel<D, BS>); }
 };
 
 template <typename T, int D, int BS>
@@ -1621,7 +1860,7 @@ template <typename T, int D, int BS>
 cudaError_t launch_decode_impl(const DecodeLaunch &L, cudaStream_t stream)
 {
     const DecodeParams &p = L.p;
-    void *kern = KernelOf<T, D, BS>::get();
+    void *kern = KernelOf<T, D, BS>::get(p.group <= kNarrowRows);
     const size_t smem = smem_bytes_for<T, D, BS>(item_rows_cap(p));
     const size_t smem_max = smem_bytes_for<T, D, BS>(kHeadsPerItem);
     int dev = 0;

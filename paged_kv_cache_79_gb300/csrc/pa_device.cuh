@@ -150,6 +150,15 @@ __device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t &r0, uint3
                  : "r"(addr));
 }
 
+// Transpose of an 8x8 matrix of 16-bit elements held one row per four lanes
+// (lane l: row l / 4, columns 2 (l % 4) and 2 (l % 4) + 1) into the same layout.
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t a)
+{
+    uint32_t d;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(a));
+    return d;
+}
+
 template <typename T>
 struct Mma;
 

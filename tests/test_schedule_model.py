@@ -130,11 +130,17 @@ def test_more_ctas_than_positions():
 
 # ---------------------------------------------------------------------------
 # Shared-prefix decode: pass 1 streams each group's P shared blocks once per kv
-# head and member group (up to 16 // group members' query rows at a time), pass 0
+# head and member group (the query rows of up to 8 // group members for groups
+# of at most 8 heads, else 16 // group), pass 0
 # every sequence's blocks P .. nb.  Together they must cover every (sequence,
 # query head, block) exactly once.
 # ---------------------------------------------------------------------------
 HEADS_PER_ITEM = 16
+NARROW_ROWS = 8
+
+
+def members_per_item(group):
+    return (NARROW_ROWS if group <= NARROW_ROWS else HEADS_PER_ITEM) // group
 
 
 def shared_units(lens, share, Hkv, group, bs, pass_):
@@ -153,7 +159,7 @@ def shared_units(lens, share, Hkv, group, bs, pass_):
         m = 1
         while s + m < S and share[s + m][0] == s:
             m += 1
-        mpi = HEADS_PER_ITEM // group
+        mpi = members_per_item(group)
         out.append((Hkv * ((m + mpi - 1) // mpi), 0, P))
     return out
 
@@ -165,7 +171,7 @@ def rows_of(pass_, s, u, share, lens, Hkv, group):
         m = 1
         while s + m < S and share[s + m][0] == s:
             m += 1
-        mpi = HEADS_PER_ITEM // group
+        mpi = members_per_item(group)
         mgroups = (m + mpi - 1) // mpi
         kvh, mg = divmod(u, mgroups)
         members = range(s + mg * mpi, s + min(m, (mg + 1) * mpi))
@@ -184,7 +190,8 @@ def check_shared(lens, share, Hkv, group, bs, bps, G):
             items, _ = walk_units(su, bps, G, c)
             for (s, u, j0, j1, _, _, _, _) in items:
                 rows = rows_of(pass_, s, u, share, lens, Hkv, group)
-                assert len(rows) <= HEADS_PER_ITEM
+                # the kernel sizes an item's accumulators for this many rows
+                assert len(rows) <= (NARROW_ROWS if group <= NARROW_ROWS else HEADS_PER_ITEM)
                 for j in range(j0, j1):
                     for (x, h) in rows:
                         key = (x, h, j)
@@ -225,8 +232,8 @@ def test_shared_prefix_passes_cover_every_block_once(seed):
 
 
 def test_shared_prefix_workload_shape():
-    # 16 prompts x 8 samples, MHA 40 heads: pass 1 has 16 * 40 units of 16-row items
-    # with 8 rows used; pass 0 has 128 * 40 units of the private blocks
+    # 16 prompts x 8 samples, MHA 40 heads: pass 1 has 16 * 40 units of 8-row items
+    # (all 8 samples); pass 0 has 128 * 40 units of the private blocks
     lens = [1024 + 1 + (i * 37) % 513 for i in range(128)]
     share = [(8 * (i // 8), 64) for i in range(128)]
     su1 = shared_units(lens, share, 40, 1, 16, 1)

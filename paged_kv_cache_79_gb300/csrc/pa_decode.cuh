@@ -89,6 +89,10 @@ __device__ __forceinline__ void trace_add(int slot, unsigned long long v)
     if (blockIdx.x < kTraceCtas)
         g_trace[blockIdx.x * kTraceSlots + slot] += v;
 }
+__device__ __forceinline__ bool trace_first_tile()
+{
+    return blockIdx.x < kTraceCtas && g_trace[blockIdx.x * kTraceSlots + 1] == 0;
+}
 #define PA_TRACE_SET(slot, v) trace_set((slot), (v))
 #define PA_TRACE_ADD(slot, v) trace_add((slot), (v))
 #define PA_TRACE_DEFINE_READER(name)                                                     \
@@ -687,6 +691,21 @@ __device__ __forceinline__ int find_seq_at(const DecodeParams &p, int bs, int bp
     return p.num_seqs;
 }
 
+// CTAs the balanced split spreads a stream of `total` positions over: the whole
+// grid once each CTA gets at least kMinPositions positions, fewer for small
+// batches, where cutting a unit between CTAs costs more (a partial store, a count
+// and a merge on the critical path) than the stages it spreads.  The rest of the
+// grid exits at once.
+#ifndef PA_MIN_POSITIONS
+#define PA_MIN_POSITIONS 4
+#endif
+constexpr long long kMinPositions = PA_MIN_POSITIONS;
+__device__ __forceinline__ long long balanced_grid(long long total)
+{
+    const long long g = (total + kMinPositions - 1) / kMinPositions;
+    return g < 1 ? 1 : (g < (long long)gridDim.x ? g : (long long)gridDim.x);
+}
+
 // CTA of a G-CTA grid whose stage range contains stream stage x.
 __device__ __forceinline__ long long cta_of(long long x, long long total, long long G)
 {
@@ -697,9 +716,11 @@ template <class Prod>
 __device__ __forceinline__ void walk_balanced(const DecodeParams &p, int bs, int bps, Prod &pr,
                                               int lane)
 {
-    const long long G = gridDim.x;
     const long long cta = blockIdx.x;
     const long long total = stream_total(p, bs, bps, lane);
+    const long long G = balanced_grid(total);
+    if (cta >= G)
+        return;
     const long long s_c = cta * total / G;
     const long long e_c = (cta + 1) * total / G;
     if (s_c >= e_c)
@@ -927,7 +948,7 @@ __device__ __forceinline__ void merge_split_unit(const DecodeParams &p, const It
 {
     constexpr int VEC = D / 32;
     const long long total = ((long long)it.total_hi << 32) | (long long)it.total_lo;
-    const long long G = gridDim.x;
+    const long long G = balanced_grid(total);
     for (int r = warp; r < it.rows; r += kConsumerWarps) {
         float M = -INFINITY;
         for (int i0 = 0; i0 < it.nparts; i0 += 32) {
@@ -1109,11 +1130,24 @@ __device__ __forceinline__ bool consume_item_n8(const DecodeParams &p, const Cta
         if ((int)(g % kConsumerWarps) != warp)
             continue;
         const uint32_t st = g % C::kStages;
+#ifdef PA_TRACE
+        const unsigned long long t_sw = dev::global_timer_ns();
+#endif
         if (!warp_wait(&c.full[st], (g / C::kStages) & 1u)) {
             if (lane == 0)
                 raise_error(p, c.abort, PA_DEVERR_TIMEOUT_FULL);
             return false;
         }
+#ifdef PA_TRACE
+        if (threadIdx.x == 0) {
+            const unsigned long long t_now = dev::global_timer_ns();
+            PA_TRACE_ADD(13, t_now - t_sw);
+            PA_TRACE_SET(11, t_now);
+            if (trace_first_tile()) {
+                PA_TRACE_SET(1, t_now);
+            }
+        }
+#endif
         const int valid = min(min(C::kBPS, it.j1 - j) * BS, it.len - j * BS);
         const uint32_t kb = dev::smem_addr(c.ring + (size_t)st * C::kStageBytes);
         const uint32_t vb = kb + C::kTileBytes;

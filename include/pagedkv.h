@@ -10,6 +10,10 @@
  *   [T]  CSDN tutorial "PagedAttention实战": §2.1 Page / PageTable, §2.2
  *        BlockManager, §3.1 SequenceManager.append_kv, §3.2 PagedAttention.compute,
  *        §5.1 clone_sequence.
+ *   [K]  Bidirectional KV-cache transfer for multi-turn prefill/decode-disaggregated
+ *        vLLM (spke.com translation of an AWS blog post): sections "Bidirectional
+ *        KV transfer" (KV blocks move between the nodes' pools) and "KV recompute
+ *        threshold" (default 64 tokens).
  *
  * Conventions shared by every entry point
  *   - All device buffers are allocated and owned by the caller.  The library never
@@ -272,6 +276,58 @@ pa_status pa_copy_blocks(void *k_cache, void *v_cache, const int32_t *src_dst_pa
                          int num_pairs, int num_blocks, size_t block_bytes, void *stream);
 
 /*
+ * pa_swap_blocks -- move whole blocks between two pools, e.g. the device pool and a
+ * pool in pinned host memory ([S] "vLLM": a preempted request's blocks move to CPU
+ * memory and come back when it resumes).
+ *
+ * Defines, for each pair i (src_i, dst_i) = src_dst_pairs[i]:
+ *     dst_k[dst_i] = src_k[src_i];  dst_v[dst_i] = src_v[src_i]
+ * with a block = block_bytes contiguous bytes, pools of src_num_blocks and
+ * dst_num_blocks blocks.  Each pool pointer may be device memory or pinned host
+ * memory mapped into the device's address space (cudaHostAlloc / cudaHostRegister
+ * memory under unified addressing); so may src_dst_pairs.  Pairs with an index out
+ * of range are skipped; destinations must be distinct and must not overlap a
+ * source of the same call.  Bit-exact.  pa_alloc_swap_out / pa_alloc_swap_in emit
+ * the pairs.
+ * Errors: PA_ERR_INVALID (null or misaligned pointer, bad size, or a pointer the
+ *   device cannot reach: pageable host memory, checked with cudaPointerGetAttributes
+ *   before the launch), PA_ERR_UNSUPPORTED (block_bytes above 1 GiB), PA_ERR_CUDA.
+ *   num_pairs = 0 is a no-op.
+ */
+pa_status pa_swap_blocks(const void *src_k, const void *src_v, void *dst_k, void *dst_v,
+                         const int32_t *src_dst_pairs, int num_pairs, int src_num_blocks,
+                         int dst_num_blocks, size_t block_bytes, void *stream);
+
+/*
+ * pa_gather_blocks / pa_scatter_blocks -- pack blocks of a pool into a contiguous
+ * staging buffer and unpack them into (other) blocks of a pool: the two local
+ * halves of moving a sequence's KV from one engine's pool to another's ([K]
+ * "Bidirectional KV transfer": the receiving side reads the sender's KV blocks and
+ * places them in its own blocks).
+ *     gather:  staging_k[i] = k_cache[block_ids[i]]   (and v), i < num_ids
+ *     scatter: k_cache[block_ids[i]] = staging_k[i]   (and v)
+ * staging_k / staging_v: [num_ids][block_bytes] contiguous, device or pinned host
+ * memory; block_ids: device-accessible int32 [num_ids].  Ids outside
+ * [0, num_blocks) are skipped (their staging block is left as it was).  Scatter ids
+ * must be distinct.  Bit-exact.  Errors as pa_swap_blocks.
+ */
+pa_status pa_gather_blocks(const void *k_cache, const void *v_cache, const int32_t *block_ids,
+                           int num_ids, int num_blocks, void *staging_k, void *staging_v,
+                           size_t block_bytes, void *stream);
+pa_status pa_scatter_blocks(const void *staging_k, const void *staging_v, void *k_cache,
+                            void *v_cache, const int32_t *block_ids, int num_ids, int num_blocks,
+                            size_t block_bytes, void *stream);
+
+/*
+ * Host predicate of [K] "KV recompute threshold": fetching another engine's KV for
+ * a prefix pays off only from threshold_tokens reusable tokens up (the article's
+ * default is 64); below it the receiver recomputes the prefix.  1 = transfer,
+ * 0 = recompute (also for reusable_tokens <= 0).
+ */
+int pa_kv_transfer_worthwhile(long long reusable_tokens, long long threshold_tokens);
+#define PA_KV_RECOMPUTE_THRESHOLD_DEFAULT 64
+
+/*
  * Device-side error flags of the current device (bitwise OR of PA_DEVERR_*), read
  * and cleared with a synchronous copy after `stream` drains.  A kernel that gives
  * up on a wait (a TMA transfer that never lands, ~2 s) sets a flag and returns
@@ -333,6 +389,41 @@ int pa_alloc_refcount(const pa_alloc *a, int block);     /* -1 if out of range *
 int pa_alloc_num_free(const pa_alloc *a);
 /* Copy up to `cap` free-list entries (bottom to top: the next pop is the last). */
 pa_status pa_alloc_free_list(const pa_alloc *a, int32_t *out, int cap, int *n);
+
+/*
+ * Swap space ([S] "vLLM": when GPU memory runs short, the scheduler pauses a
+ * request by moving its blocks to CPU memory, and brings them back later).
+ * pa_alloc_set_host_pool gives the allocator num_host_blocks blocks of host memory
+ * (ids 0..H-1, free list 0, 1, ..., H-1, popped from the end); allowed while no
+ * sequence is swapped out.
+ *
+ * pa_alloc_swap_out(seqs[0..n)): every distinct device block the sequences
+ * reference (met in the given sequence order, then table order) takes the next free
+ * host block; each reference moves to the host block (device refcount - 1, host
+ * refcount + 1; a device block reaching 0 goes to the end of the device free list,
+ * in release order).  pairs[2i], pairs[2i+1] = (device block, host block), in the
+ * order the host blocks were taken, *num_pairs = their count: the copies to run with
+ * pa_swap_blocks(device pool -> host pool) before the device blocks are reused.  A
+ * device block also held by a sequence that stays resident keeps its data and
+ * refcount; the swapped sequences get their own host copy.
+ * pa_alloc_swap_in is the reverse: (host block, device block) pairs, host blocks
+ * reaching 0 return to the end of the host free list.
+ * A swapped-out sequence keeps its length; pa_alloc_block_table returns its host
+ * block ids; pa_alloc_append / pa_alloc_fork refuse it (PA_ERR_INVALID);
+ * pa_alloc_free_seq releases its host blocks.
+ * Errors (nothing changes): PA_ERR_INVALID (a sequence not live, in the wrong pool,
+ * listed twice, or cap < the number of pairs, *num_pairs telling how many are
+ * needed), PA_ERR_OOM (fewer free blocks in the target pool than pairs).
+ */
+pa_status pa_alloc_set_host_pool(pa_alloc *a, int num_host_blocks);
+pa_status pa_alloc_swap_out(pa_alloc *a, const int *seqs, int n, int32_t *pairs, int cap,
+                            int *num_pairs);
+pa_status pa_alloc_swap_in(pa_alloc *a, const int *seqs, int n, int32_t *pairs, int cap,
+                           int *num_pairs);
+int pa_alloc_is_swapped(const pa_alloc *a, int seq);       /* 1, 0; -1 if not live */
+int pa_alloc_host_refcount(const pa_alloc *a, int block);  /* -1 if out of range */
+int pa_alloc_num_free_host(const pa_alloc *a);
+pa_status pa_alloc_host_free_list(const pa_alloc *a, int32_t *out, int cap, int *n);
 
 /*
  * Host helper: the share argument of pa_decode_shared, derived from the block

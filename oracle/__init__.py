@@ -17,7 +17,14 @@ Contents
                            pos % page_size); a negative slot skips the token.
   copy_blocks(...)         copy-on-write of whole blocks, pair by pair
                            (azimuth.plus summary, section "Memory sharing").
-  BlockAllocator           reference allocator (oracle/allocator.py).
+  swap_blocks(...)         block moves between two pools (summary, section "vLLM":
+                           a preempted request's blocks go to CPU memory and back).
+  gather_blocks(...),      pack blocks into a contiguous buffer and back (spke.com
+  scatter_blocks(...)      article on bidirectional KV transfer, section
+                           "Bidirectional KV transfer").
+  kv_transfer_worthwhile   the same article's recompute threshold (section "KV
+                           recompute threshold").
+  BlockAllocator           reference allocator (oracle/allocator.py), swap included.
   run_script(...)          execute a workload's allocator script with the above.
 
 Parity status: every function here is pinned by tests/test_oracle_*.py against
@@ -143,6 +150,46 @@ def copy_blocks(k_cache: np.ndarray, v_cache: np.ndarray, pairs: Sequence[Tuple[
     for src, dst in pairs:
         k_cache[dst] = k_cache[src]
         v_cache[dst] = v_cache[src]
+
+
+def swap_blocks(src_k: np.ndarray, src_v: np.ndarray, dst_k: np.ndarray, dst_v: np.ndarray,
+                pairs: Sequence[Tuple[int, int]]) -> None:
+    """dst[dst_i] = src[src_i] for every pair: block moves between two pools
+    (azimuth.plus summary, section "vLLM": blocks of a preempted request go to CPU
+    memory and come back).  Pairs with an index outside a pool are skipped."""
+    for s, d in pairs:
+        if 0 <= s < src_k.shape[0] and 0 <= d < dst_k.shape[0]:
+            dst_k[d] = src_k[s]
+            dst_v[d] = src_v[s]
+
+
+def gather_blocks(k_cache: np.ndarray, v_cache: np.ndarray, block_ids: Sequence[int]):
+    """Contiguous copies of the listed blocks, in order (the sending half of a KV
+    transfer; spke.com article, section "Bidirectional KV transfer").  Ids outside
+    the pool give zero blocks."""
+    ks = np.zeros((len(block_ids),) + k_cache.shape[1:], dtype=k_cache.dtype)
+    vs = np.zeros_like(ks)
+    for i, b in enumerate(block_ids):
+        if 0 <= b < k_cache.shape[0]:
+            ks[i] = k_cache[b]
+            vs[i] = v_cache[b]
+    return ks, vs
+
+
+def scatter_blocks(staging_k: np.ndarray, staging_v: np.ndarray, k_cache: np.ndarray,
+                   v_cache: np.ndarray, block_ids: Sequence[int]) -> None:
+    """cache[block_ids[i]] = staging[i] (the receiving half)."""
+    for i, b in enumerate(block_ids):
+        if 0 <= b < k_cache.shape[0]:
+            k_cache[b] = staging_k[i]
+            v_cache[b] = staging_v[i]
+
+
+def kv_transfer_worthwhile(reusable_tokens: int, threshold: int = 64) -> bool:
+    """spke.com article, section "KV recompute threshold": the prefill side
+    recomputes when fewer than `threshold` tokens could be reused and fetches the
+    KV when that many or more can (default 64)."""
+    return reusable_tokens > 0 and reusable_tokens >= threshold
 
 
 def run_script(events, num_blocks: int, block_size: int, free_order,

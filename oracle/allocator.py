@@ -19,6 +19,9 @@ Policy, from the pages:
     tutorial's append_kv writes into shared pages in place; the summary's
     copy-on-write rule is followed instead.)
 
+  * azimuth.plus summary, section "vLLM": under memory pressure the scheduler pauses
+    a request by moving its blocks to CPU memory (swap) and brings them back later.
+
 Readings where the pages are silent:
   * the initial free list is an explicit permutation (a seeded shuffle of the pool);
     allocation pops its last element;
@@ -27,6 +30,12 @@ Readings where the pages are silent:
   * OOM leaves every piece of state unchanged;
   * freeing a sequence walks its table from logical block 0 upwards;
   * the slot of a token is physical_block * block_size + offset.
+  * swapping moves whole sequences: each distinct block they hold (sequence order,
+    then table order) gets one block of the other pool, taken from the end of that
+    pool's free list; the host pool's free list starts as 0..H-1; a block another
+    resident sequence still holds keeps its data there, the swapped sequences get
+    their own copy; released blocks go to the end of their free list in release
+    order; a swapped-out sequence cannot grow or be forked until it is swapped in.
 """
 from __future__ import annotations
 
@@ -53,6 +62,9 @@ class BlockAllocator:
         self.ref: List[int] = [0] * num_blocks
         self.tables: Dict[int, List[int]] = {}
         self.lengths: Dict[int, int] = {}
+        self.swapped: Dict[int, bool] = {}
+        self.host_free: List[int] = []
+        self.host_ref: List[int] = []
         self._next_id = 0
 
     # -- tutorial §2.2 ---------------------------------------------------------
@@ -77,6 +89,8 @@ class BlockAllocator:
         return sid
 
     def fork(self, parent: int) -> int:
+        if self.swapped.get(parent):
+            raise ValueError("a swapped-out sequence cannot be forked")
         table = list(self.tables[parent])
         sid = self._next_id
         self._next_id += 1
@@ -91,6 +105,8 @@ class BlockAllocator:
 
         Returns (slot, cow) with cow = (src_block, dst_block) when the target block
         was shared and had to be copied, else None."""
+        if self.swapped.get(seq):
+            raise ValueError("a swapped-out sequence cannot grow")
         table = self.tables[seq]
         pos = self.lengths[seq]
         logical, offset = divmod(pos, self.block_size)
@@ -108,9 +124,74 @@ class BlockAllocator:
         return table[logical] * self.block_size + offset, cow
 
     def free_seq(self, seq: int) -> None:
+        on_host = self.swapped.pop(seq, False)
         for b in self.tables.pop(seq):
-            self._release(b)
+            if on_host:
+                self.host_ref[b] -= 1
+                if self.host_ref[b] == 0:
+                    self.host_free.append(b)
+            else:
+                self._release(b)
         del self.lengths[seq]
+
+    # -- swap space (summary section "vLLM") -------------------------------------
+    def set_host_pool(self, num_host_blocks: int) -> None:
+        if any(self.swapped.values()):
+            raise ValueError("sequences are swapped out")
+        self.host_free = list(range(num_host_blocks))
+        self.host_ref = [0] * num_host_blocks
+
+    def swap_out(self, seqs: Sequence[int]) -> List[Tuple[int, int]]:
+        """Move the sequences to the host pool; (device block, host block) copies."""
+        return self._move(seqs, to_host=True)
+
+    def swap_in(self, seqs: Sequence[int]) -> List[Tuple[int, int]]:
+        """Move the sequences back; (host block, device block) copies."""
+        return self._move(seqs, to_host=False)
+
+    def _move(self, seqs: Sequence[int], to_host: bool) -> List[Tuple[int, int]]:
+        seqs = [int(q) for q in seqs]
+        if len(set(seqs)) != len(seqs):
+            raise ValueError("a sequence is listed twice")
+        for q in seqs:
+            if q not in self.tables or self.swapped.get(q, False) == to_host:
+                raise ValueError(f"sequence {q} is not live in the source pool")
+        if to_host:
+            src_ref, src_free, dst_ref, dst_free = self.ref, self.free, self.host_ref, self.host_free
+        else:
+            src_ref, src_free, dst_ref, dst_free = self.host_ref, self.host_free, self.ref, self.free
+        distinct: List[int] = []
+        seen = set()
+        for q in seqs:
+            for b in self.tables[q]:
+                if b not in seen:
+                    seen.add(b)
+                    distinct.append(b)
+        if len(distinct) > len(dst_free):
+            raise OracleOOM("no free block in the target pool")
+        copy_of = {b: dst_free.pop() for b in distinct}
+        for q in seqs:
+            table = self.tables[q]
+            for j, b in enumerate(table):
+                dst_ref[copy_of[b]] += 1
+                src_ref[b] -= 1
+                if src_ref[b] == 0:
+                    src_free.append(b)
+                table[j] = copy_of[b]
+            self.swapped[q] = to_host
+        return [(b, copy_of[b]) for b in distinct]
+
+    def is_swapped(self, seq: int) -> bool:
+        return bool(self.swapped.get(seq, False))
+
+    def host_refcount(self, block: int) -> int:
+        return self.host_ref[block]
+
+    def num_free_host(self) -> int:
+        return len(self.host_free)
+
+    def host_free_list(self) -> List[int]:
+        return list(self.host_free)
 
     # -- views -----------------------------------------------------------------
     def block_table(self, seq: int) -> List[int]:

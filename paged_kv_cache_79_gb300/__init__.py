@@ -10,6 +10,9 @@ calls on tensors that are not CUDA tensors raise.
     pa_decode_shared        decode reading each shared prefix block once per group
     pa_reshape_and_cache    write new tokens' K/V rows through a slot mapping
     pa_copy_blocks          copy-on-write block copies
+    pa_swap_blocks          block moves between the device pool and pinned host memory
+    pa_gather_blocks /      pack blocks into a contiguous staging buffer and back
+      pa_scatter_blocks       (the local halves of a KV transfer)
     BlockAllocator          host ref-counted block allocator (pa_alloc_*)
 """
 from __future__ import annotations
@@ -55,6 +58,15 @@ def _dtype_code(t) -> int:
 def _cuda(t, name: str):
     if not t.is_cuda:
         raise ValueError(f"{name} must be a CUDA tensor (the library has no CPU path)")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t.data_ptr()
+
+
+def _dev_ptr(t, name: str):
+    """Pointer of a CUDA tensor or of a pinned host tensor (device-accessible)."""
+    if not (t.is_cuda or t.is_pinned()):
+        raise ValueError(f"{name} must be a CUDA tensor or pinned host memory")
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
     return t.data_ptr()
@@ -346,8 +358,96 @@ class BlockAllocator:
                "pa_alloc_free_list")
         return out[:n.value].tolist()
 
+    # swap space in host memory -------------------------------------------------
+    def set_host_pool(self, num_host_blocks: int) -> None:
+        _check(self._lib.pa_alloc_set_host_pool(self._h, num_host_blocks), "pa_alloc_set_host_pool")
+        self.num_host_blocks = num_host_blocks
+
+    def _move(self, fn, name, seqs):
+        import numpy as np
+        ids = np.ascontiguousarray(list(seqs), dtype=np.int32).reshape(-1)
+        n = ctypes.c_int()
+        cap = max(1, sum(len(self.block_table(q)) for q in ids.tolist())) if ids.size else 1
+        pairs = np.empty((cap, 2), dtype=np.int32)
+        _check(fn(self._h, ids.ctypes.data if ids.size else None, int(ids.size), pairs.ctypes.data, cap,
+                  ctypes.byref(n)), name)
+        return pairs[:n.value]
+
+    def swap_out(self, seqs) -> "object":
+        """Move `seqs` to the host pool: int32 [k, 2] (device block, host block) pairs."""
+        return self._move(self._lib.pa_alloc_swap_out, "pa_alloc_swap_out", seqs)
+
+    def swap_in(self, seqs) -> "object":
+        """Move `seqs` back to the device pool: int32 [k, 2] (host block, device block) pairs."""
+        return self._move(self._lib.pa_alloc_swap_in, "pa_alloc_swap_in", seqs)
+
+    def is_swapped(self, seq: int) -> bool:
+        v = self._lib.pa_alloc_is_swapped(self._h, seq)
+        if v < 0:
+            raise PagedKVError(PA_ERR_INVALID, "pa_alloc_is_swapped")
+        return bool(v)
+
+    def host_refcount(self, block: int) -> int:
+        return self._lib.pa_alloc_host_refcount(self._h, block)
+
+    def num_free_host(self) -> int:
+        return self._lib.pa_alloc_num_free_host(self._h)
+
+    def host_free_list(self) -> List[int]:
+        import numpy as np
+        n = ctypes.c_int()
+        _check(self._lib.pa_alloc_host_free_list(self._h, None, 0, ctypes.byref(n)), "pa_alloc_host_free_list")
+        out = np.empty(max(n.value, 1), dtype=np.int32)
+        _check(self._lib.pa_alloc_host_free_list(self._h, out.ctypes.data, n.value, ctypes.byref(n)),
+               "pa_alloc_host_free_list")
+        return out[:n.value].tolist()
+
+
+def _block_bytes(cache) -> int:
+    return cache[0].numel() * cache.element_size()
+
+
+def pa_swap_blocks(src_k, src_v, dst_k, dst_v, src_dst_pairs, stream=None):
+    """dst pool blocks <- src pool blocks for each (src, dst) pair; pools are [NB, ...]
+    tensors on the device or in pinned host memory (pairs likewise)."""
+    if src_dst_pairs.shape[0] == 0:
+        return
+    st = _load().pa_swap_blocks(_dev_ptr(src_k, "src_k"), _dev_ptr(src_v, "src_v"), _dev_ptr(dst_k, "dst_k"),
+                                _dev_ptr(dst_v, "dst_v"), _dev_ptr(src_dst_pairs, "src_dst_pairs"),
+                                int(src_dst_pairs.shape[0]), int(src_k.shape[0]), int(dst_k.shape[0]),
+                                _block_bytes(src_k), _stream(stream))
+    _check(st, "pa_swap_blocks")
+
+
+def pa_gather_blocks(k_cache, v_cache, block_ids, staging_k, staging_v, stream=None):
+    """staging[i] <- cache[block_ids[i]] (staging: [n, ...] device or pinned host tensors)."""
+    if block_ids.shape[0] == 0:
+        return
+    st = _load().pa_gather_blocks(_dev_ptr(k_cache, "k_cache"), _dev_ptr(v_cache, "v_cache"),
+                                  _dev_ptr(block_ids, "block_ids"), int(block_ids.shape[0]),
+                                  int(k_cache.shape[0]), _dev_ptr(staging_k, "staging_k"),
+                                  _dev_ptr(staging_v, "staging_v"), _block_bytes(k_cache), _stream(stream))
+    _check(st, "pa_gather_blocks")
+
+
+def pa_scatter_blocks(staging_k, staging_v, k_cache, v_cache, block_ids, stream=None):
+    """cache[block_ids[i]] <- staging[i]."""
+    if block_ids.shape[0] == 0:
+        return
+    st = _load().pa_scatter_blocks(_dev_ptr(staging_k, "staging_k"), _dev_ptr(staging_v, "staging_v"),
+                                   _dev_ptr(k_cache, "k_cache"), _dev_ptr(v_cache, "v_cache"),
+                                   _dev_ptr(block_ids, "block_ids"), int(block_ids.shape[0]),
+                                   int(k_cache.shape[0]), _block_bytes(k_cache), _stream(stream))
+    _check(st, "pa_scatter_blocks")
+
+
+def pa_kv_transfer_worthwhile(reusable_tokens: int, threshold_tokens: int = 64) -> bool:
+    """Fetch another engine's KV for a prefix (True) or recompute it (False)."""
+    return bool(_load().pa_kv_transfer_worthwhile(int(reusable_tokens), int(threshold_tokens)))
+
 
 __all__ = ["pa_decode", "pa_decode_append", "pa_decode_shared", "pa_decode_shared_workspace_size",
            "share_groups", "pa_decode_noalloc", "pa_decode_workspace_size", "pa_decode_partition_size", "alloc_workspace",
-           "pa_reshape_and_cache", "pa_copy_blocks", "pa_device_errors", "pa_status_string",
+           "pa_reshape_and_cache", "pa_copy_blocks", "pa_swap_blocks", "pa_gather_blocks",
+           "pa_scatter_blocks", "pa_kv_transfer_worthwhile", "pa_device_errors", "pa_status_string",
            "BlockAllocator", "PagedKVError", "OutOfBlocks", "library_path"]

@@ -51,6 +51,20 @@ SIGNATURES = {
     "pa_alloc_refcount": (c_int, [c_void_p, c_int]),
     "pa_alloc_num_free": (c_int, [c_void_p]),
     "pa_alloc_free_list": (c_int, [c_void_p, c_void_p, c_int, c_int_p]),
+    "pa_alloc_set_host_pool": (c_int, [c_void_p, c_int]),
+    "pa_alloc_swap_out": (c_int, [c_void_p, c_void_p, c_int, c_void_p, c_int, c_int_p]),
+    "pa_alloc_swap_in": (c_int, [c_void_p, c_void_p, c_int, c_void_p, c_int, c_int_p]),
+    "pa_alloc_is_swapped": (c_int, [c_void_p, c_int]),
+    "pa_alloc_host_refcount": (c_int, [c_void_p, c_int]),
+    "pa_alloc_num_free_host": (c_int, [c_void_p]),
+    "pa_alloc_host_free_list": (c_int, [c_void_p, c_void_p, c_int, c_int_p]),
+    "pa_swap_blocks": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_int, c_int,
+                               c_size_t, c_void_p]),
+    "pa_gather_blocks": (c_int, [c_void_p, c_void_p, c_void_p, c_int, c_int, c_void_p, c_void_p, c_size_t,
+                                 c_void_p]),
+    "pa_scatter_blocks": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_int, c_size_t,
+                                  c_void_p]),
+    "pa_kv_transfer_worthwhile": (c_int, [ctypes.c_longlong, ctypes.c_longlong]),
 }
 
 

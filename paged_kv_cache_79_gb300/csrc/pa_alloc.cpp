@@ -12,6 +12,7 @@
 // Host memory only; every failure leaves the state unchanged.
 #include <algorithm>
 #include <new>
+#include <unordered_map>
 #include <vector>
 
 #include "../../include/pagedkv.h"
@@ -21,8 +22,12 @@ struct pa_alloc {
     int block_size = 0;
     std::vector<int32_t> free_stack;            // top = back()
     std::vector<int32_t> refs;
+    int num_host_blocks = 0;                    // swap space in host memory
+    std::vector<int32_t> host_free;             // top = back()
+    std::vector<int32_t> host_refs;
     struct Seq {
         bool live = false;
+        bool swapped = false;                   // blocks are host-pool ids
         int64_t len = 0;
         std::vector<int32_t> blocks;
     };
@@ -34,6 +39,68 @@ namespace {
 bool live(const pa_alloc *a, int seq)
 {
     return a && seq >= 0 && seq < (int)a->seqs.size() && a->seqs[seq].live;
+}
+
+bool resident(const pa_alloc *a, int seq) { return live(a, seq) && !a->seqs[seq].swapped; }
+
+// Move every reference of seqs[0..n) from one pool to the other (swap out: device
+// -> host; swap in: host -> device).  Each distinct source block, met in sequence
+// order then table order, takes the top of the target pool's free stack; pairs get
+// (source, target) in that order.  Source blocks whose count reaches zero go to the
+// end of their free stack in the order the references are released.  All or
+// nothing: the checks come first.
+pa_status move_seqs(pa_alloc *a, const int *seqs, int n, bool out, int32_t *pairs, int cap,
+                    int *num_pairs)
+{
+    if (!a || n < 0 || (n > 0 && !seqs) || !num_pairs || cap < 0 || (cap > 0 && !pairs))
+        return PA_ERR_INVALID;
+    std::vector<int32_t> &src_refs = out ? a->refs : a->host_refs;
+    std::vector<int32_t> &dst_refs = out ? a->host_refs : a->refs;
+    std::vector<int32_t> &src_free = out ? a->free_stack : a->host_free;
+    std::vector<int32_t> &dst_free = out ? a->host_free : a->free_stack;
+    std::unordered_map<int32_t, int32_t> target;
+    std::vector<int32_t> order;
+    try {
+        for (int i = 0; i < n; ++i) {
+            const int q = seqs[i];
+            if (!live(a, q) || a->seqs[q].swapped != !out)
+                return PA_ERR_INVALID;
+            for (int k = 0; k < i; ++k)
+                if (seqs[k] == q)
+                    return PA_ERR_INVALID;
+            for (int32_t b : a->seqs[q].blocks)
+                if (target.emplace(b, -1).second)
+                    order.push_back(b);
+        }
+        src_free.reserve(src_refs.size());
+    } catch (...) {
+        return PA_ERR_OOM;
+    }
+    *num_pairs = (int)order.size();
+    if (order.size() > dst_free.size())
+        return PA_ERR_OOM;
+    if ((size_t)cap < order.size())
+        return PA_ERR_INVALID;
+    for (size_t i = 0; i < order.size(); ++i) {
+        const int32_t t = dst_free.back();
+        dst_free.pop_back();
+        dst_refs[t] = 0;
+        target[order[i]] = t;
+        pairs[2 * i] = order[i];
+        pairs[2 * i + 1] = t;
+    }
+    for (int i = 0; i < n; ++i) {
+        pa_alloc::Seq &sq = a->seqs[seqs[i]];
+        for (int32_t &b : sq.blocks) {
+            const int32_t t = target[b];
+            dst_refs[t] += 1;
+            if (--src_refs[b] == 0)
+                src_free.push_back(b);
+            b = t;
+        }
+        sq.swapped = out;
+    }
+    return PA_OK;
 }
 
 // One append; `stage` receives the copy pair.  No state changes on PA_ERR_OOM.
@@ -129,7 +196,7 @@ pa_status pa_alloc_new_seq(pa_alloc *a, int *seq_id)
 
 pa_status pa_alloc_fork(pa_alloc *a, int parent, int *child)
 {
-    if (!live(a, parent) || !child)
+    if (!resident(a, parent) || !child)
         return PA_ERR_INVALID;
     try {
         pa_alloc::Seq c;
@@ -148,7 +215,7 @@ pa_status pa_alloc_fork(pa_alloc *a, int parent, int *child)
 
 pa_status pa_alloc_append(pa_alloc *a, int seq, int64_t *slot, int32_t *cow_src, int32_t *cow_dst)
 {
-    if (!live(a, seq) || !slot)
+    if (!resident(a, seq) || !slot)
         return PA_ERR_INVALID;
     int32_t s = -1, d = -1;
     try {
@@ -167,7 +234,7 @@ pa_status pa_alloc_append(pa_alloc *a, int seq, int64_t *slot, int32_t *cow_src,
 pa_status pa_alloc_append_n(pa_alloc *a, int seq, int n, int64_t *slots, int32_t *cow_pairs,
                             int *num_cow, int *done)
 {
-    if (!live(a, seq) || n < 0 || (n > 0 && !slots) || !num_cow)
+    if (!resident(a, seq) || n < 0 || (n > 0 && !slots) || !num_cow)
         return PA_ERR_INVALID;
     *num_cow = 0;
     if (done)
@@ -199,21 +266,24 @@ pa_status pa_alloc_free_seq(pa_alloc *a, int seq)
     if (!live(a, seq))
         return PA_ERR_INVALID;
     pa_alloc::Seq &s = a->seqs[seq];
-    // the free stack never exceeds num_blocks entries, so reserve up front
+    std::vector<int32_t> &refs = s.swapped ? a->host_refs : a->refs;
+    std::vector<int32_t> &stack = s.swapped ? a->host_free : a->free_stack;
+    // a free stack never exceeds its pool's size, so reserve up front
     try {
-        a->free_stack.reserve(a->num_blocks);
+        stack.reserve(refs.size());
     } catch (...) {
         return PA_ERR_OOM;
     }
     for (int32_t b : s.blocks) {
-        a->refs[b] -= 1;
-        if (a->refs[b] == 0)
-            a->free_stack.push_back(b);
+        refs[b] -= 1;
+        if (refs[b] == 0)
+            stack.push_back(b);
     }
     s.blocks.clear();
     s.blocks.shrink_to_fit();
     s.len = 0;
     s.live = false;
+    s.swapped = false;
     return PA_OK;
 }
 
@@ -251,6 +321,61 @@ pa_status pa_alloc_free_list(const pa_alloc *a, int32_t *out, int cap, int *n)
     *n = (int)a->free_stack.size();
     std::copy(a->free_stack.begin(),
               a->free_stack.begin() + std::min<size_t>(a->free_stack.size(), (size_t)cap), out);
+    return PA_OK;
+}
+
+pa_status pa_alloc_set_host_pool(pa_alloc *a, int num_host_blocks)
+{
+    if (!a || num_host_blocks < 0)
+        return PA_ERR_INVALID;
+    for (const pa_alloc::Seq &q : a->seqs)
+        if (q.live && q.swapped)
+            return PA_ERR_INVALID;
+    try {
+        a->host_refs.assign(num_host_blocks, 0);
+        a->host_free.resize(num_host_blocks);
+    } catch (...) {
+        return PA_ERR_OOM;
+    }
+    for (int i = 0; i < num_host_blocks; ++i)
+        a->host_free[i] = i;
+    a->num_host_blocks = num_host_blocks;
+    return PA_OK;
+}
+
+pa_status pa_alloc_swap_out(pa_alloc *a, const int *seqs, int n, int32_t *pairs, int cap,
+                            int *num_pairs)
+{
+    return move_seqs(a, seqs, n, true, pairs, cap, num_pairs);
+}
+
+pa_status pa_alloc_swap_in(pa_alloc *a, const int *seqs, int n, int32_t *pairs, int cap,
+                           int *num_pairs)
+{
+    return move_seqs(a, seqs, n, false, pairs, cap, num_pairs);
+}
+
+int pa_alloc_is_swapped(const pa_alloc *a, int seq)
+{
+    return live(a, seq) ? (a->seqs[seq].swapped ? 1 : 0) : -1;
+}
+
+int pa_alloc_host_refcount(const pa_alloc *a, int block)
+{
+    if (!a || block < 0 || block >= a->num_host_blocks)
+        return -1;
+    return a->host_refs[block];
+}
+
+int pa_alloc_num_free_host(const pa_alloc *a) { return a ? (int)a->host_free.size() : -1; }
+
+pa_status pa_alloc_host_free_list(const pa_alloc *a, int32_t *out, int cap, int *n)
+{
+    if (!a || !n || cap < 0 || (cap > 0 && !out))
+        return PA_ERR_INVALID;
+    *n = (int)a->host_free.size();
+    std::copy(a->host_free.begin(),
+              a->host_free.begin() + std::min<size_t>(a->host_free.size(), (size_t)cap), out);
     return PA_OK;
 }
 

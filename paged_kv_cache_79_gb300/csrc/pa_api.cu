@@ -10,6 +10,8 @@
 
 #include "pa_internal.h"
 
+#include <initializer_list>
+
 #ifndef PA_L2_PROMOTION
 #define PA_L2_PROMOTION CU_TENSOR_MAP_L2_PROMOTION_L2_256B
 #endif
@@ -499,6 +501,102 @@ pa_status pa_copy_blocks(void *k_cache, void *v_cache, const int32_t *src_dst_pa
     const cudaError_t e = launch_copy_blocks(k_cache, v_cache, src_dst_pairs, num_pairs, num_blocks,
                                              block_bytes, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? PA_OK : cuda_fail(e);
+}
+
+namespace {
+// A pointer the kernels may dereference: device memory, managed memory, or pinned
+// host memory whose device address is the host address (unified addressing).
+bool device_accessible(const void *ptr)
+{
+    cudaPointerAttributes at;
+    if (cudaPointerGetAttributes(&at, ptr) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    if (at.type == cudaMemoryTypeDevice || at.type == cudaMemoryTypeManaged)
+        return true;
+    return at.type == cudaMemoryTypeHost && at.devicePointer == ptr;
+}
+
+bool all_accessible(std::initializer_list<const void *> ptrs)
+{
+    for (const void *p : ptrs)
+        if (!device_accessible(p))
+            return false;
+    return true;
+}
+}  // namespace
+
+pa_status pa_swap_blocks(const void *src_k, const void *src_v, void *dst_k, void *dst_v,
+                         const int32_t *src_dst_pairs, int num_pairs, int src_num_blocks,
+                         int dst_num_blocks, size_t block_bytes, void *stream)
+{
+    if (num_pairs == 0)
+        return PA_OK;
+    if (!src_k || !src_v || !dst_k || !dst_v || !src_dst_pairs || num_pairs < 0 ||
+        src_num_blocks <= 0 || dst_num_blocks <= 0 || block_bytes == 0 || block_bytes % 16 != 0)
+        return PA_ERR_INVALID;
+    if (!aligned(src_k, 16) || !aligned(src_v, 16) || !aligned(dst_k, 16) || !aligned(dst_v, 16) ||
+        !aligned(src_dst_pairs, 4))
+        return PA_ERR_INVALID;
+    if (block_bytes / 16 > 65535ull * 1024ull)
+        return PA_ERR_UNSUPPORTED;
+    if (!all_accessible({src_k, src_v, dst_k, dst_v, src_dst_pairs}))
+        return PA_ERR_INVALID;
+    const cudaError_t e = launch_move_blocks(src_k, src_v, dst_k, dst_v, src_dst_pairs, 2,
+                                             src_dst_pairs + 1, 2, num_pairs, src_num_blocks,
+                                             dst_num_blocks, block_bytes,
+                                             static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PA_OK : cuda_fail(e);
+}
+
+namespace {
+pa_status stage_blocks(const void *src_k, const void *src_v, void *dst_k, void *dst_v,
+                       const int32_t *block_ids, int num_ids, int num_blocks, size_t block_bytes,
+                       bool gather, void *stream)
+{
+    if (num_ids == 0)
+        return PA_OK;
+    if (!src_k || !src_v || !dst_k || !dst_v || !block_ids || num_ids < 0 || num_blocks <= 0 ||
+        block_bytes == 0 || block_bytes % 16 != 0)
+        return PA_ERR_INVALID;
+    if (!aligned(src_k, 16) || !aligned(src_v, 16) || !aligned(dst_k, 16) || !aligned(dst_v, 16) ||
+        !aligned(block_ids, 4))
+        return PA_ERR_INVALID;
+    if (block_bytes / 16 > 65535ull * 1024ull)
+        return PA_ERR_UNSUPPORTED;
+    if (!all_accessible({src_k, src_v, dst_k, dst_v, block_ids}))
+        return PA_ERR_INVALID;
+    const cudaError_t e =
+        gather ? launch_move_blocks(src_k, src_v, dst_k, dst_v, block_ids, 1, nullptr, 0, num_ids,
+                                    num_blocks, num_ids, block_bytes,
+                                    static_cast<cudaStream_t>(stream))
+               : launch_move_blocks(src_k, src_v, dst_k, dst_v, nullptr, 0, block_ids, 1, num_ids,
+                                    num_ids, num_blocks, block_bytes,
+                                    static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PA_OK : cuda_fail(e);
+}
+}  // namespace
+
+pa_status pa_gather_blocks(const void *k_cache, const void *v_cache, const int32_t *block_ids,
+                           int num_ids, int num_blocks, void *staging_k, void *staging_v,
+                           size_t block_bytes, void *stream)
+{
+    return stage_blocks(k_cache, v_cache, staging_k, staging_v, block_ids, num_ids, num_blocks,
+                        block_bytes, true, stream);
+}
+
+pa_status pa_scatter_blocks(const void *staging_k, const void *staging_v, void *k_cache,
+                            void *v_cache, const int32_t *block_ids, int num_ids, int num_blocks,
+                            size_t block_bytes, void *stream)
+{
+    return stage_blocks(staging_k, staging_v, k_cache, v_cache, block_ids, num_ids, num_blocks,
+                        block_bytes, false, stream);
+}
+
+int pa_kv_transfer_worthwhile(long long reusable_tokens, long long threshold_tokens)
+{
+    return reusable_tokens > 0 && reusable_tokens >= threshold_tokens ? 1 : 0;
 }
 
 pa_status pa_device_errors(unsigned int *flags, void *stream)

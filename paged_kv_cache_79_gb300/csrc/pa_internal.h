@@ -99,6 +99,10 @@ void note_cuda_error(cudaError_t e);
 cudaError_t launch_reshape_and_cache(const void *k, const void *v, void *k_cache, void *v_cache,
                                      const int64_t *slots, int num_tokens, size_t row_bytes,
                                      long long num_slots, cudaStream_t stream);
+cudaError_t launch_move_blocks(const void *src_k, const void *src_v, void *dst_k, void *dst_v,
+                               const int32_t *src_ids, int src_stride, const int32_t *dst_ids,
+                               int dst_stride, int num, int src_blocks, int dst_blocks,
+                               size_t block_bytes, cudaStream_t stream);
 cudaError_t launch_copy_blocks(void *k_cache, void *v_cache, const int32_t *pairs, int num_pairs,
                                int num_blocks, size_t block_bytes, cudaStream_t stream);
 

@@ -468,6 +468,87 @@ def run_reference(args):
                     "d2h_bytes_per_step": 0}}
 
 
+# ----------------------------------------------------------------------------
+# secondary measurements (not the headline step): block moves and pool accounting
+# ----------------------------------------------------------------------------
+def run_blocks(args):
+    """GB/s of the block-move kernels: swap between the device pool and pinned host
+    memory, staging gathers/scatters on the device.  Bytes = blocks moved x block
+    bytes x 2 (K and V), counted once per move."""
+    import numpy as np
+    import torch
+    import paged_kv_cache_79_gb300 as P
+    from paged_kv_cache_79_gb300 import build as libbuild
+    libbuild.build()
+    dev = "cuda:0"
+    nb, n, shape = 4096, 2048, (16, 40, 128)      # MHA fp16 blocks of 160 KB
+    g = torch.Generator(device=dev).manual_seed(7)
+    kc = torch.randn((nb,) + shape, device=dev, generator=g).half()
+    vc = torch.randn((nb,) + shape, device=dev, generator=g).half()
+    hk = torch.empty((n,) + shape, dtype=torch.float16).pin_memory()
+    hv = torch.empty_like(hk).pin_memory()
+    dk = torch.empty((n,) + shape, dtype=torch.float16, device=dev)
+    dv = torch.empty_like(dk)
+    ids = torch.from_numpy(np.random.default_rng(0).permutation(nb)[:n].astype(np.int32)).to(dev)
+    seq = torch.arange(n, dtype=torch.int32, device=dev)
+    p_out = torch.stack([ids, seq], 1).contiguous()
+    p_in = torch.stack([seq, ids], 1).contiguous()
+    moved = 2 * n * kc[0].numel() * kc.element_size()
+    flush = L2Flush(dev)
+
+    def timed(fn):
+        for _ in range(args.warmup):
+            fn()
+        ts = []
+        for _ in range(args.steps):
+            flush()
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            b.record()
+            b.synchronize()
+            ts.append(a.elapsed_time(b))
+        ms = sorted(ts)[len(ts) // 2]
+        return {"us": round(ms * 1000, 1), "GB/s": round(moved / (ms * 1e-3) / 1e9, 1)}
+
+    res = {
+        "swap_out_device_to_pinned_host": timed(lambda: P.pa_swap_blocks(kc, vc, hk, hv, p_out)),
+        "swap_in_pinned_host_to_device": timed(lambda: P.pa_swap_blocks(hk, hv, kc, vc, p_in)),
+        "gather_device_to_device": timed(lambda: P.pa_gather_blocks(kc, vc, ids, dk, dv)),
+        "scatter_device_to_device": timed(lambda: P.pa_scatter_blocks(dk, dv, kc, vc, ids)),
+        "copy_engine_device_to_pinned_host_contiguous": timed(
+            lambda: (hk.copy_(dk, non_blocking=True), hv.copy_(dv, non_blocking=True))),
+    }
+    peak, kind = measured_peak()
+    return {"op": "blocks", "blocks": n, "block_bytes": kc[0].numel() * kc.element_size(),
+            "bytes_per_move": moved, "results": res,
+            "device_copy_frac": round(2 * res["gather_device_to_device"]["GB/s"] / peak, 4),
+            "device_copy_note": f"device-to-device moves read and write each byte: 2 x GB/s vs the "
+                                f"{kind} copy bandwidth {peak} GB/s",
+            "steps": args.steps, "warmup": args.warmup}
+
+
+def run_memory(args):
+    """Pool accounting on allocator traces (host only): waste of slots and the
+    saving from shared blocks, after the last step of each trace."""
+    import workloads as W
+    from paged_kv_cache_79_gb300 import build as libbuild
+    from paged_kv_cache_79_gb300 import runner
+    libbuild.build()
+    res = {}
+    for name, kw in [("shared_prefix_fp16", {}), ("shared_prefix_fp16", {"prompt_len": 1032}),
+                     ("beam_search_fp16", {"beams": 4}), ("beam_search_fp16", {"beams": 8}),
+                     ("long_multiturn_bf16", {}), ("gqa_bf16", {})]:
+        w = W.by_name(name, **kw)
+        u = runner.replay_usage(w)
+        last = u[-1]
+        res[w.name] = {"used_blocks": last["used_blocks"], "logical_blocks": last["logical_blocks"],
+                       "waste": round(last["waste"], 4), "sharing_saving": round(last["sharing_saving"], 4),
+                       "mean_sharing_saving_over_steps": round(sum(x["sharing_saving"] for x in u) / len(u), 4)}
+    return {"op": "memory", "data": "synthetic allocator traces", "results": res}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -481,10 +562,18 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=10.0)
     ap.add_argument("--no-share", action="store_true",
                     help="decode every sequence's blocks separately even where groups share a prefix")
+    ap.add_argument("--op", default="decode", choices=["decode", "blocks", "memory"],
+                    help="decode: the headline step (default); blocks: block-move GB/s; "
+                         "memory: pool accounting on allocator traces")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
-    line = run_reference(args) if args.impl == "reference" else run_ours(args)
+    if args.op == "blocks":
+        line = run_blocks(args)
+    elif args.op == "memory":
+        line = run_memory(args)
+    else:
+        line = run_reference(args) if args.impl == "reference" else run_ours(args)
     if line is not None:
         print(json.dumps(line), flush=True)
 

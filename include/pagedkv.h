@@ -416,6 +416,30 @@ pa_status pa_alloc_free_list(const pa_alloc *a, int32_t *out, int cap, int *n);
  * needed), PA_ERR_OOM (fewer free blocks in the target pool than pairs).
  */
 pa_status pa_alloc_set_host_pool(pa_alloc *a, int num_host_blocks);
+
+/*
+ * Memory accounting of the device pool ([S] "Results": the remaining waste of paged
+ * KV memory is the unfilled tail of each sequence's last block, under B tokens;
+ * [S] "Memory sharing": forked samples and beams share blocks).  Over the resident
+ * (not swapped-out) sequences:
+ *   used_blocks     device blocks with refcount > 0
+ *   logical_blocks  table entries summed over the sequences (what unshared
+ *                   per-sequence storage would take)
+ *   token_slots     used_blocks * block_size
+ *   tokens          slots holding a token: per used block, the largest number of
+ *                   rows any of its holders has filled
+ * Waste fraction = 1 - tokens / token_slots; sharing saving = 1 - used_blocks /
+ * logical_blocks.
+ */
+typedef struct {
+    int64_t used_blocks;
+    int64_t logical_blocks;
+    int64_t token_slots;
+    int64_t tokens;
+    int64_t resident_seqs;
+    int64_t swapped_seqs;
+} pa_alloc_usage;
+pa_status pa_alloc_usage_stats(const pa_alloc *a, pa_alloc_usage *out);
 pa_status pa_alloc_swap_out(pa_alloc *a, const int *seqs, int n, int32_t *pairs, int cap,
                             int *num_pairs);
 pa_status pa_alloc_swap_in(pa_alloc *a, const int *seqs, int n, int32_t *pairs, int cap,

@@ -181,6 +181,27 @@ class BlockAllocator:
             self.swapped[q] = to_host
         return [(b, copy_of[b]) for b in distinct]
 
+    # -- accounting: summary sections "Results" (waste) and "Memory sharing" ------
+    def usage(self) -> Dict[str, int]:
+        """used_blocks, logical_blocks, token_slots, tokens over resident sequences
+        (tokens: for each used block, the most rows any holder has filled)."""
+        filled: Dict[int, int] = {}
+        logical = 0
+        resident = swapped = 0
+        for seq, table in self.tables.items():
+            if self.swapped.get(seq):
+                swapped += 1
+                continue
+            resident += 1
+            logical += len(table)
+            T = self.lengths[seq]
+            for j, b in enumerate(table):
+                rows = min(self.block_size, T - j * self.block_size)
+                filled[b] = max(filled.get(b, 0), rows)
+        used = sum(1 for r in self.ref if r > 0)
+        return {"used_blocks": used, "logical_blocks": logical, "token_slots": used * self.block_size,
+                "tokens": sum(filled.values()), "resident_seqs": resident, "swapped_seqs": swapped}
+
     def is_swapped(self, seq: int) -> bool:
         return bool(self.swapped.get(seq, False))
 

@@ -358,6 +358,19 @@ class BlockAllocator:
                "pa_alloc_free_list")
         return out[:n.value].tolist()
 
+    def usage(self) -> dict:
+        """Device-pool accounting (pa_alloc_usage_stats) plus the derived waste and
+        sharing-saving fractions."""
+        class _Usage(ctypes.Structure):
+            _fields_ = [(n, ctypes.c_int64) for n in ("used_blocks", "logical_blocks", "token_slots",
+                                                       "tokens", "resident_seqs", "swapped_seqs")]
+        u = _Usage()
+        _check(self._lib.pa_alloc_usage_stats(self._h, ctypes.byref(u)), "pa_alloc_usage_stats")
+        d = {n: getattr(u, n) for n, _ in _Usage._fields_}
+        d["waste"] = 1.0 - d["tokens"] / d["token_slots"] if d["token_slots"] else 0.0
+        d["sharing_saving"] = 1.0 - d["used_blocks"] / d["logical_blocks"] if d["logical_blocks"] else 0.0
+        return d
+
     # swap space in host memory -------------------------------------------------
     def set_host_pool(self, num_host_blocks: int) -> None:
         _check(self._lib.pa_alloc_set_host_pool(self._h, num_host_blocks), "pa_alloc_set_host_pool")

@@ -52,6 +52,7 @@ SIGNATURES = {
     "pa_alloc_num_free": (c_int, [c_void_p]),
     "pa_alloc_free_list": (c_int, [c_void_p, c_void_p, c_int, c_int_p]),
     "pa_alloc_set_host_pool": (c_int, [c_void_p, c_int]),
+    "pa_alloc_usage_stats": (c_int, [c_void_p, c_void_p]),
     "pa_alloc_swap_out": (c_int, [c_void_p, c_void_p, c_int, c_void_p, c_int, c_int_p]),
     "pa_alloc_swap_in": (c_int, [c_void_p, c_void_p, c_int, c_void_p, c_int, c_int_p]),
     "pa_alloc_is_swapped": (c_int, [c_void_p, c_int]),

@@ -324,6 +324,44 @@ pa_status pa_alloc_free_list(const pa_alloc *a, int32_t *out, int cap, int *n)
     return PA_OK;
 }
 
+pa_status pa_alloc_usage_stats(const pa_alloc *a, pa_alloc_usage *out)
+{
+    if (!a || !out)
+        return PA_ERR_INVALID;
+    pa_alloc_usage u = {};
+    // rows of each device block that hold a token of some resident sequence: rows
+    // fill from 0 upward, so it is the largest count any holder has in it
+    std::vector<int32_t> rows;
+    try {
+        rows.assign(a->num_blocks, 0);
+    } catch (...) {
+        return PA_ERR_OOM;
+    }
+    for (const pa_alloc::Seq &q : a->seqs) {
+        if (!q.live)
+            continue;
+        if (q.swapped) {
+            u.swapped_seqs += 1;
+            continue;
+        }
+        u.resident_seqs += 1;
+        u.logical_blocks += (int64_t)q.blocks.size();
+        for (size_t j = 0; j < q.blocks.size(); ++j) {
+            const int64_t r = std::min<int64_t>(a->block_size, q.len - (int64_t)j * a->block_size);
+            rows[q.blocks[j]] = std::max<int32_t>(rows[q.blocks[j]], (int32_t)r);
+        }
+    }
+    for (int b = 0; b < a->num_blocks; ++b) {
+        if (a->refs[b] > 0) {
+            u.used_blocks += 1;
+            u.tokens += rows[b];
+        }
+    }
+    u.token_slots = u.used_blocks * a->block_size;
+    *out = u;
+    return PA_OK;
+}
+
 pa_status pa_alloc_set_host_pool(pa_alloc *a, int num_host_blocks)
 {
     if (!a || num_host_blocks < 0)

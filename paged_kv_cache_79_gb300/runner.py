@@ -167,3 +167,28 @@ def execute(w, k_cache, v_cache, step_kv: Callable, query: Callable,
         else:
             raise TypeError(f"unknown event {ev!r}")
     return alloc, last
+
+
+def replay_usage(w, host_blocks: int = 0):
+    """Run `w`'s allocator script on the host only (no device data) and return the
+    device-pool accounting (BlockAllocator.usage) after every decode step."""
+    alloc = BlockAllocator(w.num_blocks, w.block_size, w.free_order)
+    out = []
+    for ev in w.events:
+        kind = _kind(ev)
+        if kind == "NewSeq":
+            alloc.new_seq()
+        elif kind == "Fork":
+            alloc.fork(ev.parent)
+        elif kind == "FreeSeq":
+            alloc.free_seq(ev.seq)
+        elif kind == "Prefill":
+            if ev.n > 0:
+                alloc.append_n(ev.seq, ev.n)
+        elif kind == "Step":
+            for q in ev.seqs:
+                alloc.append(q)
+            out.append(alloc.usage())
+        else:
+            raise TypeError(f"unknown event {ev!r}")
+    return out

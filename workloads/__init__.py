@@ -259,6 +259,42 @@ def long_multiturn_bf16(groups: int = 64, lo: int = 128, hi: int = 131072) -> Wo
                     sorted(order), partition_size=512, data_seed=2004)
 
 
+def beam_search_fp16(beams: int = 4, prompt_len: int = 500, steps: int = 200, seed: int = 6,
+                     pool: Optional[int] = None) -> Workload:
+    """Beam search over one prompt (allocator trace; MHA fp16 shapes as in the
+    parallel-sampling configuration).
+
+    The prompt is prefilled once and forked into `beams` beams.  At every step each
+    of the `beams` new beams picks its parent among the current beams (seeded,
+    uniform, with replacement), is created as a fork of it, the previous beams are
+    freed, and every new beam appends one token -- so beams that share a parent share
+    its blocks and copy the partial last block on their first write."""
+    rng = _rng(20 + seed)
+    b = 16
+    ev: List[object] = [NewSeq(), Prefill(0, prompt_len)]
+    cur = [0]
+    nxt = 1
+    for _ in range(beams - 1):
+        ev.append(Fork(0))
+        cur.append(nxt)
+        nxt += 1
+    for k in range(steps):
+        parents = rng.integers(0, beams, size=beams)
+        new = []
+        for p_ in parents:
+            ev.append(Fork(cur[int(p_)]))
+            new.append(nxt)
+            nxt += 1
+        for q in cur:
+            ev.append(FreeSeq(q))
+        cur = new
+        ev.append(Step(tuple(cur), k))
+    if pool is None:
+        pool = 2 * beams * (_blocks(prompt_len + steps, b) + 2) + 8
+    return Workload(f"beam_search_fp16_k{beams}", 40, 40, 128, b, "f16", pool, free_order(pool, rng), ev,
+                    list(cur), data_seed=2006)
+
+
 def by_name(name: str, **kw) -> Workload:
     table = {
         "tiny": tiny,
@@ -267,6 +303,7 @@ def by_name(name: str, **kw) -> Workload:
         "shared_prefix_fp16": shared_prefix_fp16,
         "shared_prefix_fp16_p1032": lambda **k: shared_prefix_fp16(prompt_len=1032, **k),
         "long_multiturn_bf16": long_multiturn_bf16,
+        "beam_search_fp16": beam_search_fp16,
     }
     return table[name](**kw)
 

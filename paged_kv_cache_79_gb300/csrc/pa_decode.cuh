@@ -226,16 +226,20 @@ struct Item {
     int c_first, nparts;
     unsigned int total_lo, total_hi;  // stream length (to tell empty CTA ranges)
     int tseq;               // sequence whose block-table row gives the blocks
-    int packed;             // members << 16 | rows per member << 8 | kToPrefix/kMergePrefix
+    int packed;             // members << 16 | rows per member << 8 | rot << 2 | flags
     __device__ int members() const { return packed >> 16; }
     __device__ int rpm() const { return (packed >> 8) & 0xff; }
-    __device__ int flags() const { return packed & 0xff; }
+    __device__ int flags() const { return packed & 3; }  // kToPrefix / kMergePrefix
+    // Stage i of the item goes to consumer warp (i + rot) % 4.  rot is a function of
+    // the item alone (not of the CTA that runs it), so the warps' partial sums, and
+    // with them the rounding of the result, do not depend on the schedule.
+    __device__ int rot() const { return (packed >> 2) & 3; }
 };
 static_assert(sizeof(Item) == 64, "one 64-byte descriptor slot");
 
-__device__ __forceinline__ int pack_rows(int members, int rpm, int flags)
+__device__ __forceinline__ int pack_rows(int members, int rpm, int flags, int rot = 0)
 {
-    return (members << 16) | (rpm << 8) | flags;
+    return (members << 16) | (rpm << 8) | ((rot & 3) << 2) | flags;
 }
 
 __device__ __forceinline__ Item decode_item(const DecodeParams &p, int bs, long long w, int seq,
@@ -269,7 +273,7 @@ __device__ __forceinline__ Item decode_item(const DecodeParams &p, int bs, long 
     it.nparts = 0;
     it.total_lo = it.total_hi = 0;
     it.tseq = seq;
-    it.packed = pack_rows(1, it.rows, 0);
+    it.packed = pack_rows(1, it.rows, 0, (int)(w & 3));
     return it;
 }
 
@@ -695,7 +699,9 @@ __device__ __forceinline__ int find_seq_at(const DecodeParams &p, int bs, int bp
 // grid once each CTA gets at least kMinPositions positions, fewer for small
 // batches, where cutting a unit between CTAs costs more (a partial store, a count
 // and a merge on the critical path) than the stages it spreads.  The rest of the
-// grid exits at once.
+// grid exits at once.  (Cutting the stream into more, dynamically claimed chunks
+// than CTAs evens out the end of a launch but costs more than it saves here: each
+// extra cut adds a split unit, with its fences and count, and a claim round trip.)
 #ifndef PA_MIN_POSITIONS
 #define PA_MIN_POSITIONS 4
 #endif
@@ -713,18 +719,13 @@ __device__ __forceinline__ long long cta_of(long long x, long long total, long l
 }
 
 template <class Prod>
-__device__ __forceinline__ void walk_balanced(const DecodeParams &p, int bs, int bps, Prod &pr,
-                                              int lane)
+__device__ __forceinline__ bool walk_chunk(const DecodeParams &p, int bs, int bps, Prod &pr,
+                                           int lane, long long total, long long G, long long cta)
 {
-    const long long cta = blockIdx.x;
-    const long long total = stream_total(p, bs, bps, lane);
-    const long long G = balanced_grid(total);
-    if (cta >= G)
-        return;
     const long long s_c = cta * total / G;
     const long long e_c = (cta + 1) * total / G;
     if (s_c >= e_c)
-        return;
+        return true;
     long long base = 0;
     int s = find_seq_at(p, bs, bps, s_c, &base, lane);
     for (; s < p.num_seqs && base < e_c && !*pr.c.abort; ++s) {
@@ -791,11 +792,27 @@ __device__ __forceinline__ void walk_balanced(const DecodeParams &p, int bs, int
                     it.nparts = np;
                 }
             }
+            // consecutive items of a CTA start their warp rotation where the stream is
+            it.packed = (it.packed & ~(3 << 2)) |
+                        ((int)((ns == 0 ? a : max(ra, s_c)) & 3) << 2);
             if (!pr.emit(it))
-                return;
+                return false;
         }
         base += (long long)su.nunits * span;
     }
+    return !*pr.c.abort;
+}
+
+// The producer's walk of the balanced split: CTA c streams positions
+// [c * total / G, (c + 1) * total / G).
+template <class Prod>
+__device__ __forceinline__ void walk_balanced(const DecodeParams &p, int bs, int bps, Prod &pr,
+                                              int lane)
+{
+    const long long total = stream_total(p, bs, bps, lane);
+    const long long G = balanced_grid(total);
+    if ((long long)blockIdx.x < G)
+        walk_chunk(p, bs, bps, pr, lane, total, G, (long long)blockIdx.x);
 }
 
 template <class Prod>
@@ -1126,8 +1143,9 @@ __device__ __forceinline__ bool consume_item_n8(const DecodeParams &p, const Cta
         o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
     float ma = -INFINITY, mb = -INFINITY;  // running max of rows 2 q4 and 2 q4 + 1
     float la = 0.f, lb = 0.f;              // this lane's share of their exp sums
+    const int rot = it.rot();
     for (int j = it.j0; j < it.j1; j += C::kBPS, ++g) {
-        if ((int)(g % kConsumerWarps) != warp)
+        if (((j - it.j0) / C::kBPS + rot) % kConsumerWarps != warp)
             continue;
         const uint32_t st = g % C::kStages;
 #ifdef PA_TRACE
@@ -1404,8 +1422,9 @@ __global__ void __launch_bounds__(kThreads, 2)
         float mrow0 = -INFINITY, mrow1 = -INFINITY, lrow0 = 0.f, lrow1 = 0.f;
         bool alive = true;
 
+        const int rot = it.rot();
         for (int j = it.j0; j < it.j1; j += C::kBPS, ++g) {
-            if ((int)(g % kConsumerWarps) != warp)
+            if (((j - it.j0) / C::kBPS + rot) % kConsumerWarps != warp)
                 continue;
             const uint32_t st = g % C::kStages;
 #ifdef PA_TRACE
@@ -1655,8 +1674,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 acc[r][e] = 0.f;
         }
         bool alive = true;
+        const int rot = it.rot();
         for (int j = it.j0; j < it.j1; ++j, ++g) {
-            if ((int)(g % kConsumerWarps) != warp)
+            if ((j - it.j0 + rot) % kConsumerWarps != warp)
                 continue;
             const uint32_t st = g % C::kStages;
             if (!warp_wait(&c.full[st], (g / C::kStages) & 1u)) {

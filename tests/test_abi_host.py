@@ -113,6 +113,18 @@ def test_balanced_workspace_does_not_depend_on_lengths():
     assert a == b > 0
 
 
+def test_balanced_workspace_formula():
+    # C = 4 CTAs per SM at most: C merge counters, then 2 * C * 16 fp32 rows of d
+    # values and their log2-sum-exp
+    import torch
+    sms = torch.cuda.get_device_properties(0).multi_processor_count if torch.cuda.is_available() else 160
+    C = 4 * sms
+    rows = 2 * C * 16
+    align = lambda n: (n + 255) // 256 * 256
+    for d in (64, 128):
+        assert P.pa_decode_workspace_size(3, 8, 8, d, 16, 7, 0) == align(C * 8) + align(rows * d * 4) + rows * 4
+
+
 # ---------------------------------------------------------------------------
 # allocator: the library's C++ allocator against the oracle's Python allocator
 # ---------------------------------------------------------------------------

@@ -259,7 +259,7 @@ namespace {
 size_t prefix_buffer_bytes(int num_seqs, int num_q_heads, int head_dim)
 {
     const size_t rows = (size_t)num_seqs * num_q_heads;
-    return ((rows * head_dim * 4 + 255) & ~size_t(255)) + ((rows * 4 + 255) & ~size_t(255));
+    return (rows * (size_t)(head_dim + 4) * 4 + 255) & ~size_t(255);
 }
 
 // pa_decode, pa_decode_append and pa_decode_shared: k_new/v_new null for a plain
@@ -314,13 +314,8 @@ pa_status decode_impl(void *out, const void *q, const void *k_cache, const void 
         need += prefix_buffer_bytes(num_seqs, num_q_heads, head_dim);
     if (need > 0 && (!workspace || workspace_bytes < need || !aligned(workspace, 16)))
         return PA_ERR_INVALID;
-    float *pfx_o = nullptr, *pfx_lse = nullptr;
-    if (shared) {
-        const size_t rows = (size_t)num_seqs * num_q_heads;
-        pfx_o = reinterpret_cast<float *>(static_cast<char *>(workspace) + pfx_at);
-        pfx_lse = reinterpret_cast<float *>(static_cast<char *>(workspace) + pfx_at +
-                                            ((rows * head_dim * 4 + 255) & ~size_t(255)));
-    }
+    float *pfx = shared ? reinterpret_cast<float *>(static_cast<char *>(workspace) + pfx_at)
+                        : nullptr;
 
     DecodeLaunch L;
     std::memset(&L, 0, sizeof L);
@@ -382,8 +377,7 @@ pa_status decode_impl(void *out, const void *q, const void *k_cache, const void 
         DecodeLaunch L1 = L;
         L1.p.pass = 1;
         L1.p.share = share;
-        L1.p.pfx_o = pfx_o;
-        L1.p.pfx_lse = pfx_lse;
+        L1.p.pfx = pfx;
         L1.p.k_new = nullptr;
         L1.p.v_new = nullptr;
         cudaError_t e = launch(L1);
@@ -392,8 +386,7 @@ pa_status decode_impl(void *out, const void *q, const void *k_cache, const void 
         // pass 0: each sequence's own blocks (and newest token), merged with pass 1
         L.p.pass = 0;
         L.p.share = share;
-        L.p.pfx_o = pfx_o;
-        L.p.pfx_lse = pfx_lse;
+        L.p.pfx = pfx;
         L.p.epoch = next_epoch();
     }
     cudaError_t e = launch(L);

@@ -112,8 +112,12 @@ __device__ __forceinline__ bool trace_first_tile()
 #endif
 
 struct SmemLayout {
-    uint32_t acc, ml, items, q, newrow, newinfo, bars, flag, total;
+    uint32_t acc, ml, pfx, items, q, newrow, newinfo, bars, flag, total;
 };
+
+// Shared-prefix buffer rows: o (head_dim floats), then the log2-sum-exp, padded to
+// a multiple of 16 bytes.
+constexpr int kPfxPad = 4;
 
 constexpr int kItemSlots = 2;  // work-item descriptors (and their query rows) in flight
 
@@ -129,6 +133,13 @@ __host__ __device__ inline int item_rows_cap(const DecodeParams &p)
     return p.group < kHeadsPerItem ? p.group : kHeadsPerItem;
 }
 
+// Rows of shared-prefix data an item of this launch merges (pass 0 of the
+// shared-prefix decode), else 0.
+__host__ __device__ inline int item_pfx_rows(const DecodeParams &p)
+{
+    return (p.pass == 0 && p.share) ? item_rows_cap(p) : 0;
+}
+
 // Members of a group whose query rows share one shared-prefix item: the rows
 // fill the 8-row (group <= 8) or 16-row item.
 __host__ __device__ inline int members_per_item(int group)
@@ -136,10 +147,11 @@ __host__ __device__ inline int members_per_item(int group)
     return (group <= kNarrowRows ? kNarrowRows : kHeadsPerItem) / group;
 }
 
-// Shared memory: stage ring | merge accumulators | merge (max, sum) | item
+// Shared memory: stage ring | merge accumulators | merge (max, sum) | shared-prefix
+// rows (two item buffers; pass 0 of the shared-prefix decode only) | item
 // descriptors | query rows per item slot | mbarriers | abort flag.
 __host__ __device__ inline SmemLayout make_layout(int stages, int stage_bytes, int rows, int D,
-                                                  int elem_bytes)
+                                                  int elem_bytes, int pfx_rows = 0)
 {
     SmemLayout L;
     uint32_t o = (uint32_t)stages * (uint32_t)stage_bytes;
@@ -148,6 +160,8 @@ __host__ __device__ inline SmemLayout make_layout(int stages, int stage_bytes, i
     L.ml = o;
     o += kConsumerWarps * kHeadsPerItem * 2 * 4;
     o = (o + 127u) & ~127u;
+    L.pfx = o;
+    o += (uint32_t)(2 * pfx_rows * (D + kPfxPad) * 4);
     L.items = o;
     o += kItemSlots * 64u;
     L.q = o;
@@ -291,6 +305,7 @@ struct CtaState {
     uint64_t *full, *empty;            // per ring stage
     uint64_t *item_full, *item_empty;  // per item slot
     uint64_t *csync;                   // consumer-only barrier (all consumer threads arrive)
+    float *pfx;                        // two buffers of shared-prefix rows (item parity)
     volatile int *abort;
     volatile int *merge;               // this CTA completes the current split unit
     volatile uint32_t *sink;           // per consumer warp: see dev::settle_loads
@@ -311,6 +326,7 @@ __device__ __forceinline__ CtaState cta_state(uint8_t *smem, const SmemLayout &l
     c.item_full = c.empty + stages;
     c.item_empty = c.item_full + kItemSlots;
     c.csync = c.item_empty + kItemSlots;
+    c.pfx = reinterpret_cast<float *>(smem + lay.pfx);
     c.abort = reinterpret_cast<volatile int *>(smem + lay.flag);
     c.merge = reinterpret_cast<volatile int *>(smem + lay.flag + 4);
     c.sink = reinterpret_cast<volatile uint32_t *>(smem + lay.flag + 16);
@@ -848,26 +864,45 @@ __device__ __forceinline__ void producer_loop(const DecodeParams &p, const CUten
 // ---------------------------------------------------------------------------
 template <typename T, int D>
 __device__ __forceinline__ void store_result(const DecodeParams &p, const Item &it, int r, int col,
-                                             float o, float lse)
+                                             float o, float lse, const float *pfx_s)
 {
+    constexpr int PS = D + kPfxPad;
     const int rpm = it.rpm();
     const size_t row = (size_t)(it.seq + r / rpm) * p.num_q_heads + it.qrow0 + r % rpm;
     const int f = it.flags();
     if (f & kToPrefix) {
-        p.pfx_o[row * D + col] = o;
+        p.pfx[row * PS + col] = o;
         if (col == 0)
-            p.pfx_lse[row] = lse;
+            p.pfx[row * PS + D] = lse;
         return;
     }
     if (f & kMergePrefix) {
-        const float lp = __ldcg(p.pfx_lse + row);
+        // the item's prefix rows, staged in shared memory when the item started
+        const float lp = pfx_s[r * PS + D];
         const float m2 = fmaxf(lse, lp);
         if (m2 != -INFINITY) {
             const float wa = exp2f(lse - m2), wb = exp2f(lp - m2);
-            o = (wa * o + wb * __ldcg(p.pfx_o + row * D + col)) / (wa + wb);
+            o = (wa * o + wb * pfx_s[r * PS + col]) / (wa + wb);
         }
     }
     reinterpret_cast<T *>(p.out)[row * D + col] = dev::from_float<T>(o);
+}
+
+// Pass 0 of the shared-prefix decode: start copying the item's prefix rows (o and
+// log2-sum-exp, written by pass 1) into buffer `buf` with per-thread asynchronous
+// copies; the consumers wait for them (cp.async.wait_all) before the barrier that
+// precedes the item's final store.  The two buffers alternate by item, so this
+// item's copies never land under a warp still merging the previous item.
+template <int D>
+__device__ __forceinline__ void stage_prefix(const DecodeParams &p, const Item &it, float *buf,
+                                             int tid)
+{
+    constexpr int PS = D + kPfxPad;
+    const float *src = p.pfx + ((size_t)it.seq * p.num_q_heads + it.qrow0) * PS;
+    const int units = it.rows * PS / 4;  // 16-byte units
+    for (int k = tid; k < units; k += 32 * kConsumerWarps)
+        dev::cp_async16(dev::smem_addr(buf + 4 * k), src + 4 * k);
+    dev::cp_async_commit();
 }
 
 // ---------------------------------------------------------------------------
@@ -876,7 +911,7 @@ __device__ __forceinline__ void store_result(const DecodeParams &p, const Item &
 template <typename T, int D>
 __device__ __forceinline__ void finalize_item(const DecodeParams &p, const Item &it,
                                               const float *acc, const float *ml, int rows_cap,
-                                              int tid)
+                                              int tid, const float *pfx_s)
 {
     constexpr int S = D + kAccPad;
     for (int idx = tid; idx < it.rows * D; idx += 32 * kConsumerWarps) {
@@ -906,7 +941,7 @@ __device__ __forceinline__ void finalize_item(const DecodeParams &p, const Item 
         }
         const float o = (L > 0.f) ? O / L : 0.f;
         if (!it.partial) {
-            store_result<T, D>(p, it, r, col, o, (L > 0.f) ? M + log2f(L) : -INFINITY);
+            store_result<T, D>(p, it, r, col, o, (L > 0.f) ? M + log2f(L) : -INFINITY, pfx_s);
         } else {
             const size_t pr = (size_t)it.prow0 + r;
             p.part_o[pr * D + col] = o;
@@ -961,7 +996,7 @@ __device__ __forceinline__ long long split_slot(const Item &it, int i, long long
 // query head; lane i holds partial i's log2-sum-exp.
 template <typename T, int D>
 __device__ __forceinline__ void merge_split_unit(const DecodeParams &p, const Item &it, int warp,
-                                              int lane)
+                                              int lane, const float *pfx_s)
 {
     constexpr int VEC = D / 32;
     const long long total = ((long long)it.total_hi << 32) | (long long)it.total_lo;
@@ -1012,7 +1047,7 @@ __device__ __forceinline__ void merge_split_unit(const DecodeParams &p, const It
         const float lse = M + log2f(W);
 #pragma unroll
         for (int e = 0; e < VEC; ++e)
-            store_result<T, D>(p, it, r, lane * VEC + e, acc[e] / W, lse);
+            store_result<T, D>(p, it, r, lane * VEC + e, acc[e] / W, lse, pfx_s);
     }
 }
 
@@ -1023,7 +1058,7 @@ __device__ __forceinline__ void merge_split_unit(const DecodeParams &p, const It
 // False on a timeout.
 template <typename T, int D>
 __device__ __forceinline__ bool finish_item(const DecodeParams &p, const Item &it, const CtaState &c,
-                                            uint32_t &sph, int warp, int lane)
+                                            uint32_t &sph, int warp, int lane, const float *pfx_s)
 {
     const bool split = p.balanced && it.partial;
     if (!consumer_sync(c, sph))
@@ -1039,7 +1074,7 @@ __device__ __forceinline__ bool finish_item(const DecodeParams &p, const Item &i
     if (!consumer_sync(c, sph))
         return false;
     if (*c.merge)
-        merge_split_unit<T, D>(p, it, warp, lane);
+        merge_split_unit<T, D>(p, it, warp, lane, pfx_s);
     return true;
 }
 
@@ -1332,7 +1367,9 @@ __global__ void __launch_bounds__(kThreads, 2)
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int rows_cap = item_rows_cap(p);
-    const SmemLayout lay = make_layout(C::kStages, C::kStageBytes, rows_cap, D, sizeof(T));
+    const int pfx_rows = item_pfx_rows(p);
+    const SmemLayout lay =
+        make_layout(C::kStages, C::kStageBytes, rows_cap, D, sizeof(T), pfx_rows);
     const CtaState c = cta_state(smem, lay, C::kStages);
     init_cta(c, C::kStages);
 
@@ -1377,6 +1414,10 @@ __global__ void __launch_bounds__(kThreads, 2)
         const Item it = load_item(&c.items[slot]);
         if (it.seq < 0)
             break;
+        const bool merge_pfx = (it.flags() & kMergePrefix) != 0;
+        float *pfx_s = c.pfx + (n & 1) * pfx_rows * (D + kPfxPad);
+        if (merge_pfx)
+            stage_prefix<D>(p, it, pfx_s, threadIdx.x);
         if constexpr (N8) {
             if (!consume_item_n8<T, D, BS>(p, c, it, slot, g, warp, lane, rows_cap))
                 break;
@@ -1587,13 +1628,15 @@ __global__ void __launch_bounds__(kThreads, 2)
 #ifdef PA_TRACE
         const unsigned long long t_m0 = dev::global_timer_ns();
 #endif
+        if (merge_pfx)
+            dev::cp_async_wait_all();
         if (!consumer_sync(c, sph)) {
             if (lane == 0)
                 raise_error(p, c.abort, PA_DEVERR_TIMEOUT_FULL);
             break;
         }
-        finalize_item<T, D>(p, it, c.macc, c.mml, rows_cap, threadIdx.x);
-        if (!finish_item<T, D>(p, it, c, sph, warp, lane)) {
+        finalize_item<T, D>(p, it, c.macc, c.mml, rows_cap, threadIdx.x, pfx_s);
+        if (!finish_item<T, D>(p, it, c, sph, warp, lane, pfx_s)) {
             if (lane == 0)
                 raise_error(p, c.abort, PA_DEVERR_TIMEOUT_FULL);
             break;
@@ -1635,7 +1678,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int rows_cap = item_rows_cap(p);
-    const SmemLayout lay = make_layout(C::kStages, C::kStageBytes, rows_cap, D, sizeof(float));
+    const int pfx_rows = item_pfx_rows(p);
+    const SmemLayout lay =
+        make_layout(C::kStages, C::kStageBytes, rows_cap, D, sizeof(float), pfx_rows);
     const CtaState c = cta_state(smem, lay, C::kStages);
     init_cta(c, C::kStages);
 
@@ -1661,6 +1706,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const Item it = load_item(&c.items[slot]);
         if (it.seq < 0)
             break;
+        const bool merge_pfx = (it.flags() & kMergePrefix) != 0;
+        float *pfx_s = c.pfx + (n & 1) * pfx_rows * (D + kPfxPad);
+        if (merge_pfx)
+            stage_prefix<D>(p, it, pfx_s, threadIdx.x);
         const float *qs = reinterpret_cast<const float *>(c.qslots) + slot * H * D;
 
         float acc[H][VEC];
@@ -1802,13 +1851,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
         }
+        if (merge_pfx)
+            dev::cp_async_wait_all();
         if (!consumer_sync(c, sph)) {
             if (lane == 0)
                 raise_error(p, c.abort, PA_DEVERR_TIMEOUT_FULL);
             break;
         }
-        finalize_item<float, D>(p, it, c.macc, c.mml, rows_cap, threadIdx.x);
-        if (!finish_item<float, D>(p, it, c, sph, warp, lane)) {
+        finalize_item<float, D>(p, it, c.macc, c.mml, rows_cap, threadIdx.x, pfx_s);
+        if (!finish_item<float, D>(p, it, c, sph, warp, lane, pfx_s)) {
             if (lane == 0)
                 raise_error(p, c.abort, PA_DEVERR_TIMEOUT_FULL);
             break;
@@ -1901,11 +1952,11 @@ struct KernelOf<float, D, BS> {
 };
 
 template <typename T, int D, int BS>
-inline size_t smem_bytes_for(int rows)
+inline size_t smem_bytes_for(int rows, int pfx_rows = 0)
 {
     using C = Cfg<T, D, BS>;
     rows = rows < kHeadsPerItem ? rows : kHeadsPerItem;
-    return make_layout(C::kStages, C::kStageBytes, rows, D, sizeof(T)).total;
+    return make_layout(C::kStages, C::kStageBytes, rows, D, sizeof(T), pfx_rows).total;
 }
 
 int cached_occupancy(void *kernel, int device, size_t smem, size_t max_smem);
@@ -1915,8 +1966,8 @@ cudaError_t launch_decode_impl(const DecodeLaunch &L, cudaStream_t stream)
 {
     const DecodeParams &p = L.p;
     void *kern = KernelOf<T, D, BS>::get(p.group <= kNarrowRows);
-    const size_t smem = smem_bytes_for<T, D, BS>(item_rows_cap(p));
-    const size_t smem_max = smem_bytes_for<T, D, BS>(kHeadsPerItem);
+    const size_t smem = smem_bytes_for<T, D, BS>(item_rows_cap(p), item_pfx_rows(p));
+    const size_t smem_max = smem_bytes_for<T, D, BS>(kHeadsPerItem, kHeadsPerItem);
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess)

@@ -150,6 +150,15 @@ __device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t &r0, uint3
                  : "r"(addr));
 }
 
+// 16-byte asynchronous copy global -> shared (per thread), its group commit, and
+// the wait for all of this thread's outstanding groups.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
 // Transpose of an 8x8 matrix of 16-bit elements held one row per four lanes
 // (lane l: row l / 4, columns 2 (l % 4) and 2 (l % 4) + 1) into the same layout.
 __device__ __forceinline__ uint32_t movmatrix_trans(uint32_t a)

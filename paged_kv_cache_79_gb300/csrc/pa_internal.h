@@ -52,12 +52,11 @@ struct DecodeParams {
     void *v_cache;
     // Shared-prefix decode (null share: off).  share[s] = {first member of s's
     // group, shared leading blocks}; pass 1 streams each group's shared blocks once
-    // for all members and writes fp32 rows + log2-sum-exp to pfx_o / pfx_lse
+    // for all members and writes fp32 rows + log2-sum-exp to pfx
     // ([S][Hq][D], [S][Hq]); pass 0 then covers each sequence's own blocks and merges.
     const int32_t *share;
     int pass;
-    float *pfx_o;
-    float *pfx_lse;
+    float *pfx;  // rows of head_dim + 4 floats: the row's o, then its log2-sum-exp
 };
 
 // Balanced split: partial slots are reserved for at most this many CTAs per SM.

@@ -264,7 +264,9 @@ def run_ours(args):
     # partitions: plus the merge kernel when a table spans several partitions
     merge = parts > 0 and -(-bt.shape[1] // (parts // w.block_size)) > 1
     fused = ds.fusable
-    shared = ds.share is not None and not args.no_share
+    # the shared-prefix decode where the groups save enough reads to pay for its
+    # second launch (parallel sampling: ~69%; multi-turn groups here: ~3%)
+    shared = ds.share is not None and ds.share_pays and not args.no_share
     if shared:
         merge = False
         parts = 0
@@ -273,18 +275,20 @@ def run_ours(args):
 
     with torch.cuda.stream(stream):
         step = ds.run_shared if shared else (ds.run_fused if fused else ds.run)
-        for _ in range(args.warmup):
-            step(stream)
-        torch.cuda.synchronize(device)
-        if world > 1:
-            dist.barrier()
         ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
                torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+        # the sampler starts first: warm-up runs right before the timed steps, so the
+        # GPU does not idle (and drop its clocks) between them
         clocks = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
         if clocks:
             clocks.start()
             time.sleep(0.3)
+        for _ in range(args.warmup):
+            flush()
+            step(stream)
         torch.cuda.synchronize(device)
+        if world > 1:
+            dist.barrier()
         t_wall = time.perf_counter()
         for i in range(args.steps):
             flush()                                         # evict the previous step from L2
@@ -350,7 +354,8 @@ def run_ours(args):
                    "append": "fused into the decode launch" if fused else "separate launch",
                    "prefix_sharing": (f"{int((ds.share[:, 0] >= 0).sum())} sequences in groups that "
                                       "read their shared leading blocks once (two-pass decode)"
-                                      if shared else "none"),
+                                      if shared else "not used (groups save too few reads)"
+                                      if ds.share is not None and not args.no_share else "none"),
                    "appended_tokens": n_tok,
                    "cow_pairs": n_pairs,
                    "l2": "flushed before every timed step (512 MB write, then 1 GB read)",

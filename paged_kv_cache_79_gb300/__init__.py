@@ -208,6 +208,25 @@ def share_groups(block_tables, context_lens, block_size: int, min_shared_blocks:
     return share
 
 
+def share_saving(share, context_lens, block_size: int) -> float:
+    """Fraction of the batch's block reads that pa_decode_shared saves over pa_decode:
+    each group of m members sharing P blocks reads (m - 1) * P blocks fewer.  The
+    second launch and the merge cost a few percent, so sharing pays from roughly
+    10% saved (SHARE_MIN_SAVING)."""
+    import numpy as np
+    share = np.asarray(share)
+    cl = np.asarray(context_lens).astype(np.int64)
+    logical = int(((cl + block_size - 1) // block_size).sum())
+    saved = 0
+    for s in range(share.shape[0]):
+        if share[s, 0] >= 0 and share[s, 0] != s:      # every member but the first
+            saved += int(share[s, 1])
+    return saved / logical if logical else 0.0
+
+
+SHARE_MIN_SAVING = 0.10
+
+
 def pa_decode_noalloc(out, q, k_cache, v_cache, block_tables, context_lens, scale: float,
                       num_q_heads: int, num_kv_heads: int, head_dim: int, block_size: int,
                       partition_size: int = 0, stream=None):
@@ -460,7 +479,7 @@ def pa_kv_transfer_worthwhile(reusable_tokens: int, threshold_tokens: int = 64) 
 
 
 __all__ = ["pa_decode", "pa_decode_append", "pa_decode_shared", "pa_decode_shared_workspace_size",
-           "share_groups", "pa_decode_noalloc", "pa_decode_workspace_size", "pa_decode_partition_size", "alloc_workspace",
+           "share_groups", "share_saving", "SHARE_MIN_SAVING", "pa_decode_noalloc", "pa_decode_workspace_size", "pa_decode_partition_size", "alloc_workspace",
            "pa_reshape_and_cache", "pa_copy_blocks", "pa_swap_blocks", "pa_gather_blocks",
            "pa_scatter_blocks", "pa_kv_transfer_worthwhile", "pa_device_errors", "pa_status_string",
            "BlockAllocator", "PagedKVError", "OutOfBlocks", "library_path"]

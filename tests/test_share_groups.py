@@ -128,3 +128,11 @@ def test_multiturn_groups():
             assert got.tolist() == [[4 * g, want]] * 4
         else:
             assert got.tolist() == [[-1, 0]] * 4
+
+
+def test_share_saving_counts_every_member_but_the_first():
+    # two groups: 3 members x 4 shared blocks, 2 members x 1 block; one loner
+    share = np.array([[0, 4], [0, 4], [0, 4], [3, 1], [3, 1], [-1, 0]], dtype=np.int32)
+    cl = np.array([80, 70, 65, 20, 30, 16], dtype=np.int32)     # B = 16: 5+5+5+2+2+1 blocks
+    assert P.share_saving(share, cl, 16) == pytest.approx((2 * 4 + 1 * 1) / 20)
+    assert P.share_saving(np.full((2, 2), -1, np.int32), np.array([5, 9]), 16) == 0.0

@@ -46,6 +46,7 @@ def test_tiny_fifty_appends_each_decoded():
                                                      w.free_order)[0].block_table(0)
     oalloc = oracle.BlockAllocator(w.num_blocks, w.block_size, w.free_order)
     oalloc.new_seq()
+    worst = 0.0
     for i, (out, q, table, T) in enumerate(outs):
         slot, _ = oalloc.append(0)
         k, v = W.step_tensors(w, W.Step((0,), i), DEV)
@@ -53,7 +54,9 @@ def test_tiny_fifty_appends_each_decoded():
         assert table == oalloc.block_table(0) and T == i + 1
         bt = np.array([table], dtype=np.int32)
         want = oracle.decode(q, kh, vh, bt, np.array([T], np.int32), w.softmax_scale, "f32", 8, 8, 64, 16)
-        assert_close(out, want, "f32", f"step {i}")
+        err, rel = assert_close(out, want, "f32", f"step {i}")
+        worst = max(worst, err)
+    print(f"\n[parity] tiny: max abs err over 50 decodes {worst:.3e}")
     assert np.array_equal(raw(kc), kh) and np.array_equal(raw(vc), vh)
 
 
@@ -86,7 +89,9 @@ def _check_workload(w, sample=None, min_seqs=0, shared=False):
     q = raw(ds.q)
     want = oracle.decode(q[seqs], kh, vh, obt[seqs], ocl[seqs], w.softmax_scale, w.dtype, w.num_q_heads,
                          w.num_kv_heads, w.head_dim, w.block_size)
-    assert_close(out[seqs], want, w.dtype, w.name)
+    err, rel = assert_close(out[seqs], want, w.dtype, w.name)
+    print(f"\n[parity] {w.name}{' shared' if shared else ''}: {len(seqs)} sequences, "
+          f"max abs err {err:.3e}, normwise rel {rel:.3e}")
     assert P.pa_device_errors() == 0
     return out, ds
 
@@ -136,7 +141,8 @@ def test_long_multiturn_bf16():
         n = (ocl[s] + w.block_size - 1) // w.block_size
         sbt[i, :n] = [remap[int(b)] for b in obt[s, :n]]
     want = oracle.decode(raw(ds.q)[seqs], ks, vs, sbt, ocl[seqs], w.softmax_scale, "bf16", 32, 8, 128, 32)
-    assert_close(out[seqs], want, "bf16", w.name)
+    err, rel = assert_close(out[seqs], want, "bf16", w.name)
+    print(f"\n[parity] {w.name}: {len(seqs)} sampled sequences, max abs err {err:.3e}, normwise rel {rel:.3e}")
     # the turns of a group share their leading blocks: the two-pass decode agrees too
     assert ds.share is not None
     out_s = ds.decode_shared().clone()

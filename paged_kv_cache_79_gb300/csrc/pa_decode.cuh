@@ -953,10 +953,10 @@ __device__ __forceinline__ void finalize_item(const DecodeParams &p, const Item 
 
 // ---------------------------------------------------------------------------
 // Balanced split: merge of a unit whose stages several CTAs shared.  Each CTA
-// writes its partial (fp32 output rows + log2-sum-exp), makes it visible
-// (__threadfence) and counts it on the unit's counter; the CTA whose count
-// completes the set merges every partial with the log-sum-exp rule.  No CTA waits
-// for another.  Counters hold (epoch << 32 | count): a value left by an earlier call
+// writes its partial (fp32 output rows + log2-sum-exp), releases it with a GPU-scope
+// fence and counts it on the unit's counter; the CTA whose count completes the set
+// takes an acquire fence and merges every partial with the log-sum-exp rule.  No CTA waits for
+// another.  Counters hold (epoch << 32 | count): a value left by an earlier call
 // carries another epoch and counts as zero, so they never need clearing.
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ bool count_partial(const DecodeParams &p, const Item &it)
@@ -1002,6 +1002,27 @@ __device__ __forceinline__ void merge_split_unit(const DecodeParams &p, const It
     const long long total = ((long long)it.total_hi << 32) | (long long)it.total_lo;
     const long long G = balanced_grid(total);
     for (int r = warp; r < it.rows; r += kConsumerWarps) {
+        if (it.nparts == 2) {
+            // the usual case (a unit cut once): both parts' loads in flight at once
+            const int r0 = (int)split_slot(it, 0, total, G) * kHeadsPerItem + r;
+            const int r1 = (int)split_slot(it, 1, total, G) * kHeadsPerItem + r;
+            const float l0 = __ldcg(p.part_lse + r0), l1 = __ldcg(p.part_lse + r1);
+            float v0[VEC], v1[VEC];
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) {
+                v0[e] = __ldcg(p.part_o + (size_t)r0 * D + lane * VEC + e);
+                v1[e] = __ldcg(p.part_o + (size_t)r1 * D + lane * VEC + e);
+            }
+            const float M = fmaxf(l0, l1);
+            const float w0 = exp2f(l0 - M), w1 = exp2f(l1 - M);
+            const float W = w0 + w1;
+            const float lse = M + log2f(W);
+#pragma unroll
+            for (int e = 0; e < VEC; ++e)
+                store_result<T, D>(p, it, r, lane * VEC + e, (w0 * v0[e] + w1 * v1[e]) / W, lse,
+                                   pfx_s);
+            continue;
+        }
         float M = -INFINITY;
         for (int i0 = 0; i0 < it.nparts; i0 += 32) {
             const int i = i0 + lane;
@@ -1053,8 +1074,9 @@ __device__ __forceinline__ void merge_split_unit(const DecodeParams &p, const It
 
 // End of an item for the consumer warps: shared-memory reuse barrier and, for a
 // split unit of the balanced schedule, the count-and-merge step.  The barrier
-// orders every consumer thread's partial stores before thread 0's GPU-scope fence
-// and count (fences are cumulative); the merging CTA fences again before reading.
+// orders every consumer thread's partial stores before thread 0's release fence and
+// count (fences are cumulative over what thread 0 has observed); the merging CTA's
+// acquire fence, then the next barrier, let all its threads see the other partials.
 // False on a timeout.
 template <typename T, int D>
 __device__ __forceinline__ bool finish_item(const DecodeParams &p, const Item &it, const CtaState &c,
@@ -1066,9 +1088,14 @@ __device__ __forceinline__ bool finish_item(const DecodeParams &p, const Item &i
     if (!split)
         return true;
     if (threadIdx.x == 0) {
+        // release: this CTA's partial rows (observed through the barrier above)
+        // become visible before the count; acquire, only in the CTA that completes
+        // the set: it then sees every other partial and passes that on through the
+        // next barrier
         dev::fence_acq_rel_gpu();
         const bool last = count_partial(p, it);
-        dev::fence_acq_rel_gpu();
+        if (last)
+            dev::fence_acq_rel_gpu();
         *c.merge = last ? 1 : 0;
     }
     if (!consumer_sync(c, sph))

@@ -175,7 +175,8 @@ pa_status pa_decode_shared(void *out, const void *q, void *k_cache, void *v_cach
                            int num_q_heads, int num_kv_heads, int head_dim, int block_size,
                            pa_dtype dtype, void *workspace, size_t workspace_bytes, void *stream);
 
-/* Workspace bytes of pa_decode_shared: pa_decode_workspace_size(..., 0) plus fp32
+/* Workspace bytes of pa_decode_shared: twice pa_decode_workspace_size(..., 0) (the
+ * two launches may overlap, each has its own counters and partial rows) plus fp32
  * shared-prefix rows [S][Hq][d + 4] (the row's o, then its log2-sum-exp, then
  * padding; 256-byte aligned end).  (size_t)-1 for invalid arguments. */
 size_t pa_decode_shared_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads,

@@ -309,13 +309,18 @@ pa_status decode_impl(void *out, const void *q, const void *k_cache, const void 
     if (need == (size_t)-1)
         return PA_ERR_INVALID;
     const bool shared = share != nullptr && balanced && num_q_heads / num_kv_heads <= kHeadsPerItem;
+    // the shared-prefix passes may run at the same time (pass 0 overlaps the end of
+    // pass 1), so each has its own merge counters and partial slots
+    const size_t pass1_at = need;
+    if (shared)
+        need += need;
     const size_t pfx_at = need;
     if (shared)
         need += prefix_buffer_bytes(num_seqs, num_q_heads, head_dim);
     if (need > 0 && (!workspace || workspace_bytes < need || !aligned(workspace, 16)))
         return PA_ERR_INVALID;
-    float *pfx = shared ? reinterpret_cast<float *>(static_cast<char *>(workspace) + pfx_at)
-                        : nullptr;
+    char *const ws_base = static_cast<char *>(workspace);
+    float *pfx = shared ? reinterpret_cast<float *>(ws_base + pfx_at) : nullptr;
 
     DecodeLaunch L;
     std::memset(&L, 0, sizeof L);
@@ -375,6 +380,12 @@ pa_status decode_impl(void *out, const void *q, const void *k_cache, const void 
     if (shared) {
         // pass 1: every group's shared blocks once, all members' rows at a time
         DecodeLaunch L1 = L;
+        char *w1 = ws_base + pass1_at;
+        L1.p.counters = reinterpret_cast<unsigned long long *>(w1);
+        L1.p.part_o = reinterpret_cast<float *>(w1 + counter_bytes(sms));
+        L1.p.part_lse = reinterpret_cast<float *>(
+            w1 + counter_bytes(sms) +
+            ((balanced_rows(sms) * (size_t)head_dim * 4 + 255) & ~size_t(255)));
         L1.p.pass = 1;
         L1.p.share = share;
         L1.p.pfx = pfx;
@@ -432,7 +443,7 @@ size_t pa_decode_shared_workspace_size(int num_seqs, int num_q_heads, int num_kv
                                                  block_size, max_blocks_per_seq, 0);
     if (base == (size_t)-1)
         return base;
-    return base + prefix_buffer_bytes(num_seqs, num_q_heads, head_dim);
+    return 2 * base + prefix_buffer_bytes(num_seqs, num_q_heads, head_dim);
 }
 
 pa_status pa_decode_shared(void *out, const void *q, void *k_cache, void *v_cache,

@@ -333,7 +333,12 @@ __device__ __forceinline__ CtaState cta_state(uint8_t *smem, const SmemLayout &l
     return c;
 }
 
-__device__ __forceinline__ void init_cta(const CtaState &c, int stages)
+__device__ __forceinline__ bool defers_dependency(const DecodeParams &p)
+{
+    return p.pass == 0 && p.share != nullptr;
+}
+
+__device__ __forceinline__ void init_cta(const DecodeParams &p, const CtaState &c, int stages)
 {
     if (threadIdx.x == 0) {
         for (int s = 0; s < stages; ++s) {
@@ -349,8 +354,14 @@ __device__ __forceinline__ void init_cta(const CtaState &c, int stages)
         dev::fence_mbar_init();
     }
     __syncthreads();
-    // Everything read below may be produced by the previous kernel in the stream.
-    dev::grid_dependency_wait();
+    // Everything read below may be produced by the previous kernel in the stream,
+    // except in pass 0 of the shared-prefix decode: the previous kernel is pass 1,
+    // which writes only the prefix rows (and its own counters and partial slots),
+    // so pass 0 streams its blocks while pass 1 finishes and waits only before it
+    // first reads a prefix row (its own predecessors had completed before pass 1
+    // passed this point).
+    if (!defers_dependency(p))
+        dev::grid_dependency_wait();
     dev::grid_launch_dependents();
 }
 
@@ -1398,7 +1409,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     const SmemLayout lay =
         make_layout(C::kStages, C::kStageBytes, rows_cap, D, sizeof(T), pfx_rows);
     const CtaState c = cta_state(smem, lay, C::kStages);
-    init_cta(c, C::kStages);
+    init_cta(p, c, C::kStages);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -1424,6 +1435,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
     bool first_tile = true;
 #endif
+    bool pfx_ready = !defers_dependency(p);  // prefix rows may be read
     for (uint32_t n = 0;; ++n) {
         const uint32_t slot = n % kItemSlots;
 #ifdef PA_TRACE
@@ -1443,7 +1455,7 @@ __global__ void __launch_bounds__(kThreads, 2)
             break;
         const bool merge_pfx = (it.flags() & kMergePrefix) != 0;
         float *pfx_s = c.pfx + (n & 1) * pfx_rows * (D + kPfxPad);
-        if (merge_pfx)
+        if (merge_pfx && pfx_ready)
             stage_prefix<D>(p, it, pfx_s, threadIdx.x);
         if constexpr (N8) {
             if (!consume_item_n8<T, D, BS>(p, c, it, slot, g, warp, lane, rows_cap))
@@ -1655,8 +1667,14 @@ __global__ void __launch_bounds__(kThreads, 2)
 #ifdef PA_TRACE
         const unsigned long long t_m0 = dev::global_timer_ns();
 #endif
-        if (merge_pfx)
+        if (merge_pfx) {
+            if (!pfx_ready) {  // first prefix row of this CTA: wait for pass 1 once
+                dev::grid_dependency_wait();
+                pfx_ready = true;
+                stage_prefix<D>(p, it, pfx_s, threadIdx.x);
+            }
             dev::cp_async_wait_all();
+        }
         if (!consumer_sync(c, sph)) {
             if (lane == 0)
                 raise_error(p, c.abort, PA_DEVERR_TIMEOUT_FULL);
@@ -1709,7 +1727,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const SmemLayout lay =
         make_layout(C::kStages, C::kStageBytes, rows_cap, D, sizeof(float), pfx_rows);
     const CtaState c = cta_state(smem, lay, C::kStages);
-    init_cta(c, C::kStages);
+    init_cta(p, c, C::kStages);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -1723,6 +1741,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int part = lane / BS;
     uint32_t g = 0;
     uint32_t sph = 0;
+    bool pfx_ready = !defers_dependency(p);  // prefix rows may be read
     for (uint32_t n = 0;; ++n) {
         const uint32_t slot = n % kItemSlots;
         if (!warp_wait(&c.item_full[slot], (n / kItemSlots) & 1u)) {
@@ -1735,7 +1754,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
         const bool merge_pfx = (it.flags() & kMergePrefix) != 0;
         float *pfx_s = c.pfx + (n & 1) * pfx_rows * (D + kPfxPad);
-        if (merge_pfx)
+        if (merge_pfx && pfx_ready)
             stage_prefix<D>(p, it, pfx_s, threadIdx.x);
         const float *qs = reinterpret_cast<const float *>(c.qslots) + slot * H * D;
 
@@ -1878,8 +1897,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
         }
-        if (merge_pfx)
+        if (merge_pfx) {
+            if (!pfx_ready) {  // first prefix row of this CTA: wait for pass 1 once
+                dev::grid_dependency_wait();
+                pfx_ready = true;
+                stage_prefix<D>(p, it, pfx_s, threadIdx.x);
+            }
             dev::cp_async_wait_all();
+        }
         if (!consumer_sync(c, sph)) {
             if (lane == 0)
                 raise_error(p, c.abort, PA_DEVERR_TIMEOUT_FULL);

@@ -98,6 +98,38 @@ class DecodeStep:
                          stream)
 
 
+class PackedInputs:
+    """The inputs of a step packed at 256-byte aligned offsets into one pinned host
+    buffer and one device buffer, so that they cross the bus in a single copy
+    (each separate copy has a fixed cost of its own).  `views` are device tensors
+    aliasing the device buffer; `host` tensors alias the host buffer."""
+
+    def __init__(self, tensors, device):
+        import torch
+        offs, total = {}, 0
+        for name, t in tensors.items():
+            n = t.numel() * t.element_size()
+            offs[name] = (total, n)
+            total += (n + 255) // 256 * 256
+        total = max(total, 256)
+        self.host_buf = torch.empty(total, dtype=torch.uint8).pin_memory()
+        self.dev_buf = torch.empty(total, dtype=torch.uint8, device=device)
+        self.views, self.host = {}, {}
+        for name, t in tensors.items():
+            o, n = offs[name]
+            self.host[name] = self.host_buf[o:o + n].view(t.dtype).view(t.shape)
+            self.views[name] = self.dev_buf[o:o + n].view(t.dtype).view(t.shape)
+            self.host[name].copy_(t)
+
+    def upload(self, stream=None):
+        """One host-to-device copy of every input (on the current stream)."""
+        self.dev_buf.copy_(self.host_buf, non_blocking=True)
+
+    @property
+    def nbytes(self) -> int:
+        return sum(t.numel() * t.element_size() for t in self.host.values())
+
+
 def execute(w, k_cache, v_cache, step_kv: Callable, query: Callable,
             on_step: Optional[Callable] = None, stream=None, width: Optional[int] = None):
     """Run workload `w`'s script on the device caches.

@@ -208,3 +208,25 @@ def test_shared_step_equals_separate_step():
                          w.num_kv_heads, w.head_dim, w.block_size)
     assert_close(ds.out, want, w.dtype, "shared step")
     assert P.pa_device_errors() == 0
+
+
+def test_packed_inputs_step_equals_the_plain_step():
+    """The step run on inputs uploaded in one packed copy gives the same caches and
+    output, bit for bit, as the step on the original device tensors."""
+    import dataclasses
+    w = W.mha_fp16()
+    kc, vc = _gpu_tensors(w)
+    alloc, ds = runner.execute(w, kc, vc, _step_kv(w), _query(w))
+    k0, v0 = kc.clone(), vc.clone()
+    ds.run_fused()
+    torch.cuda.synchronize()
+    out1, k1, v1 = ds.out.clone(), kc.clone(), vc.clone()
+    kc.copy_(k0)
+    vc.copy_(v0)
+    names = ["q", "step_k", "step_v", "slots", "pairs", "block_tables", "context_lens"]
+    packed = runner.PackedInputs({n: getattr(ds, n).cpu() for n in names}, DEV)
+    packed.upload()
+    dsv = dataclasses.replace(ds, out=torch.empty_like(ds.out), **packed.views)
+    dsv.run_fused()
+    torch.cuda.synchronize()
+    assert torch.equal(kc, k1) and torch.equal(vc, v1) and torch.equal(dsv.out, out1)

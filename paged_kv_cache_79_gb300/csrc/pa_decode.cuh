@@ -240,7 +240,7 @@ struct Item {
     int c_first, nparts;
     unsigned int total_lo, total_hi;  // stream length (to tell empty CTA ranges)
     int tseq;               // sequence whose block-table row gives the blocks
-    int packed;             // members << 16 | rows per member << 8 | rot << 2 | flags
+    int packed;             // members << 16 | rows per member << 8 | divisor << 4 | rot << 2 | flags
     __device__ int members() const { return packed >> 16; }
     __device__ int rpm() const { return (packed >> 8) & 0xff; }
     __device__ int flags() const { return packed & 3; }  // kToPrefix / kMergePrefix
@@ -248,6 +248,8 @@ struct Item {
     // the item alone (not of the CTA that runs it), so the warps' partial sums, and
     // with them the rounding of the result, do not depend on the schedule.
     __device__ int rot() const { return (packed >> 2) & 3; }
+    // balanced split: positions per CTA the stream was cut by (see balanced_divisor)
+    __device__ int divisor() const { return (packed >> 4) & 0xf; }
 };
 static_assert(sizeof(Item) == 64, "one 64-byte descriptor slot");
 
@@ -681,14 +683,20 @@ __device__ __forceinline__ long long seq_weight(const DecodeParams &p, int s, in
 }
 
 // Positions of the whole stream (every lane gets the value).
-__device__ __forceinline__ long long stream_total(const DecodeParams &p, int bs, int bps, int lane)
+__device__ __forceinline__ long long stream_total(const DecodeParams &p, int bs, int bps, int lane,
+                                                  long long *units = nullptr)
 {
-    long long t = 0;
+    long long t = 0, n = 0;
     for (int s0 = 0; s0 < p.num_seqs; s0 += 32) {
         const int s = s0 + lane;
-        if (s < p.num_seqs)
-            t += seq_weight(p, s, bs, bps);
+        if (s < p.num_seqs) {
+            const SeqUnits u = seq_units(p, s, bs, bps);
+            t += (long long)u.nunits * (kUnitCost + u.ns);
+            n += u.nunits;
+        }
     }
+    if (units)
+        *units = warp_sum_ll(n);
     return warp_sum_ll(t);
 }
 
@@ -733,9 +741,17 @@ __device__ __forceinline__ int find_seq_at(const DecodeParams &p, int bs, int bp
 #define PA_MIN_POSITIONS 4
 #endif
 constexpr long long kMinPositions = PA_MIN_POSITIONS;
-__device__ __forceinline__ long long balanced_grid(long long total)
+// Positions per CTA at least: kMinPositions, or, for a batch of short units (8
+// positions or fewer on average), the average unit, so that a few short units give
+// each CTA about one whole unit instead of cutting every unit in two.
+__device__ __forceinline__ int balanced_divisor(long long total, long long units)
 {
-    const long long g = (total + kMinPositions - 1) / kMinPositions;
+    const long long avg = units > 0 ? (total + units - 1) / units : 1;
+    return (int)(avg <= 8 && avg > kMinPositions ? avg : kMinPositions);
+}
+__device__ __forceinline__ long long balanced_grid(long long total, int divisor)
+{
+    const long long g = (total + divisor - 1) / divisor;
     return g < 1 ? 1 : (g < (long long)gridDim.x ? g : (long long)gridDim.x);
 }
 
@@ -747,7 +763,8 @@ __device__ __forceinline__ long long cta_of(long long x, long long total, long l
 
 template <class Prod>
 __device__ __forceinline__ bool walk_chunk(const DecodeParams &p, int bs, int bps, Prod &pr,
-                                           int lane, long long total, long long G, long long cta)
+                                           int lane, long long total, long long G, long long cta,
+                                           int div)
 {
     const long long s_c = cta * total / G;
     const long long e_c = (cta + 1) * total / G;
@@ -820,8 +837,8 @@ __device__ __forceinline__ bool walk_chunk(const DecodeParams &p, int bs, int bp
                 }
             }
             // consecutive items of a CTA start their warp rotation where the stream is
-            it.packed = (it.packed & ~(3 << 2)) |
-                        ((int)((ns == 0 ? a : max(ra, s_c)) & 3) << 2);
+            it.packed = (it.packed & ~(0x3f << 2)) |
+                        ((int)((ns == 0 ? a : max(ra, s_c)) & 3) << 2) | (div << 4);
             if (!pr.emit(it))
                 return false;
         }
@@ -836,10 +853,12 @@ template <class Prod>
 __device__ __forceinline__ void walk_balanced(const DecodeParams &p, int bs, int bps, Prod &pr,
                                               int lane)
 {
-    const long long total = stream_total(p, bs, bps, lane);
-    const long long G = balanced_grid(total);
+    long long units = 0;
+    const long long total = stream_total(p, bs, bps, lane, &units);
+    const int div = balanced_divisor(total, units);
+    const long long G = balanced_grid(total, div);
     if ((long long)blockIdx.x < G)
-        walk_chunk(p, bs, bps, pr, lane, total, G, (long long)blockIdx.x);
+        walk_chunk(p, bs, bps, pr, lane, total, G, (long long)blockIdx.x, div);
 }
 
 template <class Prod>
@@ -1011,7 +1030,7 @@ __device__ __forceinline__ void merge_split_unit(const DecodeParams &p, const It
 {
     constexpr int VEC = D / 32;
     const long long total = ((long long)it.total_hi << 32) | (long long)it.total_lo;
-    const long long G = balanced_grid(total);
+    const long long G = balanced_grid(total, it.divisor());
     for (int r = warp; r < it.rows; r += kConsumerWarps) {
         if (it.nparts == 2) {
             // the usual case (a unit cut once): both parts' loads in flight at once

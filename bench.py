@@ -235,6 +235,24 @@ class L2Flush:
         self.sink.copy_(self.r.sum().view(1))
 
 
+def max_over_ranks(values, device="cpu"):
+    """Each value's maximum over the ranks: the job takes as long as its slowest rank
+    (identity outside torch.distributed or at world size 1)."""
+    import torch
+    import torch.distributed as dist
+    values = [float(v) for v in values]
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return values
+    t = torch.tensor(values, dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def job_gbs(bytes_per_rank, ms, world):
+    """Whole-job GB/s: every rank moves bytes_per_rank in the slowest rank's time."""
+    return world * bytes_per_rank / (ms * 1e-3) / 1e9
+
+
 def run_ours(args):
     import numpy as np
     import torch
@@ -319,17 +337,14 @@ def run_ours(args):
     dec_ms = [b.elapsed_time(c) for a, b, c in ev]
     t_step = sum(step_ms) / len(step_ms)
     t_dec = sum(dec_ms) / len(dec_ms)
-    if world > 1:
-        t = torch.tensor([t_step, t_dec], dtype=torch.float64, device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        t_step, t_dec = t.tolist()
+    t_step, t_dec = max_over_ranks([t_step, t_dec], device)
 
     # end to end through the public API with host buffers
-    e2e = run_e2e(ds, stream, device, args, by, shared)
+    e2e = run_e2e(ds, stream, device, args, by, shared, world)
 
     if rank != 0:
         return None
-    value = world * by["step"] / (t_step * 1e-3) / 1e9
+    value = job_gbs(by["step"], t_step, world)
     peak, peak_kind = measured_peak()
     dec_bytes = by["decode"] + (by["append"] if fused else 0)
     achieved = dec_bytes / (t_dec * 1e-3) / 1e9
@@ -386,7 +401,7 @@ def run_ours(args):
     return line
 
 
-def run_e2e(ds, stream, device, args, by, shared=False):
+def run_e2e(ds, stream, device, args, by, shared=False, world=1):
     """Same step through the public API with inputs in pinned host memory: H2D of
     the step's inputs (packed into one buffer, one copy), the step, D2H of the
     output -- all inside the timed region."""
@@ -419,8 +434,8 @@ def run_e2e(ds, stream, device, args, by, shared=False):
             b.synchronize()
             if i >= args.warmup:
                 times.append(a.elapsed_time(b))
-    t = sum(times) / len(times)
-    return {"value": round(by["step"] / (t * 1e-3) / 1e9, 2), "unit": "GB/s", "ms_per_step": round(t, 5),
+    t = max_over_ranks([sum(times) / len(times)], device)[0]
+    return {"value": round(job_gbs(by["step"], t, world), 2), "unit": "GB/s", "ms_per_step": round(t, 5),
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
             "note": "step inputs packed into one pinned buffer: one H2D copy, then the step, then one D2H copy"}
 

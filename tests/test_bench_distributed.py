@@ -1,0 +1,54 @@
+"""The multi-process (N > 1) bookkeeping of bench.py on CPU: gloo, world size 2.
+
+Each rank decodes its own batch, so the only cross-rank step is the time: the job
+takes as long as its slowest rank, and the whole-job value adds every rank's
+bytes.  The reference arm runs on rank 0 alone."""
+import argparse
+import os
+import socket
+
+import pytest
+import torch.multiprocessing as mp
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, world, port, q):
+    import torch.distributed as dist
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    import bench
+    got = bench.max_over_ranks([1.0 + rank, 5.0 - rank, 3.0], "cpu")
+    ref = bench.run_reference(argparse.Namespace(workload="tiny", steps=1, warmup=3, cpu_budget=1.0,
+                                                 gpus=world))
+    q.put((rank, got, ref is None))
+    dist.barrier()
+    dist.destroy_process_group()
+
+
+def test_max_over_ranks_and_rank0_reference_with_gloo():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    res = sorted(q.get(timeout=300) for _ in procs)
+    for p in procs:
+        p.join(timeout=120)
+        assert p.exitcode == 0
+    for rank, got, ref_none in res:
+        assert got == [2.0, 5.0, 3.0]
+        assert ref_none == (rank != 0)     # only rank 0 runs (and prints) the reference arm
+
+
+def test_job_value_adds_the_ranks_bytes():
+    import bench
+    assert bench.job_gbs(1e9, 1.0, 1) == pytest.approx(1000.0)
+    assert bench.job_gbs(1e9, 2.0, 4) == pytest.approx(2000.0)
+    assert bench.max_over_ranks([3.0, 1.0]) == [3.0, 1.0]      # outside torch.distributed

@@ -6,6 +6,7 @@
 #include <cstring>
 #include <map>
 #include <mutex>
+#include <random>
 #include <tuple>
 
 #include "pa_internal.h"
@@ -135,7 +136,9 @@ size_t balanced_ctas(int sms) { return (size_t)kMaxCtasPerSm * (size_t)sms; }
 size_t balanced_rows(int sms) { return 2 * balanced_ctas(sms) * kHeadsPerItem; }
 size_t counter_bytes(int sms) { return (balanced_ctas(sms) * 8 + 255) & ~size_t(255); }
 
-std::atomic<unsigned int> g_epoch{0};
+// Tags of the merge counters: a process starts from a random value, so that a
+// value a workspace kept from another process is unlikely to match.
+std::atomic<unsigned int> g_epoch{std::random_device{}()};
 
 unsigned int next_epoch()
 {

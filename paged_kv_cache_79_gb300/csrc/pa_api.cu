@@ -365,11 +365,7 @@ pa_status decode_impl(void *out, const void *q, const void *k_cache, const void 
     L.head_dim = head_dim;
     L.block_size = block_size;
     L.sm_count = sms;
-#ifdef PA_FORCE_GRID
-    L.grid = PA_FORCE_GRID;
-#else
-    L.grid = 0;
-#endif
+    L.grid = 0;  // the occupancy-sized persistent grid
     if (!make_cache_map(&L.tmap_k, k_cache, dtype, num_blocks, block_size, num_kv_heads, head_dim) ||
         !make_cache_map(&L.tmap_v, v_cache, dtype, num_blocks, block_size, num_kv_heads, head_dim))
         return cuda_fail(cudaErrorInvalidValue);

@@ -44,9 +44,6 @@ namespace pagedkv {
 #ifndef PA_STAGE_TOKENS
 #define PA_STAGE_TOKENS 32  // tokens per ring stage (fp16/bf16): blocks of 16 go two per stage
 #endif
-#ifndef PA_ITEM_ORDER
-#define PA_ITEM_ORDER 0
-#endif
 #ifndef PA_RING_BYTES
 #define PA_RING_BYTES 65536  // shared memory of the stage ring (two CTAs per SM)
 #endif
@@ -265,16 +262,9 @@ __device__ __forceinline__ Item decode_item(const DecodeParams &p, int bs, long 
     const long long units = (long long)p.num_kv_heads * p.head_groups;
     const long long rem = w - base;
     it.seq = seq;
-#if PA_ITEM_ORDER == 1
-    // the partitions of one (kv head, head group) are adjacent
-    const int np_seq = num_parts(p, seq, bs);
-    const int part = (int)(rem % np_seq);
-    const int u = (int)(rem / np_seq);
-#else
     // the kv heads of one partition are adjacent (they share DRAM pages)
     const int part = (int)(rem / units);
     const int u = (int)(rem % units);
-#endif
     it.kvh = u / p.head_groups;
     it.hg = u % p.head_groups;
     it.len = clamp_len(p, seq, bs);

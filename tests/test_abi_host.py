@@ -89,6 +89,46 @@ def test_cache_op_validation():
     assert L.pa_copy_blocks(FAKE, FAKE, FAKE, -1, 4, 64, None) == P.PA_ERR_INVALID
 
 
+def test_block_move_validation():
+    # every check below returns before any CUDA call (nothing is launched)
+    L = _lib.load()
+    assert L.pa_swap_blocks(FAKE, FAKE, FAKE, FAKE, FAKE, 0, 4, 4, 64, None) == P.PA_OK
+    assert L.pa_swap_blocks(None, FAKE, FAKE, FAKE, FAKE, 2, 4, 4, 64, None) == P.PA_ERR_INVALID
+    assert L.pa_swap_blocks(FAKE, FAKE, FAKE, FAKE, None, 2, 4, 4, 64, None) == P.PA_ERR_INVALID
+    assert L.pa_swap_blocks(FAKE, FAKE, FAKE, FAKE, FAKE, 2, 4, 4, 24, None) == P.PA_ERR_INVALID
+    assert L.pa_swap_blocks(FAKE, FAKE, FAKE, FAKE, FAKE, 2, 0, 4, 64, None) == P.PA_ERR_INVALID
+    assert L.pa_swap_blocks(FAKE + 8, FAKE, FAKE, FAKE, FAKE, 2, 4, 4, 64, None) == P.PA_ERR_INVALID
+    assert L.pa_swap_blocks(FAKE, FAKE, FAKE, FAKE, FAKE, 2, 4, 4, 16 * 65536 * 1024 + 16, None) == \
+        P.PA_ERR_UNSUPPORTED
+    gather = lambda ids, n, nbytes: L.pa_gather_blocks(FAKE, FAKE, ids, n, 4, FAKE, FAKE, nbytes, None)
+    scatter = lambda ids, n, nbytes: L.pa_scatter_blocks(FAKE, FAKE, FAKE, FAKE, ids, n, 4, nbytes, None)
+    for fn in (gather, scatter):
+        assert fn(FAKE, 0, 64) == P.PA_OK
+        assert fn(None, 3, 64) == P.PA_ERR_INVALID
+        assert fn(FAKE, -1, 64) == P.PA_ERR_INVALID
+        assert fn(FAKE, 3, 40) == P.PA_ERR_INVALID
+    assert L.pa_kv_transfer_worthwhile(64, 64) == 1 and L.pa_kv_transfer_worthwhile(63, 64) == 0
+
+
+def test_shared_decode_validation():
+    L = _lib.load()
+    args = dict(out=FAKE, q=FAKE, kc=FAKE, vc=FAKE, kn=None, vn=None, bt=FAKE, W=4, cl=FAKE, share=FAKE,
+                S=2, NB=8, scale=0.1, hq=8, hkv=8, d=128, b=16, dt=1, ws=FAKE, wsb=1 << 30)
+
+    def call(**kw):
+        a = dict(args, **kw)
+        return L.pa_decode_shared(a["out"], a["q"], a["kc"], a["vc"], a["kn"], a["vn"], a["bt"], a["W"],
+                                  a["cl"], a["share"], a["S"], a["NB"], a["scale"], a["hq"], a["hkv"],
+                                  a["d"], a["b"], a["dt"], a["ws"], a["wsb"], None)
+    assert call(S=0) == P.PA_OK
+    assert call(share=None) == P.PA_ERR_INVALID
+    assert call(share=FAKE + 4) == P.PA_ERR_INVALID              # share needs 8-byte alignment
+    assert call(kn=FAKE) == P.PA_ERR_INVALID                     # k_new without v_new
+    assert call(hq=40, hkv=2) == P.PA_ERR_UNSUPPORTED            # 20 query heads per kv head
+    assert P.pa_decode_shared_workspace_size(2, 8, 8, 128, 16, 4) > P.pa_decode_workspace_size(
+        2, 8, 8, 128, 16, 4, 0)
+
+
 def test_workspace_size_formula():
     # one partition: no workspace; several: fp32 partials + log-sum-exp per (seq, part, head)
     assert P.pa_decode_workspace_size(4, 8, 8, 64, 16, 4, 64) == 0

@@ -590,7 +590,7 @@ struct Producer {
 // G takes positions [c * total / G, (c + 1) * total / G).
 // ---------------------------------------------------------------------------
 #ifndef PA_UNIT_COST
-#define PA_UNIT_COST 2
+#define PA_UNIT_COST 4
 #endif
 constexpr int kUnitCost = PA_UNIT_COST;
 static_assert(kUnitCost >= 1, "every unit needs a start position");

@@ -16,7 +16,7 @@ import random
 
 import pytest
 
-UNIT_COST = 2   # positions charged per unit (kUnitCost in the kernel)
+UNIT_COST = 4   # positions charged per unit (kUnitCost in the kernel)
 
 
 def cta_of(x, total, G):

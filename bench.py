@@ -191,9 +191,14 @@ def prepare(name, device, seed_offset=0, partition_size=None):
     return w, ds, bt, cl
 
 
-def cpu_baseline(w, ds, bt, cl, budget_s=10.0):
+# the workloads whose oracle is also timed on one host core (tiny, MHA, GQA)
+ONE_CORE_WORKLOADS = ("tiny", "mha_fp16", "gqa_bf16")
+
+
+def cpu_baseline(w, ds, bt, cl, budget_s=10.0, threads=None):
     """Time the fp64 oracle (as it stands) on the host cores on a bounded sample:
-    whole decode steps over the sequences' blocks, repeated until ~budget_s."""
+    whole decode steps over the sequences' blocks, repeated until ~budget_s.
+    threads: the oracle's thread count for this timing (None: all host cores)."""
     import numpy as np
     import torch
     import oracle
@@ -207,17 +212,24 @@ def cpu_baseline(w, ds, bt, cl, budget_s=10.0):
     for s in range(len(cl)):
         sbt[s, :nbs[s]] = [remap[int(b)] for b in bt[s, :nbs[s]]]
     q = raw(ds.q)
-    # bound the sample: at most ~budget_s of work, at least one full decode step
-    t0 = time.perf_counter()
-    reps = 0
-    while True:
-        oracle.decode(q, kh, vh, sbt, cl, w.softmax_scale, w.dtype, w.num_q_heads, w.num_kv_heads,
-                      w.head_dim, B)
-        reps += 1
-        el = time.perf_counter() - t0
-        if el >= budget_s or reps >= 50:
-            break
-    return reps, el, oracle.num_threads()
+    before = oracle.num_threads()
+    if threads is not None:
+        oracle.set_num_threads(threads)
+    try:
+        # bound the sample: at most ~budget_s of work, at least one full decode step
+        t0 = time.perf_counter()
+        reps = 0
+        while True:
+            oracle.decode(q, kh, vh, sbt, cl, w.softmax_scale, w.dtype, w.num_q_heads,
+                          w.num_kv_heads, w.head_dim, B)
+            reps += 1
+            el = time.perf_counter() - t0
+            if el >= budget_s or reps >= 50:
+                break
+        used = oracle.num_threads()
+    finally:
+        oracle.set_num_threads(before)
+    return reps, el, used
 
 
 class L2Flush:
@@ -337,7 +349,21 @@ def run_ours(args):
     dec_ms = [b.elapsed_time(c) for a, b, c in ev]
     t_step = sum(step_ms) / len(step_ms)
     t_dec = sum(dec_ms) / len(dec_ms)
-    t_step, t_dec = max_over_ranks([t_step, t_dec], device)
+
+    # secondary: warm steps, back to back with no flush (whatever of the step the
+    # 129 MB L2 still holds from the step before is read from there)
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            step(stream)
+        wev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)]
+        for a, b in wev:
+            a.record(stream)
+            step(stream)
+            b.record(stream)
+        torch.cuda.synchronize(device)
+    t_warm = sum(a.elapsed_time(b) for a, b in wev) / len(wev)
+    t_step, t_dec, t_warm = max_over_ranks([t_step, t_dec, t_warm], device)
 
     # end to end through the public API with host buffers
     e2e = run_e2e(ds, stream, device, args, by, shared, world)
@@ -388,6 +414,8 @@ def run_ours(args):
                                 if fused else
                                 "pa_decode (partition kernel; split-KV merge fused or second kernel)")},
         "e2e": e2e,
+        "warm": {"ms_per_step": round(t_warm, 5), "value": round(job_gbs(by["step"], t_warm, world), 2),
+                 "unit": "GB/s", "note": "secondary: steps back to back without the L2 flush"},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk,
         "wall_s_timed_region": round(wall, 4),
@@ -398,6 +426,13 @@ def run_ours(args):
                                 "cores": cores, "kind": "oracle",
                                 "sample": f"{reps} full decode steps of this workload ({S} sequences), "
                                           f"fp64 C oracle, {el:.1f} s"}
+        if w.name in ONE_CORE_WORKLOADS:
+            reps, el, cores = cpu_baseline(w, ds, bt, cl, args.cpu_budget / 2, threads=1)
+            line["cpu_baseline_one_core"] = {
+                "value": round(reps * by["decode"] / el / 1e9, 4), "unit": "GB/s", "cores": cores,
+                "kind": "oracle",
+                "sample": f"{reps} full decode steps of this workload, fp64 C oracle on one core, "
+                          f"{el:.1f} s"}
     return line
 
 

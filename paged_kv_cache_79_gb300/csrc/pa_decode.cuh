@@ -74,24 +74,33 @@ constexpr int kAccPad = 8;  // floats of padding per merge row (spreads banks)
 // hooks away.
 #ifdef PA_TRACE
 constexpr int kTraceSlots = 16;
-constexpr int kTraceCtas = 4096;
+constexpr int kTraceCtas = 4096;  // rows: CTA index, plus half the rows for shared pass 1
 static __device__ unsigned long long g_trace[kTraceCtas * kTraceSlots];
-__device__ __forceinline__ void trace_set(int slot, unsigned long long v)
+__device__ __forceinline__ int trace_row(int pass)
 {
-    if (blockIdx.x < kTraceCtas)
-        g_trace[blockIdx.x * kTraceSlots + slot] = v;
+    const int r = (int)blockIdx.x + (pass ? kTraceCtas / 2 : 0);
+    return r < kTraceCtas ? r : -1;
 }
-__device__ __forceinline__ void trace_add(int slot, unsigned long long v)
+__device__ __forceinline__ void trace_set(int pass, int slot, unsigned long long v)
 {
-    if (blockIdx.x < kTraceCtas)
-        g_trace[blockIdx.x * kTraceSlots + slot] += v;
+    const int r = trace_row(pass);
+    if (r >= 0)
+        g_trace[r * kTraceSlots + slot] = v;
 }
-__device__ __forceinline__ bool trace_first_tile()
+__device__ __forceinline__ void trace_add(int pass, int slot, unsigned long long v)
 {
-    return blockIdx.x < kTraceCtas && g_trace[blockIdx.x * kTraceSlots + 1] == 0;
+    const int r = trace_row(pass);
+    if (r >= 0)
+        g_trace[r * kTraceSlots + slot] += v;
 }
-#define PA_TRACE_SET(slot, v) trace_set((slot), (v))
-#define PA_TRACE_ADD(slot, v) trace_add((slot), (v))
+__device__ __forceinline__ bool trace_first_tile(int pass)
+{
+    const int r = trace_row(pass);
+    return r >= 0 && g_trace[r * kTraceSlots + 1] == 0;
+}
+// call sites have the launch's DecodeParams in scope as `p`
+#define PA_TRACE_SET(slot, v) trace_set(p.pass, (slot), (v))
+#define PA_TRACE_ADD(slot, v) trace_add(p.pass, (slot), (v))
 #define PA_TRACE_DEFINE_READER(name)                                                     \
     extern "C" int pa_debug_trace_##name(unsigned long long *host, int n, int clear)      \
     {                                                                                   \
@@ -445,6 +454,10 @@ struct Producer {
         {
             const uint32_t slot = n % kItemSlots;
             int ok = 1;
+#ifdef PA_TRACE
+            if (lane == 0 && n == 0)
+                PA_TRACE_SET(15, dev::global_timer_ns());  // first item found
+#endif
             if (lane == 0) {
                 ok = dev::mbar_wait(dev::smem_addr(&c.item_empty[slot]),
                                     ((n / kItemSlots) & 1u) ^ 1u, kWaitTimeoutNs);
@@ -540,6 +553,8 @@ struct Producer {
                         }
                     }
 #ifdef PA_TRACE
+                    if (!t_last_issue)
+                        PA_TRACE_SET(14, dev::global_timer_ns());  // first tile issued
                     t_last_issue = dev::global_timer_ns();
                     PA_TRACE_ADD(7, 1);
 #endif
@@ -635,9 +650,21 @@ __device__ __forceinline__ SeqUnits seq_units(const DecodeParams &p, int s, int 
         if (p.share && p.share[2 * s] == s) {
             const int P = shared_blocks(p, s);
             if (P > 0) {
+                // members follow their first member: count them eight entries at a
+                // time, the eight loads in flight together
                 int m = 1;
-                while (s + m < p.num_seqs && p.share[2 * (s + m)] == s)
-                    ++m;
+                for (;;) {
+                    int v[8];
+#pragma unroll
+                    for (int k = 0; k < 8; ++k)
+                        v[k] = (s + m + k < p.num_seqs) ? p.share[2 * (s + m + k)] : -1;
+                    int k = 0;
+                    while (k < 8 && v[k] == s)
+                        ++k;
+                    m += k;
+                    if (k < 8)
+                        break;
+                }
                 const int mpi = members_per_item(p.group);
                 u.members = m;
                 u.mgroups = (m + mpi - 1) / mpi;
@@ -1243,7 +1270,7 @@ __device__ __forceinline__ bool consume_item_n8(const DecodeParams &p, const Cta
             const unsigned long long t_now = dev::global_timer_ns();
             PA_TRACE_ADD(13, t_now - t_sw);
             PA_TRACE_SET(11, t_now);
-            if (trace_first_tile()) {
+            if (trace_first_tile(p.pass)) {
                 PA_TRACE_SET(1, t_now);
             }
         }

@@ -52,3 +52,25 @@ def test_job_value_adds_the_ranks_bytes():
     assert bench.job_gbs(1e9, 1.0, 1) == pytest.approx(1000.0)
     assert bench.job_gbs(1e9, 2.0, 4) == pytest.approx(2000.0)
     assert bench.max_over_ranks([3.0, 1.0]) == [3.0, 1.0]      # outside torch.distributed
+
+
+def test_cpu_baseline_one_core_restores_the_thread_count():
+    """The one-core oracle timing runs on one thread and leaves the oracle's thread
+    count as it found it."""
+    import types
+    import torch
+    import bench
+    import oracle
+    import workloads as W
+    w = W.by_name("tiny")
+    oalloc, _ = oracle.run_script(w.events, w.num_blocks, w.block_size, w.free_order)
+    bt, cl = oracle.tables_for(oalloc, w.decode_seqs)
+    shape = (w.num_blocks, w.block_size, w.num_kv_heads, w.head_dim)
+    ds = types.SimpleNamespace(k_cache=W.randn(shape, w.dtype, 1), v_cache=W.randn(shape, w.dtype, 2),
+                               q=W.query_tensor(w, 0))
+    before = oracle.num_threads()
+    reps, el, cores = bench.cpu_baseline(w, ds, bt, cl, budget_s=0.05, threads=1)
+    assert cores == 1 and reps >= 1 and el > 0
+    assert oracle.num_threads() == before
+    reps, el, cores = bench.cpu_baseline(w, ds, bt, cl, budget_s=0.05)
+    assert cores == before

@@ -626,19 +626,26 @@ struct SeqUnits {
     int mgroups;  // pass 1: member groups per kv head
 };
 
-__device__ __forceinline__ int shared_blocks(const DecodeParams &p, int s)
-{
-    if (!p.share || p.group > kHeadsPerItem || p.share[2 * s] < 0)
-        return 0;
-    const int v = p.share[2 * s + 1];
-    return v > 0 ? min(v, p.max_blocks) : 0;
-}
-
 __device__ __forceinline__ SeqUnits seq_units(const DecodeParams &p, int s, int bs, int bps)
 {
+    // Every entry of the sequence the walk may need is loaded before any is tested,
+    // so that the loads are in flight together: one memory round trip per batch of
+    // sequences rather than one per test (length, group, prefix length, members).
+    const bool grouped = p.share != nullptr && p.group <= kHeadsPerItem;
+    const bool members = grouped && p.pass == 1;
+    const int t = p.context_lens[s];
+    const int lead = grouped ? p.share[2 * s] : -1;
+    const int sp = grouped ? p.share[2 * s + 1] : 0;
+    int v[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+        v[k] = (members && s + 1 + k < p.num_seqs) ? p.share[2 * (s + 1 + k)] : -1;
+    const int cap = p.max_blocks * bs;
+    const int len = t < 0 ? 0 : (t > cap ? cap : t);
+    // leading blocks shared with the group (0: not grouped)
+    const int shared = (lead >= 0 && sp > 0) ? min(sp, p.max_blocks) : 0;
+
     SeqUnits u;
-    const int len = clamp_len(p, s, bs);
-    const int nb = (len + bs - 1) / bs;
     u.members = 1;
     u.mgroups = 1;
     if (p.pass == 1) {
@@ -647,36 +654,35 @@ __device__ __forceinline__ SeqUnits seq_units(const DecodeParams &p, int s, int 
         u.start = 0;
         u.nb = 0;
         u.len = 0;
-        if (p.share && p.share[2 * s] == s) {
-            const int P = shared_blocks(p, s);
-            if (P > 0) {
-                // members follow their first member: count them eight entries at a
-                // time, the eight loads in flight together
-                int m = 1;
-                for (;;) {
-                    int v[8];
+        if (lead == s && shared > 0) {
+            // members follow their first member; past the first eight, eight more
+            // entries at a time
+            int k = 0;
+            while (k < 8 && v[k] == s)
+                ++k;
+            int m = 1 + k;
+            while (k == 8) {
+                int w[8];
 #pragma unroll
-                    for (int k = 0; k < 8; ++k)
-                        v[k] = (s + m + k < p.num_seqs) ? p.share[2 * (s + m + k)] : -1;
-                    int k = 0;
-                    while (k < 8 && v[k] == s)
-                        ++k;
-                    m += k;
-                    if (k < 8)
-                        break;
-                }
-                const int mpi = members_per_item(p.group);
-                u.members = m;
-                u.mgroups = (m + mpi - 1) / mpi;
-                u.nunits = p.num_kv_heads * u.mgroups;
-                u.ns = (P + bps - 1) / bps;
-                u.nb = P;
-                u.len = P * bs;
+                for (int j = 0; j < 8; ++j)
+                    w[j] = (s + m + j < p.num_seqs) ? p.share[2 * (s + m + j)] : -1;
+                k = 0;
+                while (k < 8 && w[k] == s)
+                    ++k;
+                m += k;
             }
+            const int mpi = members_per_item(p.group);
+            u.members = m;
+            u.mgroups = (m + mpi - 1) / mpi;
+            u.nunits = p.num_kv_heads * u.mgroups;
+            u.ns = (shared + bps - 1) / bps;
+            u.nb = shared;
+            u.len = shared * bs;
         }
         return u;
     }
-    const int P = min(shared_blocks(p, s), nb);
+    const int nb = (len + bs - 1) / bs;
+    const int P = min(shared, nb);
     u.nunits = p.num_kv_heads * p.head_groups;
     u.ns = (nb - P + bps - 1) / bps;
     u.start = P;

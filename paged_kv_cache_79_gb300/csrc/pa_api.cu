@@ -184,6 +184,18 @@ int cached_occupancy(void *kernel, int device, size_t smem, size_t max_smem)
     auto it = g_occupancy.find(key);
     if (it != g_occupancy.end())
         return it->second;
+    // configurations past the device's per-block opt-in limit cannot launch; the
+    // attribute is raised to the largest configuration that can
+    int optin = 0;
+    if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, device) !=
+        cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    if (smem > (size_t)optin)
+        return 0;
+    if (max_smem > (size_t)optin)
+        max_smem = (size_t)optin;
     const auto lkey = std::make_pair(kernel, device);
     if (g_smem_limit[lkey] < max_smem) {
         if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,

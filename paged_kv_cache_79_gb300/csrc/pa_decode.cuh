@@ -81,22 +81,29 @@ __device__ __forceinline__ int trace_row(int pass)
     const int r = (int)blockIdx.x + (pass ? kTraceCtas / 2 : 0);
     return r < kTraceCtas ? r : -1;
 }
+// -DPA_TRACE_LITE keeps only the once-per-CTA stamps (start, end, SM, items, first
+// item, first tile issued, producer end), whose cost does not distort the schedule
+#ifdef PA_TRACE_LITE
+constexpr bool kTraceLite = true;
+#else
+constexpr bool kTraceLite = false;
+#endif
 __device__ __forceinline__ void trace_set(int pass, int slot, unsigned long long v)
 {
     const int r = trace_row(pass);
-    if (r >= 0)
+    if (r >= 0 && (!kTraceLite || slot == 0 || slot == 2 || slot == 3 || slot == 4 || slot == 8 || slot >= 14))
         g_trace[r * kTraceSlots + slot] = v;
 }
 __device__ __forceinline__ void trace_add(int pass, int slot, unsigned long long v)
 {
     const int r = trace_row(pass);
-    if (r >= 0)
+    if (r >= 0 && !kTraceLite)
         g_trace[r * kTraceSlots + slot] += v;
 }
 __device__ __forceinline__ bool trace_first_tile(int pass)
 {
     const int r = trace_row(pass);
-    return r >= 0 && g_trace[r * kTraceSlots + 1] == 0;
+    return !kTraceLite && r >= 0 && g_trace[r * kTraceSlots + 1] == 0;
 }
 // call sites have the launch's DecodeParams in scope as `p`
 #define PA_TRACE_SET(slot, v) trace_set(p.pass, (slot), (v))

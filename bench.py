@@ -195,6 +195,15 @@ def prepare(name, device, seed_offset=0, partition_size=None):
 ONE_CORE_WORKLOADS = ("tiny", "mha_fp16", "gqa_bf16")
 
 
+def workload_config(w, cl):
+    """The workload's own keys of the JSON line's config (both arms)."""
+    import numpy as np
+    return {"workload": w.name, "num_seqs": len(cl), "num_q_heads": w.num_q_heads,
+            "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim, "block_size": w.block_size,
+            "num_blocks": w.num_blocks, "context_tokens": int(np.sum(cl)),
+            "max_context": int(np.max(cl))}
+
+
 def cpu_baseline(w, ds, bt, cl, budget_s=10.0, threads=None):
     """Time the fp64 oracle (as it stands) on the host cores on a bounded sample:
     whole decode steps over the sequences' blocks, repeated until ~budget_s.
@@ -387,10 +396,7 @@ def run_ours(args):
         "vs_baseline": None,
         "dtype": w.dtype,
         "data": "synthetic (seeded N(0,1) q/K/V; seeded allocator script)",
-        "config": {"workload": w.name, "num_seqs": S, "num_q_heads": w.num_q_heads,
-                   "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim, "block_size": w.block_size,
-                   "num_blocks": w.num_blocks, "context_tokens": int(np.sum(cl)),
-                   "max_context": int(np.max(cl)),
+        "config": {**workload_config(w, cl),
                    "split": "balanced" if parts == 0 else f"fixed partitions of {parts} tokens",
                    "append": "fused into the decode launch" if fused else "separate launch",
                    "prefix_sharing": (f"{int((ds.share[:, 0] >= 0).sum())} sequences in groups that "
@@ -512,11 +518,13 @@ def run_reference(args):
     t = sum(times) / len(times)
     value = by["decode"] / t / 1e9
     cores = oracle.num_threads()
-    return {"metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": 0, "steps": args.steps,
+    return {"metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": args.gpus,
+            "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(t * 1e3, 3), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "impl": "reference",
-            "config": {"workload": w.name, "num_seqs": len(cl), "context_tokens": int(np.sum(cl))},
+            "config": {**workload_config(w, cl),
+                       "parallelism": "the oracle on rank 0's host cores (no GPU)"},
             "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
                              "sample": f"one full decode step of {w.name} per timed step (fp64 C oracle)"},
             "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,

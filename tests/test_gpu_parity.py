@@ -7,7 +7,7 @@ import torch
 
 import oracle
 import paged_kv_cache_79_gb300 as P
-from tests.gpu_harness import assert_close, raw, small_case
+from tests.gpu_harness import TOL_F32, assert_close, errors, raw, small_case
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -244,3 +244,45 @@ def test_decode_append_equals_append_then_decode(dtype, D, B, Hq, Hkv, lens, par
     want = oracle.decode(raw(q), kh, vh, bt.numpy(), cl.numpy(), 0.11, dtype, Hq, Hkv, D, B)
     assert_close(out2, want, dtype)
     assert P.pa_device_errors() == 0
+
+
+@pytest.mark.parametrize("dtype", ["f32", "f16", "bf16"])
+@pytest.mark.parametrize("Hq,Hkv,lens", [(8, 8, [1, 300, 4097]), (64, 8, [2, 5000]), (16, 1, [777])])
+def test_large_scores_match_oracle(dtype, Hq, Hkv, lens):
+    # q scaled by 40: scores of standard deviation ~40 (a softmax peaked on a few
+    # keys, exponent differences of thousands); the running max and the split-unit
+    # merges must still give the oracle's result, with nothing overflowing
+    D, B = 128, 16
+    q, kc, vc, bt, cl = small_case(len(lens) * 31 + Hq, dtype, D, B, Hq, Hkv, lens)
+    q = (q.float() * 40).to(q.dtype)
+    scale = 1.0 / math.sqrt(D)
+    got = run_decode(q, kc, vc, bt, cl, scale, Hq, Hkv, D, B)
+    want = oracle_decode(q, kc, vc, bt, cl, scale, dtype, Hq, Hkv, D, B)
+    if dtype == "f32":
+        # fp32 storage: a score's rounding error in fp32 is proportional to its size
+        # (sum of D products, each rounded relative to itself), so the 1e-5 bound
+        # stated for unit-scale scores grows with the factor 40 applied to q
+        assert np.all(np.isfinite(got.cpu().numpy()))
+        err = errors(got, want)[0]
+        assert err <= 40 * TOL_F32, f"f32 large scores: max abs err {err:.3e} > {40 * TOL_F32}"
+    else:
+        assert_close(got, want, dtype, f"{dtype} G{Hq // Hkv} {lens} large scores")
+
+
+@pytest.mark.parametrize("where", ["first", "middle", "last"])
+def test_one_dominant_key_across_a_split_context(where):
+    # a 30000-token context (split over many CTAs) whose keys are random except one,
+    # a large multiple of the query: the output is that key's value row, wherever the
+    # key sits relative to the split points
+    dtype, D, B, Hq, Hkv = "bf16", 128, 16, 8, 8
+    lens = [30000]
+    q, kc, vc, bt, cl = small_case(17, dtype, D, B, Hq, Hkv, lens)
+    tok = {"first": 0, "middle": 14999, "last": 29999}[where]
+    blk, row = int(bt[0, tok // B]), tok % B
+    kc[blk, row] = (q[0].float() * 8).to(kc.dtype)       # head h key = 8 q[h]: score ~90
+    scale = 1.0 / math.sqrt(D)
+    got = run_decode(q, kc, vc, bt, cl, scale, Hq, Hkv, D, B)
+    want = oracle_decode(q, kc, vc, bt, cl, scale, dtype, Hq, Hkv, D, B)
+    assert_close(got, want, dtype, f"dominant key at {where}")
+    # the dominant key's weight is ~1: the output is (nearly) its value row
+    assert torch.allclose(got[0].float().cpu(), vc[blk, row].float(), atol=0.05, rtol=0.02)

@@ -23,15 +23,21 @@
 //   warp 4      producer: reads the block table of the item, and for every block
 //               issues TMA tile loads of K and V (box = head_dim x block_size of one
 //               kv head, 128-byte swizzle) into a ring of shared-memory stages;
-//   warps 0..3  consumers: block g of the CTA's stream goes to warp g % 4; each
+//   warps 0..3  consumers: ring stage i of an item (32 tokens for fp16/bf16, one
+//               block for fp32) goes to warp (i + rot) % 4, rot fixed by the item's
+//               place in the stream, so consecutive items continue the rotation and
+//               the rounding does not depend on which CTA runs an item; each warp
 //               keeps an online-softmax state (max, exp-sum, weighted V) per query
-//               head; at the end of an item the four states are merged through
+//               row; at the end of an item the four states are merged through
 //               shared memory and written as the final output (the item is a whole
 //               unit) or as a partial (fp32 output + log2-sum-exp).
-// For fp16/bf16 the consumers use mma.sync.m16n8k16 with fp32 accumulation:
-// S[16 heads x 8 tokens] = Q K^T, then O[16 heads x 8 dims] += P V, P kept in
-// registers (the C fragment of Q K^T is the A fragment of P V).  For fp32 they use
-// CUDA-core FMAs (tensor cores would round fp32 to tf32).
+// For fp16/bf16 the consumers use mma.sync.m16n8k16 with fp32 accumulation.  Items
+// of up to 8 query rows (a group of <= 8 heads, or the members of a shared prefix)
+// take the transposed products S^T[tokens x rows] = K Q^T and O^T += V^T P^T, so a
+// 16-row MMA tile carries 16 tokens rather than padding rows; wider items take
+// S[16 rows x 8 tokens] = Q K^T, then O += P V, P kept in registers (the C fragment
+// of Q K^T is the A fragment of P V).  For fp32 they use CUDA-core FMAs (tensor
+// cores would round fp32 to tf32).
 #pragma once
 
 #include <cfloat>

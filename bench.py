@@ -84,11 +84,22 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+def strip_comments(src: str) -> str:
+    """C/C++ source without its comments and blank space (string literals in these
+    sources hold no comment markers)."""
+    import re
+    src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)
+    src = re.sub(r"//[^\n]*", " ", src)
+    return " ".join(src.split())
+
+
 def decode_source_hash():
+    """Hash of the decode sources' code (comments and spacing excluded): the traffic
+    counters stay valid while only comments change."""
     h = hashlib.sha256()
     for n in DECODE_SOURCES:
-        with open(os.path.join(ROOT, "paged_kv_cache_79_gb300", "csrc", n), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, "paged_kv_cache_79_gb300", "csrc", n), encoding="utf-8") as f:
+            h.update(strip_comments(f.read()).encode())
     return h.hexdigest()[:16]
 
 

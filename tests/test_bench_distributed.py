@@ -74,3 +74,20 @@ def test_cpu_baseline_one_core_restores_the_thread_count():
     assert oracle.num_threads() == before
     reps, el, cores = bench.cpu_baseline(w, ds, bt, cl, budget_s=0.05)
     assert cores == before
+
+
+def test_traffic_counters_follow_code_not_comments(tmp_path, monkeypatch):
+    """The committed DRAM counters are reported while the decode sources' code is the
+    one they were taken on: comment edits keep them, code edits drop them."""
+    import bench
+    assert bench.strip_comments("int a; // x\n/* y\n z */ int  b;") == "int a; int b;"
+    src = tmp_path / "paged_kv_cache_79_gb300" / "csrc"
+    src.mkdir(parents=True)
+    for n in bench.DECODE_SOURCES:
+        (src / n).write_text("int f() { return 1; } // v1\n")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    h = bench.decode_source_hash()
+    (src / bench.DECODE_SOURCES[0]).write_text("/* new comment */ int f() {  return 1; }\n")
+    assert bench.decode_source_hash() == h
+    (src / bench.DECODE_SOURCES[0]).write_text("int f() { return 2; }\n")
+    assert bench.decode_source_hash() != h

@@ -1759,8 +1759,12 @@ __global__ void __launch_bounds__(kThreads, 2)
 
 // ---------------------------------------------------------------------------
 // fp32 partition kernel: CUDA-core consumers (same producer, ring and merge).
+// H: query rows an item of the launch carries at most (1, 4 or 16).  The
+// consumers' per-row state and loops are sized by it: a launch whose items hold
+// one row (multi-head attention) carries no predicated-off work for fifteen
+// others and keeps its state in registers.
 // ---------------------------------------------------------------------------
-template <int D, int BS>
+template <int D, int BS, int H>
 __global__ void __launch_bounds__(kThreads, 1)
     pa_decode_f32_kernel(const __grid_constant__ DecodeParams p,
                          const __grid_constant__ CUtensorMap tmap_k,
@@ -1771,7 +1775,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr int NPART = 32 / BS;       // lanes per token in the score phase
     constexpr int DP = D / NPART;        // head dims per lane in the score phase
     constexpr int VEC = D / 32;          // head dims per lane in the P V phase
-    constexpr int H = kHeadsPerItem;
+    static_assert(H == 1 || H == 4 || H == kHeadsPerItem, "row capacities 1, 4, 16");
     constexpr int SA = D + kAccPad;
 
     extern __shared__ uint8_t smem_raw[];
@@ -1796,6 +1800,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int part = lane / BS;
     uint32_t g = 0;
     uint32_t sph = 0;
+#ifdef PA_TRACE
+    if (threadIdx.x == 0) {
+        unsigned int smid;
+        asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+        PA_TRACE_SET(0, dev::global_timer_ns());
+        PA_TRACE_SET(8, smid);
+    }
+#endif
     bool pfx_ready = !defers_dependency(p);  // prefix rows may be read
     for (uint32_t n = 0;; ++n) {
         const uint32_t slot = n % kItemSlots;
@@ -1811,7 +1823,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         float *pfx_s = c.pfx + (n & 1) * pfx_rows * (D + kPfxPad);
         if (merge_pfx && pfx_ready)
             stage_prefix<D>(p, it, pfx_s, threadIdx.x);
-        const float *qs = reinterpret_cast<const float *>(c.qslots) + slot * H * D;
+        const float *qs = reinterpret_cast<const float *>(c.qslots) + slot * kHeadsPerItem * D;
 
         float acc[H][VEC];
         float mr[H], lr[H];
@@ -1829,12 +1841,24 @@ __global__ void __launch_bounds__(kThreads, 1)
             if ((j - it.j0 + rot) % kConsumerWarps != warp)
                 continue;
             const uint32_t st = g % C::kStages;
+#ifdef PA_TRACE
+            const unsigned long long t_sw = dev::global_timer_ns();
+#endif
             if (!warp_wait(&c.full[st], (g / C::kStages) & 1u)) {
                 if (lane == 0)
                     raise_error(p, c.abort, PA_DEVERR_TIMEOUT_FULL);
                 alive = false;
                 break;
             }
+#ifdef PA_TRACE
+            if (threadIdx.x == 0) {
+                const unsigned long long t_now = dev::global_timer_ns();
+                PA_TRACE_ADD(13, t_now - t_sw);
+                PA_TRACE_SET(11, t_now);
+                if (trace_first_tile(p.pass))
+                    PA_TRACE_SET(1, t_now);
+            }
+#endif
             const int valid = min(BS, it.len - j * BS);
             const uint8_t *kt = c.ring + (size_t)st * C::kStageBytes;
             const uint8_t *vt = kt + C::kTileBytes;
@@ -1947,8 +1971,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int e = 0; e < VEC; ++e)
                     mine[r * SA + lane * VEC + e] = acc[r][e];
                 if (lane == 0) {
-                    c.mml[(warp * H + r) * 2] = lr[r] > 0.f ? mr[r] : -INFINITY;
-                    c.mml[(warp * H + r) * 2 + 1] = lr[r];
+                    c.mml[(warp * kHeadsPerItem + r) * 2] = lr[r] > 0.f ? mr[r] : -INFINITY;
+                    c.mml[(warp * kHeadsPerItem + r) * 2 + 1] = lr[r];
                 }
             }
         }
@@ -1960,20 +1984,37 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             dev::cp_async_wait_all();
         }
+#ifdef PA_TRACE
+        const unsigned long long t_m0 = dev::global_timer_ns();
+        if (threadIdx.x == 0)
+            PA_TRACE_SET(12, t_m0);  // warp 0 done with the item's stages
+#endif
         if (!consumer_sync(c, sph)) {
             if (lane == 0)
                 raise_error(p, c.abort, PA_DEVERR_TIMEOUT_FULL);
             break;
         }
+#ifdef PA_TRACE
+        if (threadIdx.x == 0)
+            PA_TRACE_SET(10, dev::global_timer_ns());  // all warps done
+#endif
         finalize_item<float, D>(p, it, c.macc, c.mml, rows_cap, threadIdx.x, pfx_s);
         if (!finish_item<float, D>(p, it, c, sph, warp, lane, pfx_s)) {
             if (lane == 0)
                 raise_error(p, c.abort, PA_DEVERR_TIMEOUT_FULL);
             break;
         }
+#ifdef PA_TRACE
+        if (threadIdx.x == 0)
+            PA_TRACE_ADD(9, dev::global_timer_ns() - t_m0);
+#endif
         if (*c.abort)
             break;
     }
+#ifdef PA_TRACE
+    if (threadIdx.x == 0)
+        PA_TRACE_SET(2, dev::global_timer_ns());
+#endif
 }
 // ---------------------------------------------------------------------------
 // Split-KV merge: out[s][h] = sum_p 2^(lse_p - M) o_p / sum_p 2^(lse_p - M).
@@ -2047,15 +2088,23 @@ __global__ void __launch_bounds__(128)
 // consumers; wider items the 16-row form.
 template <typename T, int D, int BS>
 struct KernelOf {
-    static void *get(bool narrow)
+    static void *get(const DecodeParams &p)
     {
-        return narrow ? reinterpret_cast<void *>(&pa_decode_mma_kernel<T, D, BS, true>)
-                      : reinterpret_cast<void *>(&pa_decode_mma_kernel<T, D, BS, false>);
+        return p.group <= kNarrowRows
+                   ? reinterpret_cast<void *>(&pa_decode_mma_kernel<T, D, BS, true>)
+                   : reinterpret_cast<void *>(&pa_decode_mma_kernel<T, D, BS, false>);
     }
 };
 template <int D, int BS>
 struct KernelOf<float, D, BS> {
-    static void *get(bool) { return reinterpret_cast<void *>(&pa_decode_f32_kernel<D, BS>); }
+    // by the launch's row capacity (its widest item)
+    static void *get(const DecodeParams &p)
+    {
+        const int rows_cap = item_rows_cap(p);
+        return rows_cap <= 1   ? reinterpret_cast<void *>(&pa_decode_f32_kernel<D, BS, 1>)
+               : rows_cap <= 4 ? reinterpret_cast<void *>(&pa_decode_f32_kernel<D, BS, 4>)
+                               : reinterpret_cast<void *>(&pa_decode_f32_kernel<D, BS, kHeadsPerItem>);
+    }
 };
 
 template <typename T, int D, int BS>
@@ -2072,7 +2121,7 @@ template <typename T, int D, int BS>
 cudaError_t launch_decode_impl(const DecodeLaunch &L, cudaStream_t stream)
 {
     const DecodeParams &p = L.p;
-    void *kern = KernelOf<T, D, BS>::get(p.group <= kNarrowRows);
+    void *kern = KernelOf<T, D, BS>::get(p);
     const size_t smem = smem_bytes_for<T, D, BS>(item_rows_cap(p), item_pfx_rows(p));
     const size_t smem_max = smem_bytes_for<T, D, BS>(kHeadsPerItem, kHeadsPerItem);
     int dev = 0;

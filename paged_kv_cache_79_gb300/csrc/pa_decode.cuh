@@ -192,7 +192,7 @@ __host__ __device__ inline SmemLayout make_layout(int stages, int stage_bytes, i
     o = (o + 15u) & ~15u;
     L.bars = o;
     o += (2u * (uint32_t)stages + 2u * kItemSlots + 1u) * 8u;
-    L.flag = o;  // abort flag, merge flag, then one scratch word per consumer warp
+    L.flag = o;  // abort flag, merge flag, counter seen, then a scratch word per consumer warp
     o += 16u + 4u * kConsumerWarps;
     L.total = o + 1024u;  // slack to align the base to 1024 bytes (128-byte swizzle)
     return L;
@@ -322,6 +322,7 @@ struct CtaState {
     float *pfx;                        // two buffers of shared-prefix rows (item parity)
     volatile int *abort;
     volatile int *merge;               // this CTA completes the current split unit
+    unsigned long long *ctr_seen;      // the split unit's counter as the probe read it
     volatile uint32_t *sink;           // per consumer warp: see dev::settle_loads
 };
 
@@ -343,6 +344,7 @@ __device__ __forceinline__ CtaState cta_state(uint8_t *smem, const SmemLayout &l
     c.pfx = reinterpret_cast<float *>(smem + lay.pfx);
     c.abort = reinterpret_cast<volatile int *>(smem + lay.flag);
     c.merge = reinterpret_cast<volatile int *>(smem + lay.flag + 4);
+    c.ctr_seen = reinterpret_cast<unsigned long long *>(smem + lay.flag + 8);
     c.sink = reinterpret_cast<volatile uint32_t *>(smem + lay.flag + 16);
     return c;
 }
@@ -975,9 +977,9 @@ __device__ __forceinline__ void stage_prefix(const DecodeParams &p, const Item &
 // Merge the four consumer states of one item and store it.
 // ---------------------------------------------------------------------------
 template <typename T, int D>
-__device__ __forceinline__ void finalize_item(const DecodeParams &p, const Item &it,
-                                              const float *acc, const float *ml, int rows_cap,
-                                              int tid, const float *pfx_s)
+__device__ __forceinline__ void finalize_item(const DecodeParams &p, const Item &it, float *acc,
+                                              const float *ml, int rows_cap, int tid,
+                                              const float *pfx_s, bool own_in_smem)
 {
     constexpr int S = D + kAccPad;
     for (int idx = tid; idx < it.rows * D; idx += 32 * kConsumerWarps) {
@@ -1008,6 +1010,11 @@ __device__ __forceinline__ void finalize_item(const DecodeParams &p, const Item 
         const float o = (L > 0.f) ? O / L : 0.f;
         if (!it.partial) {
             store_result<T, D>(p, it, r, col, o, (L > 0.f) ? M + log2f(L) : -INFINITY, pfx_s);
+        } else if (own_in_smem) {
+            // this CTA completes the unit now: its rows stay here, in the first warp's
+            // accumulator rows (each element read, then written, by this thread alone);
+            // the merge recomputes their log2-sum-exp from `ml`
+            acc[r * S + col] = o;
         } else {
             const size_t pr = (size_t)it.prow0 + r;
             p.part_o[pr * D + col] = o;
@@ -1025,10 +1032,10 @@ __device__ __forceinline__ void finalize_item(const DecodeParams &p, const Item 
 // another.  Counters hold (epoch << 32 | count): a value left by an earlier call
 // carries another epoch and counts as zero, so they never need clearing.
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ bool count_partial(const DecodeParams &p, const Item &it)
+__device__ __forceinline__ bool count_partial(const DecodeParams &p, const Item &it,
+                                              unsigned long long old)
 {
     unsigned long long *ctr = p.counters + it.c_first;
-    unsigned long long old = *reinterpret_cast<volatile unsigned long long *>(ctr);
     unsigned int cnt;
     for (;;) {  // each failed exchange means another CTA counted: at most nparts rounds
         cnt = (unsigned int)(old >> 32) == p.epoch ? (unsigned int)old : 0u;
@@ -1039,6 +1046,56 @@ __device__ __forceinline__ bool count_partial(const DecodeParams &p, const Item 
         old = prev;
     }
     return cnt + 1u == (unsigned int)it.nparts;
+}
+
+// Before the item's final barrier, thread 0 of a CTA holding one of the two parts of
+// a unit cut once reads the unit's counter.  When the other part is counted
+// already, this CTA completes the unit: after an acquire fence (the other part's
+// rows were released before its count) it merges them with its own rows, kept in
+// shared memory, and neither stores, fences nor counts its own (*c.merge = 2).
+// Otherwise the count follows the usual release (finish_item), from the value read
+// here.  Units cut more than once skip the early read: their parts tend to finish
+// together, and a value read early would only make their exchanges fail.
+__device__ __forceinline__ void probe_split_last(const DecodeParams &p, const Item &it,
+                                                 const CtaState &c)
+{
+    int early = 0;
+    if (p.balanced && it.partial) {
+        const unsigned long long v =
+            *reinterpret_cast<volatile unsigned long long *>(p.counters + it.c_first);
+        *c.ctr_seen = v;
+        const unsigned int cnt = (unsigned int)(v >> 32) == p.epoch ? (unsigned int)v : 0u;
+        if (it.nparts == 2 && cnt == 1u) {
+            dev::fence_acq_rel_gpu();
+            early = 1;
+        }
+    }
+    *c.merge = early ? 2 : 0;
+}
+
+// Log2-sum-exp of row r of this CTA's own part, from the consumer warps' (max, sum).
+__device__ __forceinline__ float own_lse(const float *ml, int r)
+{
+    float M = -FLT_MAX;
+    bool any = false;
+#pragma unroll
+    for (int c = 0; c < kConsumerWarps; ++c) {
+        const float mc = ml[(c * kHeadsPerItem + r) * 2];
+        if (mc != -INFINITY) {
+            M = fmaxf(M, mc);
+            any = true;
+        }
+    }
+    float L = 0.f;
+    if (any) {
+#pragma unroll
+        for (int c = 0; c < kConsumerWarps; ++c) {
+            const float mc = ml[(c * kHeadsPerItem + r) * 2];
+            if (mc != -INFINITY)
+                L += exp2f(mc - M) * ml[(c * kHeadsPerItem + r) * 2 + 1];
+        }
+    }
+    return L > 0.f ? M + log2f(L) : -INFINITY;
 }
 
 // Partial row i (0-based) of a split unit: slot 2 c_first + 1, then slot 2 c of the
@@ -1060,11 +1117,17 @@ __device__ __forceinline__ long long split_slot(const Item &it, int i, long long
 
 // Merge the nparts partials of a split unit into its output rows: one warp per
 // query head; lane i holds partial i's log2-sum-exp.
+// own_o: this CTA's own rows (row stride D + kAccPad) when it completes a unit cut
+// once early (probe_split_last), with their log2-sum-exp from own_ml; null when its
+// part went through the partial slots.
 template <typename T, int D>
 __device__ __forceinline__ void merge_split_unit(const DecodeParams &p, const Item &it, int warp,
-                                              int lane, const float *pfx_s)
+                                              int lane, const float *pfx_s,
+                                              const float *own_o = nullptr,
+                                              const float *own_ml = nullptr)
 {
     constexpr int VEC = D / 32;
+    constexpr int S = D + kAccPad;
     const long long total = ((long long)it.total_hi << 32) | (long long)it.total_lo;
     const long long G = balanced_grid(total, it.divisor());
     for (int r = warp; r < it.rows; r += kConsumerWarps) {
@@ -1072,12 +1135,18 @@ __device__ __forceinline__ void merge_split_unit(const DecodeParams &p, const It
             // the usual case (a unit cut once): both parts' loads in flight at once
             const int r0 = (int)split_slot(it, 0, total, G) * kHeadsPerItem + r;
             const int r1 = (int)split_slot(it, 1, total, G) * kHeadsPerItem + r;
-            const float l0 = __ldcg(p.part_lse + r0), l1 = __ldcg(p.part_lse + r1);
+            const int own = own_o ? it.prow0 + r : -1;
+            const bool o0 = r0 == own, o1 = r1 == own;
+            const float lo = own_o ? own_lse(own_ml, r) : 0.f;
+            const float l0 = o0 ? lo : __ldcg(p.part_lse + r0);
+            const float l1 = o1 ? lo : __ldcg(p.part_lse + r1);
             float v0[VEC], v1[VEC];
 #pragma unroll
             for (int e = 0; e < VEC; ++e) {
-                v0[e] = __ldcg(p.part_o + (size_t)r0 * D + lane * VEC + e);
-                v1[e] = __ldcg(p.part_o + (size_t)r1 * D + lane * VEC + e);
+                v0[e] = o0 ? own_o[r * S + lane * VEC + e]
+                           : __ldcg(p.part_o + (size_t)r0 * D + lane * VEC + e);
+                v1[e] = o1 ? own_o[r * S + lane * VEC + e]
+                           : __ldcg(p.part_o + (size_t)r1 * D + lane * VEC + e);
             }
             const float M = fmaxf(l0, l1);
             const float w0 = exp2f(l0 - M), w1 = exp2f(l1 - M);
@@ -1153,13 +1222,19 @@ __device__ __forceinline__ bool finish_item(const DecodeParams &p, const Item &i
         return false;
     if (!split)
         return true;
+    if (*c.merge == 2) {
+        // completes the unit (probe_split_last): own rows from shared memory, then a
+        // barrier before the next item may overwrite them
+        merge_split_unit<T, D>(p, it, warp, lane, pfx_s, c.macc, c.mml);
+        return consumer_sync(c, sph);
+    }
     if (threadIdx.x == 0) {
         // release: this CTA's partial rows (observed through the barrier above)
         // become visible before the count; acquire, only in the CTA that completes
         // the set: it then sees every other partial and passes that on through the
         // next barrier
         dev::fence_acq_rel_gpu();
-        const bool last = count_partial(p, it);
+        const bool last = count_partial(p, it, *c.ctr_seen);
         if (last)
             dev::fence_acq_rel_gpu();
         *c.merge = last ? 1 : 0;
@@ -1730,12 +1805,14 @@ __global__ void __launch_bounds__(kThreads, 2)
             }
             dev::cp_async_wait_all();
         }
+        if (threadIdx.x == 0)
+            probe_split_last(p, it, c);
         if (!consumer_sync(c, sph)) {
             if (lane == 0)
                 raise_error(p, c.abort, PA_DEVERR_TIMEOUT_FULL);
             break;
         }
-        finalize_item<T, D>(p, it, c.macc, c.mml, rows_cap, threadIdx.x, pfx_s);
+        finalize_item<T, D>(p, it, c.macc, c.mml, rows_cap, threadIdx.x, pfx_s, *c.merge == 2);
         if (!finish_item<T, D>(p, it, c, sph, warp, lane, pfx_s)) {
             if (lane == 0)
                 raise_error(p, c.abort, PA_DEVERR_TIMEOUT_FULL);
@@ -1989,6 +2066,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (threadIdx.x == 0)
             PA_TRACE_SET(12, t_m0);  // warp 0 done with the item's stages
 #endif
+        if (threadIdx.x == 0)
+            probe_split_last(p, it, c);
         if (!consumer_sync(c, sph)) {
             if (lane == 0)
                 raise_error(p, c.abort, PA_DEVERR_TIMEOUT_FULL);
@@ -1998,7 +2077,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (threadIdx.x == 0)
             PA_TRACE_SET(10, dev::global_timer_ns());  // all warps done
 #endif
-        finalize_item<float, D>(p, it, c.macc, c.mml, rows_cap, threadIdx.x, pfx_s);
+        finalize_item<float, D>(p, it, c.macc, c.mml, rows_cap, threadIdx.x, pfx_s,
+                                *c.merge == 2);
         if (!finish_item<float, D>(p, it, c, sph, warp, lane, pfx_s)) {
             if (lane == 0)
                 raise_error(p, c.abort, PA_DEVERR_TIMEOUT_FULL);

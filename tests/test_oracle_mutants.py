@@ -36,7 +36,8 @@ MUTANTS = {
 
 
 def _build_mutant(tmp_path, name, old, new):
-    text = open(SRC).read()
+    with open(SRC) as f:
+        text = f.read()
     assert text.count(old) == 1, f"mutation site for {name} not unique"
     path = tmp_path / f"{name}.c"
     path.write_text(text.replace(old, new))

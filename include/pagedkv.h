@@ -98,7 +98,9 @@ int pa_last_cuda_error(void);
  *          merged by a second kernel.
  * Both give the same result up to fp32 rounding order.  The workspace needs no
  * initialisation: the balanced split's merge counters are tagged with a
- * per-call epoch.
+ * per-call epoch, and a completed call leaves them at zero, so the replays of a
+ * captured CUDA graph (which reuse the captured epoch) each start clean.  After a
+ * device timeout (pa_device_errors), clear a graph's workspace before replaying.
  *
  * Arguments
  *   out            device, [S][Hq][d], dtype `dtype`, written

@@ -1030,7 +1030,10 @@ __device__ __forceinline__ void finalize_item(const DecodeParams &p, const Item 
 // fence and counts it on the unit's counter; the CTA whose count completes the set
 // takes an acquire fence and merges every partial with the log-sum-exp rule.  No CTA waits for
 // another.  Counters hold (epoch << 32 | count): a value left by an earlier call
-// carries another epoch and counts as zero, so they never need clearing.
+// carries another epoch and counts as zero, so they never need clearing.  The CTA
+// that completes a unit also resets its counter to zero, so a completed launch leaves
+// every counter it used at zero: the replays of a captured CUDA graph reuse one
+// epoch, and each starts from clean counters.
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ bool count_partial(const DecodeParams &p, const Item &it,
                                               unsigned long long old)
@@ -1045,7 +1048,10 @@ __device__ __forceinline__ bool count_partial(const DecodeParams &p, const Item 
             break;
         old = prev;
     }
-    return cnt + 1u == (unsigned int)it.nparts;
+    const bool last = cnt + 1u == (unsigned int)it.nparts;
+    if (last)  // every part is counted: no other CTA touches this counter again
+        *reinterpret_cast<volatile unsigned long long *>(ctr) = 0ull;
+    return last;
 }
 
 // Before the item's final barrier, thread 0 of a CTA holding one of the two parts of
@@ -1068,6 +1074,9 @@ __device__ __forceinline__ void probe_split_last(const DecodeParams &p, const It
         if (it.nparts == 2 && cnt == 1u) {
             dev::fence_acq_rel_gpu();
             early = 1;
+            // the other part is counted and this one never will be: reset for the
+            // next launch (see count_partial)
+            *reinterpret_cast<volatile unsigned long long *>(p.counters + it.c_first) = 0ull;
         }
     }
     *c.merge = early ? 2 : 0;

@@ -616,8 +616,9 @@ struct Producer {
 // with nb blocks costs kUnitCost + ceil(nb / bps) positions -- the fixed cost of an
 // item (descriptor, query rows, block-table lookup latency, merge) counted as
 // kUnitCost stages, then its real stages.  All units of all sequences, in order
-// (sequence, kv head, head group), form one stream of `total` positions; CTA c of
-// G takes positions [c * total / G, (c + 1) * total / G).
+// (sequence, kv head, head group) -- for the own blocks of a batch with shared
+// prefixes, (kv head, head group, sequence) -- form one stream of `total`
+// positions; CTA c of G takes positions [c * total / G, (c + 1) * total / G).
 // ---------------------------------------------------------------------------
 #ifndef PA_UNIT_COST
 #define PA_UNIT_COST 4
@@ -714,40 +715,48 @@ __device__ __forceinline__ long long warp_sum_ll(long long v)
     return v;
 }
 
-__device__ __forceinline__ long long seq_weight(const DecodeParams &p, int s, int bs, int bps)
-{
-    const SeqUnits u = seq_units(p, s, bs, bps);
-    return (long long)u.nunits * (kUnitCost + u.ns);
-}
-
-// Positions of the whole stream (every lane gets the value).
+// Positions of the whole stream (every lane gets the value).  With kPrefix,
+// *prefix tells whether some sequence's units start after shared leading blocks
+// (the own blocks of a batch with shared prefixes).
+template <bool kPrefix = false>
 __device__ __forceinline__ long long stream_total(const DecodeParams &p, int bs, int bps, int lane,
-                                                  long long *units = nullptr)
+                                                  long long *units = nullptr,
+                                                  bool *prefix = nullptr)
 {
     long long t = 0, n = 0;
+    bool pre = false;
     for (int s0 = 0; s0 < p.num_seqs; s0 += 32) {
         const int s = s0 + lane;
         if (s < p.num_seqs) {
             const SeqUnits u = seq_units(p, s, bs, bps);
             t += (long long)u.nunits * (kUnitCost + u.ns);
             n += u.nunits;
+            if (kPrefix)
+                pre |= u.start > 0;
         }
     }
     if (units)
         *units = warp_sum_ll(n);
+    if (kPrefix)
+        *prefix = __any_sync(0xffffffffu, pre);
     return warp_sum_ll(t);
 }
 
 // The sequence whose positions contain x (sequences without units have none);
-// num_seqs if x >= total.  *base_out gets the sequence's first position.
-// Warp-cooperative.
+// num_seqs if x >= total.  *base_out gets the sequence's first position.  With
+// one_unit, each sequence counts the positions of one of its units (a row of the
+// (unit, sequence) order).  Warp-cooperative.
 __device__ __forceinline__ int find_seq_at(const DecodeParams &p, int bs, int bps, long long x,
-                                           long long *base_out, int lane)
+                                           long long *base_out, int lane, bool one_unit = false)
 {
     long long base = 0;
     for (int s0 = 0; s0 < p.num_seqs; s0 += 32) {
         const int s = s0 + lane;
-        const long long w = (s < p.num_seqs) ? seq_weight(p, s, bs, bps) : 0;
+        long long w = 0;
+        if (s < p.num_seqs) {
+            const SeqUnits u = seq_units(p, s, bs, bps);
+            w = (one_unit ? 1ll : (long long)u.nunits) * (kUnitCost + u.ns);
+        }
         long long incl = w;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -799,6 +808,77 @@ __device__ __forceinline__ long long cta_of(long long x, long long total, long l
     return ((x + 1) * G - 1) / total;
 }
 
+// Emits unit u of sequence s (stream positions [a, a + kUnitCost + ns)) if its
+// real stages meet the CTA's range [s_c, e_c).  Returns false once the producer
+// aborted.
+template <class Prod>
+__device__ __forceinline__ bool emit_unit(const DecodeParams &p, Prod &pr, const SeqUnits &su,
+                                          int s, long long u, long long a, long long s_c,
+                                          long long e_c, long long total, long long G,
+                                          long long cta, int bps, int div)
+{
+    const long long ns = su.ns;
+    const long long ra = a + kUnitCost;  // first real stage
+    const long long rb = ra + ns;
+    Item it;
+    it.len = su.len;
+    it.total_lo = (unsigned int)(total & 0xffffffffll);
+    it.total_hi = (unsigned int)(total >> 32);
+    it.tseq = s;
+    if (p.pass == 1) {
+        const int mpi = members_per_item(p.group);
+        const int mg = (int)(u % su.mgroups);
+        const int members = min(mpi, su.members - mg * mpi);
+        it.seq = s + mg * mpi;
+        it.kvh = (int)(u / su.mgroups);
+        it.hg = 0;
+        it.qrow0 = it.kvh * p.group;
+        it.rows = members * p.group;
+        it.packed = pack_rows(members, p.group, kToPrefix);
+    } else {
+        it.seq = s;
+        it.kvh = (int)(u / p.head_groups);
+        it.hg = (int)(u % p.head_groups);
+        it.qrow0 = it.kvh * p.group + it.hg * kHeadsPerItem;
+        it.rows = min(kHeadsPerItem, p.group - it.hg * kHeadsPerItem);
+        it.packed = pack_rows(1, it.rows, su.start > 0 ? kMergePrefix : 0);
+    }
+    it.c_first = -1;
+    it.nparts = 0;
+    if (ns == 0) {
+        // an empty unit belongs to the CTA holding its start: zero rows (or the
+        // shared-prefix rows alone)
+        if (a < s_c)
+            return true;
+        it.j0 = it.j1 = su.start;
+        it.partial = 0;
+        it.prow0 = 0;
+    } else {
+        const long long lo = max(ra, s_c), hi = min(rb, e_c);
+        if (lo >= hi)
+            return true;
+        it.j0 = su.start + (int)((lo - ra) * bps);
+        it.j1 = (int)min(su.start + (hi - ra) * bps, (long long)su.nb);
+        it.partial = (lo == ra && hi == rb) ? 0 : 1;
+        // slot 2c: the unit's stages began in an earlier CTA; 2c + 1: they go on
+        it.prow0 = (int)((2 * cta + (ra < s_c ? 0 : 1)) * kHeadsPerItem);
+        if (it.partial) {
+            const long long cf = cta_of(ra, total, G);
+            const long long cl = cta_of(rb - 1, total, G);
+            int np = 1;
+            for (long long cc = cf + 1; cc <= cl; ++cc)
+                np += (cc * total / G < (cc + 1) * total / G) ? 1 : 0;
+            it.c_first = (int)cf;
+            it.nparts = np;
+        }
+    }
+    // consecutive items of a CTA start their warp rotation where the stream is
+    it.packed = (it.packed & ~(0x3f << 2)) | ((int)((ns == 0 ? a : max(ra, s_c)) & 3) << 2) |
+                (div << 4);
+    return pr.emit(it);
+}
+
+// Stream order (sequence, unit): every unit of a sequence, then the next sequence.
 template <class Prod>
 __device__ __forceinline__ bool walk_chunk(const DecodeParams &p, int bs, int bps, Prod &pr,
                                            int lane, long long total, long long G, long long cta,
@@ -814,88 +894,68 @@ __device__ __forceinline__ bool walk_chunk(const DecodeParams &p, int bs, int bp
         const SeqUnits su = seq_units(p, s, bs, bps);
         if (su.nunits == 0)
             continue;
-        const long long ns = su.ns;
-        const long long span = kUnitCost + ns;
-        Item it;
-        it.len = su.len;
-        it.total_lo = (unsigned int)(total & 0xffffffffll);
-        it.total_hi = (unsigned int)(total >> 32);
-        it.tseq = s;
+        const long long span = kUnitCost + su.ns;
         const long long u_lo = s_c > base ? (s_c - base) / span : 0;
         const long long u_hi = min((long long)su.nunits - 1, (e_c - 1 - base) / span);
-        for (long long u = u_lo; u <= u_hi; ++u) {
-            const long long a = base + u * span;  // unit start (its cost positions)
-            const long long ra = a + kUnitCost;   // first real stage
-            const long long rb = ra + ns;
-            if (p.pass == 1) {
-                const int mpi = members_per_item(p.group);
-                const int mg = (int)(u % su.mgroups);
-                const int members = min(mpi, su.members - mg * mpi);
-                it.seq = s + mg * mpi;
-                it.kvh = (int)(u / su.mgroups);
-                it.hg = 0;
-                it.qrow0 = it.kvh * p.group;
-                it.rows = members * p.group;
-                it.packed = pack_rows(members, p.group, kToPrefix);
-            } else {
-                it.seq = s;
-                it.kvh = (int)(u / p.head_groups);
-                it.hg = (int)(u % p.head_groups);
-                it.qrow0 = it.kvh * p.group + it.hg * kHeadsPerItem;
-                it.rows = min(kHeadsPerItem, p.group - it.hg * kHeadsPerItem);
-                it.packed = pack_rows(1, it.rows, su.start > 0 ? kMergePrefix : 0);
-            }
-            it.c_first = -1;
-            it.nparts = 0;
-            if (ns == 0) {
-                // an empty unit belongs to the CTA holding its start: zero rows (or the
-                // shared-prefix rows alone)
-                if (a < s_c)
-                    continue;
-                it.j0 = it.j1 = su.start;
-                it.partial = 0;
-                it.prow0 = 0;
-            } else {
-                const long long lo = max(ra, s_c), hi = min(rb, e_c);
-                if (lo >= hi)
-                    continue;
-                it.j0 = su.start + (int)((lo - ra) * bps);
-                it.j1 = (int)min(su.start + (hi - ra) * bps, (long long)su.nb);
-                it.partial = (lo == ra && hi == rb) ? 0 : 1;
-                // slot 2c: the unit's stages began in an earlier CTA; 2c + 1: they go on
-                it.prow0 = (int)((2 * cta + (ra < s_c ? 0 : 1)) * kHeadsPerItem);
-                if (it.partial) {
-                    const long long cf = cta_of(ra, total, G);
-                    const long long cl = cta_of(rb - 1, total, G);
-                    int np = 1;
-                    for (long long cc = cf + 1; cc <= cl; ++cc)
-                        np += (cc * total / G < (cc + 1) * total / G) ? 1 : 0;
-                    it.c_first = (int)cf;
-                    it.nparts = np;
-                }
-            }
-            // consecutive items of a CTA start their warp rotation where the stream is
-            it.packed = (it.packed & ~(0x3f << 2)) |
-                        ((int)((ns == 0 ? a : max(ra, s_c)) & 3) << 2) | (div << 4);
-            if (!pr.emit(it))
+        for (long long u = u_lo; u <= u_hi; ++u)
+            if (!emit_unit(p, pr, su, s, u, base + u * span, s_c, e_c, total, G, cta, bps, div))
                 return false;
-        }
         base += (long long)su.nunits * span;
     }
     return !*pr.c.abort;
 }
 
-// The producer's walk of the balanced split: CTA c streams positions
-// [c * total / G, (c + 1) * total / G).
+// Stream order (unit, sequence), for the own blocks of a batch with shared
+// prefixes (pass 0: every sequence has the same units): unit 0 of every sequence,
+// then unit 1 of every sequence, ...  A CTA's range then holds one unit of many
+// sequences, a mix of own-part lengths, instead of every unit of one or two
+// sequences: the per-unit charge misjudges short and long units in opposite
+// directions, and a mix averages that out where a run of alike units adds it up.
 template <class Prod>
+__device__ __forceinline__ bool walk_chunk_unit_major(const DecodeParams &p, int bs, int bps,
+                                                      Prod &pr, int lane, long long total,
+                                                      long long G, long long cta, int div)
+{
+    const long long s_c = cta * total / G;
+    const long long e_c = (cta + 1) * total / G;
+    if (s_c >= e_c)
+        return true;
+    const long long U = (long long)p.num_kv_heads * p.head_groups;
+    const long long W = total / U;  // positions of one unit of every sequence
+    long long u = s_c / W;
+    long long inner = 0;
+    int s = find_seq_at(p, bs, bps, s_c - u * W, &inner, lane, true);
+    long long base = u * W + inner;
+    for (; u < U && base < e_c && !*pr.c.abort; ++u, s = 0) {
+        for (; s < p.num_seqs && base < e_c; ++s) {
+            const SeqUnits su = seq_units(p, s, bs, bps);
+            if (!emit_unit(p, pr, su, s, u, base, s_c, e_c, total, G, cta, bps, div))
+                return false;
+            base += kUnitCost + su.ns;
+        }
+    }
+    return !*pr.c.abort;
+}
+
+// The producer's walk of the balanced split: CTA c streams positions
+// [c * total / G, (c + 1) * total / G).  kOwnPass: the kernel built for the own
+// blocks of the shared-prefix decode, which takes the (unit, sequence) order when
+// the batch has shared prefixes; the other kernels carry only the (sequence, unit)
+// walk (code they never run still costs the small decodes 1-2 us).
+template <bool kOwnPass, class Prod>
 __device__ __forceinline__ void walk_balanced(const DecodeParams &p, int bs, int bps, Prod &pr,
                                               int lane)
 {
     long long units = 0;
-    const long long total = stream_total(p, bs, bps, lane, &units);
+    bool prefix = false;
+    const long long total = stream_total<kOwnPass>(p, bs, bps, lane, &units, &prefix);
     const int div = balanced_divisor(total, units);
     const long long G = balanced_grid(total, div);
-    if ((long long)blockIdx.x < G)
+    if ((long long)blockIdx.x >= G)
+        return;
+    if (kOwnPass && prefix)
+        walk_chunk_unit_major(p, bs, bps, pr, lane, total, G, (long long)blockIdx.x, div);
+    else
         walk_chunk(p, bs, bps, pr, lane, total, G, (long long)blockIdx.x, div);
 }
 
@@ -912,13 +972,14 @@ __device__ __forceinline__ void walk_fixed(const DecodeParams &p, int bs, Prod &
     }
 }
 
-template <typename T, int D, int BS, int kBPS, int kChunks, int kTileBytes, int kStages>
+template <typename T, int D, int BS, int kBPS, int kChunks, int kTileBytes, int kStages,
+          bool kOwnPass>
 __device__ __forceinline__ void producer_loop(const DecodeParams &p, const CUtensorMap *tk,
                                               const CUtensorMap *tv, const CtaState &c, int lane)
 {
     Producer<T, D, BS, kBPS, kChunks, kTileBytes, kStages> pr(p, tk, tv, c, lane);
     if (p.balanced)
-        walk_balanced(p, BS, kBPS, pr, lane);
+        walk_balanced<kOwnPass>(p, BS, kBPS, pr, lane);
     else
         walk_fixed(p, BS, pr, lane);
     pr.finish();
@@ -1523,9 +1584,10 @@ __device__ __forceinline__ bool consume_item_n8(const DecodeParams &p, const Cta
 }
 
 // ---------------------------------------------------------------------------
-// fp16 / bf16 partition kernel: tensor-core consumers.
+// fp16 / bf16 partition kernel: tensor-core consumers.  kOwnPass: the instance
+// for the own blocks of the shared-prefix decode (its producer's walk).
 // ---------------------------------------------------------------------------
-template <typename T, int D, int BS, bool N8>
+template <typename T, int D, int BS, bool N8, bool kOwnPass>
 __global__ void __launch_bounds__(kThreads, 2)
     pa_decode_mma_kernel(const __grid_constant__ DecodeParams p,
                          const __grid_constant__ CUtensorMap tmap_k,
@@ -1553,8 +1615,8 @@ __global__ void __launch_bounds__(kThreads, 2)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     if (warp == kConsumerWarps) {
-        producer_loop<T, D, BS, C::kBPS, C::kChunks, C::kTileBytes, C::kStages>(p, &tmap_k, &tmap_v,
-                                                                              c, lane);
+        producer_loop<T, D, BS, C::kBPS, C::kChunks, C::kTileBytes, C::kStages, kOwnPass>(
+            p, &tmap_k, &tmap_v, c, lane);
         return;
     }
 
@@ -1850,7 +1912,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 // one row (multi-head attention) carries no predicated-off work for fifteen
 // others and keeps its state in registers.
 // ---------------------------------------------------------------------------
-template <int D, int BS, int H>
+template <int D, int BS, int H, bool kOwnPass>
 __global__ void __launch_bounds__(kThreads, 1)
     pa_decode_f32_kernel(const __grid_constant__ DecodeParams p,
                          const __grid_constant__ CUtensorMap tmap_k,
@@ -1877,8 +1939,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     if (warp == kConsumerWarps) {
-        producer_loop<float, D, BS, C::kBPS, C::kChunks, C::kTileBytes, C::kStages>(p, &tmap_k,
-                                                                                  &tmap_v, c, lane);
+        producer_loop<float, D, BS, C::kBPS, C::kChunks, C::kTileBytes, C::kStages, kOwnPass>(
+            p, &tmap_k, &tmap_v, c, lane);
         return;
     }
 
@@ -2173,26 +2235,44 @@ __global__ void __launch_bounds__(128)
 // ---------------------------------------------------------------------------
 // Launch helpers
 // ---------------------------------------------------------------------------
+// The own-block launch of the shared-prefix decode (it has its own kernel instance).
+inline bool own_blocks_pass(const DecodeParams &p)
+{
+    return p.pass == 0 && p.share != nullptr;
+}
+
 // Items of at most 8 query rows (group <= 8) take the transposed-product
 // consumers; wider items the 16-row form.
 template <typename T, int D, int BS>
 struct KernelOf {
-    static void *get(const DecodeParams &p)
+    template <bool kOwnPass>
+    static void *pick(const DecodeParams &p)
     {
         return p.group <= kNarrowRows
-                   ? reinterpret_cast<void *>(&pa_decode_mma_kernel<T, D, BS, true>)
-                   : reinterpret_cast<void *>(&pa_decode_mma_kernel<T, D, BS, false>);
+                   ? reinterpret_cast<void *>(&pa_decode_mma_kernel<T, D, BS, true, kOwnPass>)
+                   : reinterpret_cast<void *>(&pa_decode_mma_kernel<T, D, BS, false, kOwnPass>);
+    }
+    static void *get(const DecodeParams &p)
+    {
+        return own_blocks_pass(p) ? pick<true>(p) : pick<false>(p);
     }
 };
 template <int D, int BS>
 struct KernelOf<float, D, BS> {
     // by the launch's row capacity (its widest item)
-    static void *get(const DecodeParams &p)
+    template <bool kOwnPass>
+    static void *pick(const DecodeParams &p)
     {
         const int rows_cap = item_rows_cap(p);
-        return rows_cap <= 1   ? reinterpret_cast<void *>(&pa_decode_f32_kernel<D, BS, 1>)
-               : rows_cap <= 4 ? reinterpret_cast<void *>(&pa_decode_f32_kernel<D, BS, 4>)
-                               : reinterpret_cast<void *>(&pa_decode_f32_kernel<D, BS, kHeadsPerItem>);
+        return rows_cap <= 1
+                   ? reinterpret_cast<void *>(&pa_decode_f32_kernel<D, BS, 1, kOwnPass>)
+               : rows_cap <= 4
+                   ? reinterpret_cast<void *>(&pa_decode_f32_kernel<D, BS, 4, kOwnPass>)
+                   : reinterpret_cast<void *>(&pa_decode_f32_kernel<D, BS, kHeadsPerItem, kOwnPass>);
+    }
+    static void *get(const DecodeParams &p)
+    {
+        return own_blocks_pass(p) ? pick<true>(p) : pick<false>(p);
     }
 };
 

@@ -1,7 +1,9 @@
 """The balanced split-KV schedule, restated in Python (CPU only).
 
 The partition kernel's producer warps cut the concatenated stream of units
-(sequence, kv head, head group) into equal position ranges, one per CTA; a unit
+(sequence, kv head, head group) -- for the own blocks of a batch with shared
+prefixes, (kv head, head group, sequence) -- into equal position ranges, one per
+CTA; a unit
 costs UNIT_COST positions plus one per ring stage.  This model checks, for random
 length mixes and grid sizes, the properties the kernel relies on:
   * every block of every unit is streamed by exactly one CTA;
@@ -68,6 +70,57 @@ def walk_units(su, bps, G, cta):
     return items, total
 
 
+def walk_units_unit_major(su, bps, G, cta):
+    """The (unit, sequence) order of the own-block pass of a batch with shared
+    prefixes: unit 0 of every sequence, then unit 1, ...  Every sequence has the
+    same number of units there."""
+    nss = [(nb - start + bps - 1) // bps if n else 0 for (n, start, nb) in su]
+    U = su[0][0]
+    assert all(n == U for n, _, _ in su)
+    spans = [UNIT_COST + ns for ns in nss]
+    W = sum(spans)
+    total = U * W
+    s_c, e_c = cta * total // G, (cta + 1) * total // G
+    items = []
+    if s_c >= e_c:
+        return items, total
+    for u in range(s_c // W, U):
+        base = u * W
+        if base >= e_c:
+            break
+        for s, ((_, start, nb), ns) in enumerate(zip(su, nss)):
+            a = base
+            base += spans[s]
+            if a >= e_c:
+                break
+            ra, rb = a + UNIT_COST, a + UNIT_COST + ns
+            if ns == 0:
+                if s_c <= a < e_c:
+                    items.append((s, u, start, start, False, None, None, None))
+                continue
+            lo, hi = max(ra, s_c), min(rb, e_c)
+            if lo >= hi:
+                continue
+            partial = not (lo == ra and hi == rb)
+            slot = 2 * cta + (0 if ra < s_c else 1)
+            cf = nparts = None
+            if partial:
+                cf, cl = cta_of(ra, total, G), cta_of(rb - 1, total, G)
+                nparts = 1 + sum(1 for c in range(cf + 1, cl + 1)
+                                 if c * total // G < (c + 1) * total // G)
+            items.append((s, u, start + (lo - ra) * bps, min(start + (hi - ra) * bps, nb), partial,
+                          slot, cf, nparts))
+    return items, total
+
+
+def walk_pass(su, bps, G, cta):
+    """The kernel's choice: (unit, sequence) order once some unit starts after
+    shared leading blocks, else (sequence, unit)."""
+    if any(n and start > 0 for (n, start, _) in su):
+        return walk_units_unit_major(su, bps, G, cta)
+    return walk_units(su, bps, G, cta)
+
+
 def merge_slots(cf, nparts, total, G):
     slots, cc = [2 * cf + 1], cf
     for _ in range(nparts - 1):
@@ -78,10 +131,17 @@ def merge_slots(cf, nparts, total, G):
     return slots
 
 
-def check(lens, units, bs, bps, G):
+def check(lens, units, bs, bps, G, starts=None):
+    """starts[s]: first block of sequence s's units (shared leading blocks before
+    it), which selects the (unit, sequence) order; None: all 0."""
     cover, written, zero_owner, merges = {}, {}, {}, {}
     for c in range(G):
-        items, total = walk(lens, units, bs, bps, G, c)
+        if starts is None:
+            items, total = walk(lens, units, bs, bps, G, c)
+        else:
+            su = [(units, min(p, (t + bs - 1) // bs), (t + bs - 1) // bs)
+                  for t, p in zip(lens, starts)]
+            items, total = walk_pass(su, bps, G, c)
         for (s, u, j0, j1, partial, slot, cf, nparts) in items:
             if j0 == j1:
                 assert (s, u) not in zero_owner
@@ -96,10 +156,11 @@ def check(lens, units, bs, bps, G):
                 merges.setdefault((s, u), set()).add((cf, nparts))
     for s, t in enumerate(lens):
         nb = (t + bs - 1) // bs
+        first = 0 if starts is None else min(starts[s], nb)
         for u in range(units):
-            if nb == 0:
+            if nb == first:
                 assert (s, u) in zero_owner
-            for j in range(nb):
+            for j in range(first, nb):
                 assert (s, u, j) in cover, (s, u, j)
     for (s, u), sets in merges.items():
         assert len(sets) == 1, "CTAs disagree on the merge set"
@@ -118,6 +179,33 @@ def test_balanced_schedule_invariants(seed):
     bps = 32 // bs if rng.random() < 0.7 else 1
     G = rng.choice([1, 2, 7, 152, 304, 608])
     check(lens, units, bs, bps, G)
+
+
+@pytest.mark.parametrize("seed", range(40))
+def test_unit_major_schedule_invariants(seed):
+    """The own-block pass of a batch with shared prefixes: (unit, sequence) order."""
+    rng = random.Random(500 + seed)
+    S = rng.randint(1, 30)
+    lens = [rng.choice([0, 1, 5, 16, 17, 33, 100, 700, 3000]) for _ in range(S)]
+    bs = rng.choice([16, 32])
+    starts = [rng.choice([0, 0, 1, 2, 40]) for _ in range(S)]
+    starts[rng.randrange(S)] = 1 + rng.randrange(3)
+    units = rng.choice([1, 2, 8, 40])
+    bps = 32 // bs if rng.random() < 0.7 else 1
+    G = rng.choice([1, 2, 7, 152, 304, 608])
+    check(lens, units, bs, bps, G, starts)
+
+
+def test_unit_major_gives_each_cta_a_mix_of_sequences():
+    # 128 sequences x 40 units of own parts of 0 .. 16 stages over 304 CTAs: in
+    # (sequence, unit) order a CTA sees one or two sequences, in (unit, sequence)
+    # order about 17
+    lens = [1024 + (i * 37) % 513 for i in range(128)]
+    su = [(40, 64, (t + 15) // 16) for t in lens]
+    seq_major = [len({it[0] for it in walk_units(su, 2, 304, c)[0]}) for c in range(304)]
+    unit_major = [len({it[0] for it in walk_pass(su, 2, 304, c)[0]}) for c in range(304)]
+    assert max(seq_major) <= 3
+    assert min(unit_major) >= 10
 
 
 def test_single_long_sequence_spreads_over_every_cta():
@@ -187,7 +275,7 @@ def check_shared(lens, share, Hkv, group, bs, bps, G):
     for pass_ in (1, 0):
         su = shared_units(lens, share, Hkv, group, bs, pass_)
         for c in range(G):
-            items, _ = walk_units(su, bps, G, c)
+            items, _ = walk_pass(su, bps, G, c)
             for (s, u, j0, j1, _, _, _, _) in items:
                 rows = rows_of(pass_, s, u, share, lens, Hkv, group)
                 # the kernel sizes an item's accumulators for this many rows

@@ -245,6 +245,13 @@ __device__ __forceinline__ bool find_item(const DecodeParams &p, int bs, long lo
 constexpr int kToPrefix = 1;     // result rows go to the shared-prefix buffer
 constexpr int kMergePrefix = 2;  // result rows are merged with the shared-prefix buffer
 
+// Kernel instances by launch: a plain decode carries no shared-prefix code (code
+// it never runs still costs a small decode ~2 us); the shared-prefix decode's two
+// launches each have their own.
+constexpr int kModePlain = 0;   // pa_decode, pa_decode_append
+constexpr int kModePrefix = 1;  // shared-prefix decode, pass 1: the groups' shared blocks
+constexpr int kModeOwn = 2;     // shared-prefix decode, pass 0: every sequence's own blocks
+
 // A work item: blocks [j0, j1) of one unit.  Row r of the item is query head
 // qrow0 + r % rpm of sequence seq + r / rpm (several sequences only in the
 // shared-prefix pass, where the rows of `members` sequences share one kv head).
@@ -642,12 +649,13 @@ struct SeqUnits {
     int mgroups;  // pass 1: member groups per kv head
 };
 
+template <bool kShare>
 __device__ __forceinline__ SeqUnits seq_units(const DecodeParams &p, int s, int bs, int bps)
 {
     // Every entry of the sequence the walk may need is loaded before any is tested,
     // so that the loads are in flight together: one memory round trip per batch of
     // sequences rather than one per test (length, group, prefix length, members).
-    const bool grouped = p.share != nullptr && p.group <= kHeadsPerItem;
+    const bool grouped = kShare && p.share != nullptr && p.group <= kHeadsPerItem;
     const bool members = grouped && p.pass == 1;
     const int t = p.context_lens[s];
     const int lead = grouped ? p.share[2 * s] : -1;
@@ -664,7 +672,7 @@ __device__ __forceinline__ SeqUnits seq_units(const DecodeParams &p, int s, int 
     SeqUnits u;
     u.members = 1;
     u.mgroups = 1;
-    if (p.pass == 1) {
+    if (kShare && p.pass == 1) {
         u.nunits = 0;
         u.ns = 0;
         u.start = 0;
@@ -718,7 +726,7 @@ __device__ __forceinline__ long long warp_sum_ll(long long v)
 // Positions of the whole stream (every lane gets the value).  With kPrefix,
 // *prefix tells whether some sequence's units start after shared leading blocks
 // (the own blocks of a batch with shared prefixes).
-template <bool kPrefix = false>
+template <bool kShare, bool kPrefix>
 __device__ __forceinline__ long long stream_total(const DecodeParams &p, int bs, int bps, int lane,
                                                   long long *units = nullptr,
                                                   bool *prefix = nullptr)
@@ -728,7 +736,7 @@ __device__ __forceinline__ long long stream_total(const DecodeParams &p, int bs,
     for (int s0 = 0; s0 < p.num_seqs; s0 += 32) {
         const int s = s0 + lane;
         if (s < p.num_seqs) {
-            const SeqUnits u = seq_units(p, s, bs, bps);
+            const SeqUnits u = seq_units<kShare>(p, s, bs, bps);
             t += (long long)u.nunits * (kUnitCost + u.ns);
             n += u.nunits;
             if (kPrefix)
@@ -746,6 +754,7 @@ __device__ __forceinline__ long long stream_total(const DecodeParams &p, int bs,
 // num_seqs if x >= total.  *base_out gets the sequence's first position.  With
 // one_unit, each sequence counts the positions of one of its units (a row of the
 // (unit, sequence) order).  Warp-cooperative.
+template <bool kShare>
 __device__ __forceinline__ int find_seq_at(const DecodeParams &p, int bs, int bps, long long x,
                                            long long *base_out, int lane, bool one_unit = false)
 {
@@ -754,7 +763,7 @@ __device__ __forceinline__ int find_seq_at(const DecodeParams &p, int bs, int bp
         const int s = s0 + lane;
         long long w = 0;
         if (s < p.num_seqs) {
-            const SeqUnits u = seq_units(p, s, bs, bps);
+            const SeqUnits u = seq_units<kShare>(p, s, bs, bps);
             w = (one_unit ? 1ll : (long long)u.nunits) * (kUnitCost + u.ns);
         }
         long long incl = w;
@@ -811,7 +820,7 @@ __device__ __forceinline__ long long cta_of(long long x, long long total, long l
 // Emits unit u of sequence s (stream positions [a, a + kUnitCost + ns)) if its
 // real stages meet the CTA's range [s_c, e_c).  Returns false once the producer
 // aborted.
-template <class Prod>
+template <bool kShare, class Prod>
 __device__ __forceinline__ bool emit_unit(const DecodeParams &p, Prod &pr, const SeqUnits &su,
                                           int s, long long u, long long a, long long s_c,
                                           long long e_c, long long total, long long G,
@@ -825,7 +834,7 @@ __device__ __forceinline__ bool emit_unit(const DecodeParams &p, Prod &pr, const
     it.total_lo = (unsigned int)(total & 0xffffffffll);
     it.total_hi = (unsigned int)(total >> 32);
     it.tseq = s;
-    if (p.pass == 1) {
+    if (kShare && p.pass == 1) {
         const int mpi = members_per_item(p.group);
         const int mg = (int)(u % su.mgroups);
         const int members = min(mpi, su.members - mg * mpi);
@@ -841,7 +850,7 @@ __device__ __forceinline__ bool emit_unit(const DecodeParams &p, Prod &pr, const
         it.hg = (int)(u % p.head_groups);
         it.qrow0 = it.kvh * p.group + it.hg * kHeadsPerItem;
         it.rows = min(kHeadsPerItem, p.group - it.hg * kHeadsPerItem);
-        it.packed = pack_rows(1, it.rows, su.start > 0 ? kMergePrefix : 0);
+        it.packed = pack_rows(1, it.rows, kShare && su.start > 0 ? kMergePrefix : 0);
     }
     it.c_first = -1;
     it.nparts = 0;
@@ -879,7 +888,7 @@ __device__ __forceinline__ bool emit_unit(const DecodeParams &p, Prod &pr, const
 }
 
 // Stream order (sequence, unit): every unit of a sequence, then the next sequence.
-template <class Prod>
+template <bool kShare, class Prod>
 __device__ __forceinline__ bool walk_chunk(const DecodeParams &p, int bs, int bps, Prod &pr,
                                            int lane, long long total, long long G, long long cta,
                                            int div)
@@ -889,16 +898,17 @@ __device__ __forceinline__ bool walk_chunk(const DecodeParams &p, int bs, int bp
     if (s_c >= e_c)
         return true;
     long long base = 0;
-    int s = find_seq_at(p, bs, bps, s_c, &base, lane);
+    int s = find_seq_at<kShare>(p, bs, bps, s_c, &base, lane);
     for (; s < p.num_seqs && base < e_c && !*pr.c.abort; ++s) {
-        const SeqUnits su = seq_units(p, s, bs, bps);
+        const SeqUnits su = seq_units<kShare>(p, s, bs, bps);
         if (su.nunits == 0)
             continue;
         const long long span = kUnitCost + su.ns;
         const long long u_lo = s_c > base ? (s_c - base) / span : 0;
         const long long u_hi = min((long long)su.nunits - 1, (e_c - 1 - base) / span);
         for (long long u = u_lo; u <= u_hi; ++u)
-            if (!emit_unit(p, pr, su, s, u, base + u * span, s_c, e_c, total, G, cta, bps, div))
+            if (!emit_unit<kShare>(p, pr, su, s, u, base + u * span, s_c, e_c, total, G, cta, bps,
+                                   div))
                 return false;
         base += (long long)su.nunits * span;
     }
@@ -924,12 +934,12 @@ __device__ __forceinline__ bool walk_chunk_unit_major(const DecodeParams &p, int
     const long long W = total / U;  // positions of one unit of every sequence
     long long u = s_c / W;
     long long inner = 0;
-    int s = find_seq_at(p, bs, bps, s_c - u * W, &inner, lane, true);
+    int s = find_seq_at<true>(p, bs, bps, s_c - u * W, &inner, lane, true);
     long long base = u * W + inner;
     for (; u < U && base < e_c && !*pr.c.abort; ++u, s = 0) {
         for (; s < p.num_seqs && base < e_c; ++s) {
-            const SeqUnits su = seq_units(p, s, bs, bps);
-            if (!emit_unit(p, pr, su, s, u, base, s_c, e_c, total, G, cta, bps, div))
+            const SeqUnits su = seq_units<true>(p, s, bs, bps);
+            if (!emit_unit<true>(p, pr, su, s, u, base, s_c, e_c, total, G, cta, bps, div))
                 return false;
             base += kUnitCost + su.ns;
         }
@@ -938,25 +948,25 @@ __device__ __forceinline__ bool walk_chunk_unit_major(const DecodeParams &p, int
 }
 
 // The producer's walk of the balanced split: CTA c streams positions
-// [c * total / G, (c + 1) * total / G).  kOwnPass: the kernel built for the own
-// blocks of the shared-prefix decode, which takes the (unit, sequence) order when
-// the batch has shared prefixes; the other kernels carry only the (sequence, unit)
-// walk (code they never run still costs the small decodes 1-2 us).
-template <bool kOwnPass, class Prod>
+// [c * total / G, (c + 1) * total / G).  The own-block launch of the shared-prefix
+// decode takes the (unit, sequence) order when the batch has shared prefixes.
+template <int kMode, class Prod>
 __device__ __forceinline__ void walk_balanced(const DecodeParams &p, int bs, int bps, Prod &pr,
                                               int lane)
 {
+    constexpr bool kShare = kMode != kModePlain;
+    constexpr bool kOwn = kMode == kModeOwn;
     long long units = 0;
     bool prefix = false;
-    const long long total = stream_total<kOwnPass>(p, bs, bps, lane, &units, &prefix);
+    const long long total = stream_total<kShare, kOwn>(p, bs, bps, lane, &units, &prefix);
     const int div = balanced_divisor(total, units);
     const long long G = balanced_grid(total, div);
     if ((long long)blockIdx.x >= G)
         return;
-    if (kOwnPass && prefix)
+    if (kOwn && prefix)
         walk_chunk_unit_major(p, bs, bps, pr, lane, total, G, (long long)blockIdx.x, div);
     else
-        walk_chunk(p, bs, bps, pr, lane, total, G, (long long)blockIdx.x, div);
+        walk_chunk<kShare>(p, bs, bps, pr, lane, total, G, (long long)blockIdx.x, div);
 }
 
 template <class Prod>
@@ -973,13 +983,13 @@ __device__ __forceinline__ void walk_fixed(const DecodeParams &p, int bs, Prod &
 }
 
 template <typename T, int D, int BS, int kBPS, int kChunks, int kTileBytes, int kStages,
-          bool kOwnPass>
+          int kMode>
 __device__ __forceinline__ void producer_loop(const DecodeParams &p, const CUtensorMap *tk,
                                               const CUtensorMap *tv, const CtaState &c, int lane)
 {
     Producer<T, D, BS, kBPS, kChunks, kTileBytes, kStages> pr(p, tk, tv, c, lane);
     if (p.balanced)
-        walk_balanced<kOwnPass>(p, BS, kBPS, pr, lane);
+        walk_balanced<kMode>(p, BS, kBPS, pr, lane);
     else
         walk_fixed(p, BS, pr, lane);
     pr.finish();
@@ -991,7 +1001,7 @@ __device__ __forceinline__ void producer_loop(const DecodeParams &p, const CUten
 // (prefix pass), or is first merged with the shared-prefix row by the
 // log-sum-exp rule (own blocks of a grouped sequence).
 // ---------------------------------------------------------------------------
-template <typename T, int D>
+template <typename T, int D, bool kShare>
 __device__ __forceinline__ void store_result(const DecodeParams &p, const Item &it, int r, int col,
                                              float o, float lse, const float *pfx_s)
 {
@@ -999,13 +1009,13 @@ __device__ __forceinline__ void store_result(const DecodeParams &p, const Item &
     const int rpm = it.rpm();
     const size_t row = (size_t)(it.seq + r / rpm) * p.num_q_heads + it.qrow0 + r % rpm;
     const int f = it.flags();
-    if (f & kToPrefix) {
+    if (kShare && (f & kToPrefix)) {
         p.pfx[row * PS + col] = o;
         if (col == 0)
             p.pfx[row * PS + D] = lse;
         return;
     }
-    if (f & kMergePrefix) {
+    if (kShare && (f & kMergePrefix)) {
         // the item's prefix rows, staged in shared memory when the item started
         const float lp = pfx_s[r * PS + D];
         const float m2 = fmaxf(lse, lp);
@@ -1037,7 +1047,7 @@ __device__ __forceinline__ void stage_prefix(const DecodeParams &p, const Item &
 // ---------------------------------------------------------------------------
 // Merge the four consumer states of one item and store it.
 // ---------------------------------------------------------------------------
-template <typename T, int D>
+template <typename T, int D, bool kShare>
 __device__ __forceinline__ void finalize_item(const DecodeParams &p, const Item &it, float *acc,
                                               const float *ml, int rows_cap, int tid,
                                               const float *pfx_s, bool own_in_smem)
@@ -1070,7 +1080,8 @@ __device__ __forceinline__ void finalize_item(const DecodeParams &p, const Item 
         }
         const float o = (L > 0.f) ? O / L : 0.f;
         if (!it.partial) {
-            store_result<T, D>(p, it, r, col, o, (L > 0.f) ? M + log2f(L) : -INFINITY, pfx_s);
+            store_result<T, D, kShare>(p, it, r, col, o, (L > 0.f) ? M + log2f(L) : -INFINITY,
+                                       pfx_s);
         } else if (own_in_smem) {
             // this CTA completes the unit now: its rows stay here, in the first warp's
             // accumulator rows (each element read, then written, by this thread alone);
@@ -1190,7 +1201,7 @@ __device__ __forceinline__ long long split_slot(const Item &it, int i, long long
 // own_o: this CTA's own rows (row stride D + kAccPad) when it completes a unit cut
 // once early (probe_split_last), with their log2-sum-exp from own_ml; null when its
 // part went through the partial slots.
-template <typename T, int D>
+template <typename T, int D, bool kShare>
 __device__ __forceinline__ void merge_split_unit(const DecodeParams &p, const Item &it, int warp,
                                               int lane, const float *pfx_s,
                                               const float *own_o = nullptr,
@@ -1224,8 +1235,8 @@ __device__ __forceinline__ void merge_split_unit(const DecodeParams &p, const It
             const float lse = M + log2f(W);
 #pragma unroll
             for (int e = 0; e < VEC; ++e)
-                store_result<T, D>(p, it, r, lane * VEC + e, (w0 * v0[e] + w1 * v1[e]) / W, lse,
-                                   pfx_s);
+                store_result<T, D, kShare>(p, it, r, lane * VEC + e,
+                                           (w0 * v0[e] + w1 * v1[e]) / W, lse, pfx_s);
             continue;
         }
         float M = -INFINITY;
@@ -1273,7 +1284,7 @@ __device__ __forceinline__ void merge_split_unit(const DecodeParams &p, const It
         const float lse = M + log2f(W);
 #pragma unroll
         for (int e = 0; e < VEC; ++e)
-            store_result<T, D>(p, it, r, lane * VEC + e, acc[e] / W, lse, pfx_s);
+            store_result<T, D, kShare>(p, it, r, lane * VEC + e, acc[e] / W, lse, pfx_s);
     }
 }
 
@@ -1283,7 +1294,7 @@ __device__ __forceinline__ void merge_split_unit(const DecodeParams &p, const It
 // count (fences are cumulative over what thread 0 has observed); the merging CTA's
 // acquire fence, then the next barrier, let all its threads see the other partials.
 // False on a timeout.
-template <typename T, int D>
+template <typename T, int D, bool kShare>
 __device__ __forceinline__ bool finish_item(const DecodeParams &p, const Item &it, const CtaState &c,
                                             uint32_t &sph, int warp, int lane, const float *pfx_s)
 {
@@ -1295,7 +1306,7 @@ __device__ __forceinline__ bool finish_item(const DecodeParams &p, const Item &i
     if (*c.merge == 2) {
         // completes the unit (probe_split_last): own rows from shared memory, then a
         // barrier before the next item may overwrite them
-        merge_split_unit<T, D>(p, it, warp, lane, pfx_s, c.macc, c.mml);
+        merge_split_unit<T, D, kShare>(p, it, warp, lane, pfx_s, c.macc, c.mml);
         return consumer_sync(c, sph);
     }
     if (threadIdx.x == 0) {
@@ -1312,7 +1323,7 @@ __device__ __forceinline__ bool finish_item(const DecodeParams &p, const Item &i
     if (!consumer_sync(c, sph))
         return false;
     if (*c.merge)
-        merge_split_unit<T, D>(p, it, warp, lane, pfx_s);
+        merge_split_unit<T, D, kShare>(p, it, warp, lane, pfx_s);
     return true;
 }
 
@@ -1584,10 +1595,10 @@ __device__ __forceinline__ bool consume_item_n8(const DecodeParams &p, const Cta
 }
 
 // ---------------------------------------------------------------------------
-// fp16 / bf16 partition kernel: tensor-core consumers.  kOwnPass: the instance
-// for the own blocks of the shared-prefix decode (its producer's walk).
+// fp16 / bf16 partition kernel: tensor-core consumers.  kMode: the launch it is
+// built for (kModePlain, kModePrefix, kModeOwn).
 // ---------------------------------------------------------------------------
-template <typename T, int D, int BS, bool N8, bool kOwnPass>
+template <typename T, int D, int BS, bool N8, int kMode>
 __global__ void __launch_bounds__(kThreads, 2)
     pa_decode_mma_kernel(const __grid_constant__ DecodeParams p,
                          const __grid_constant__ CUtensorMap tmap_k,
@@ -1606,7 +1617,8 @@ __global__ void __launch_bounds__(kThreads, 2)
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int rows_cap = item_rows_cap(p);
-    const int pfx_rows = item_pfx_rows(p);
+    constexpr bool kShare = kMode != kModePlain;
+    const int pfx_rows = kShare ? item_pfx_rows(p) : 0;
     const SmemLayout lay =
         make_layout(C::kStages, C::kStageBytes, rows_cap, D, sizeof(T), pfx_rows);
     const CtaState c = cta_state(smem, lay, C::kStages);
@@ -1615,7 +1627,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     if (warp == kConsumerWarps) {
-        producer_loop<T, D, BS, C::kBPS, C::kChunks, C::kTileBytes, C::kStages, kOwnPass>(
+        producer_loop<T, D, BS, C::kBPS, C::kChunks, C::kTileBytes, C::kStages, kMode>(
             p, &tmap_k, &tmap_v, c, lane);
         return;
     }
@@ -1636,7 +1648,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
     bool first_tile = true;
 #endif
-    bool pfx_ready = !defers_dependency(p);  // prefix rows may be read
+    bool pfx_ready = !kShare || !defers_dependency(p);  // prefix rows may be read
     for (uint32_t n = 0;; ++n) {
         const uint32_t slot = n % kItemSlots;
 #ifdef PA_TRACE
@@ -1654,7 +1666,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         const Item it = load_item(&c.items[slot]);
         if (it.seq < 0)
             break;
-        const bool merge_pfx = (it.flags() & kMergePrefix) != 0;
+        const bool merge_pfx = kShare && (it.flags() & kMergePrefix) != 0;
         float *pfx_s = c.pfx + (n & 1) * pfx_rows * (D + kPfxPad);
         if (merge_pfx && pfx_ready)
             stage_prefix<D>(p, it, pfx_s, threadIdx.x);
@@ -1883,8 +1895,8 @@ __global__ void __launch_bounds__(kThreads, 2)
                 raise_error(p, c.abort, PA_DEVERR_TIMEOUT_FULL);
             break;
         }
-        finalize_item<T, D>(p, it, c.macc, c.mml, rows_cap, threadIdx.x, pfx_s, *c.merge == 2);
-        if (!finish_item<T, D>(p, it, c, sph, warp, lane, pfx_s)) {
+        finalize_item<T, D, kShare>(p, it, c.macc, c.mml, rows_cap, threadIdx.x, pfx_s, *c.merge == 2);
+        if (!finish_item<T, D, kShare>(p, it, c, sph, warp, lane, pfx_s)) {
             if (lane == 0)
                 raise_error(p, c.abort, PA_DEVERR_TIMEOUT_FULL);
             break;
@@ -1912,7 +1924,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 // one row (multi-head attention) carries no predicated-off work for fifteen
 // others and keeps its state in registers.
 // ---------------------------------------------------------------------------
-template <int D, int BS, int H, bool kOwnPass>
+template <int D, int BS, int H, int kMode>
 __global__ void __launch_bounds__(kThreads, 1)
     pa_decode_f32_kernel(const __grid_constant__ DecodeParams p,
                          const __grid_constant__ CUtensorMap tmap_k,
@@ -1930,7 +1942,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int rows_cap = item_rows_cap(p);
-    const int pfx_rows = item_pfx_rows(p);
+    constexpr bool kShare = kMode != kModePlain;
+    const int pfx_rows = kShare ? item_pfx_rows(p) : 0;
     const SmemLayout lay =
         make_layout(C::kStages, C::kStageBytes, rows_cap, D, sizeof(float), pfx_rows);
     const CtaState c = cta_state(smem, lay, C::kStages);
@@ -1939,7 +1952,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     if (warp == kConsumerWarps) {
-        producer_loop<float, D, BS, C::kBPS, C::kChunks, C::kTileBytes, C::kStages, kOwnPass>(
+        producer_loop<float, D, BS, C::kBPS, C::kChunks, C::kTileBytes, C::kStages, kMode>(
             p, &tmap_k, &tmap_v, c, lane);
         return;
     }
@@ -1956,7 +1969,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         PA_TRACE_SET(8, smid);
     }
 #endif
-    bool pfx_ready = !defers_dependency(p);  // prefix rows may be read
+    bool pfx_ready = !kShare || !defers_dependency(p);  // prefix rows may be read
     for (uint32_t n = 0;; ++n) {
         const uint32_t slot = n % kItemSlots;
         if (!warp_wait(&c.item_full[slot], (n / kItemSlots) & 1u)) {
@@ -1967,7 +1980,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const Item it = load_item(&c.items[slot]);
         if (it.seq < 0)
             break;
-        const bool merge_pfx = (it.flags() & kMergePrefix) != 0;
+        const bool merge_pfx = kShare && (it.flags() & kMergePrefix) != 0;
         float *pfx_s = c.pfx + (n & 1) * pfx_rows * (D + kPfxPad);
         if (merge_pfx && pfx_ready)
             stage_prefix<D>(p, it, pfx_s, threadIdx.x);
@@ -2148,9 +2161,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (threadIdx.x == 0)
             PA_TRACE_SET(10, dev::global_timer_ns());  // all warps done
 #endif
-        finalize_item<float, D>(p, it, c.macc, c.mml, rows_cap, threadIdx.x, pfx_s,
+        finalize_item<float, D, kShare>(p, it, c.macc, c.mml, rows_cap, threadIdx.x, pfx_s,
                                 *c.merge == 2);
-        if (!finish_item<float, D>(p, it, c, sph, warp, lane, pfx_s)) {
+        if (!finish_item<float, D, kShare>(p, it, c, sph, warp, lane, pfx_s)) {
             if (lane == 0)
                 raise_error(p, c.abort, PA_DEVERR_TIMEOUT_FULL);
             break;
@@ -2235,44 +2248,53 @@ __global__ void __launch_bounds__(128)
 // ---------------------------------------------------------------------------
 // Launch helpers
 // ---------------------------------------------------------------------------
-// The own-block launch of the shared-prefix decode (it has its own kernel instance).
-inline bool own_blocks_pass(const DecodeParams &p)
+// The kernel instance a launch takes: plain decode, or one of the shared-prefix
+// decode's two launches.
+inline int launch_mode(const DecodeParams &p)
 {
-    return p.pass == 0 && p.share != nullptr;
+    if (p.share == nullptr)
+        return kModePlain;
+    return p.pass == 1 ? kModePrefix : kModeOwn;
 }
 
 // Items of at most 8 query rows (group <= 8) take the transposed-product
 // consumers; wider items the 16-row form.
 template <typename T, int D, int BS>
 struct KernelOf {
-    template <bool kOwnPass>
+    template <int kMode>
     static void *pick(const DecodeParams &p)
     {
         return p.group <= kNarrowRows
-                   ? reinterpret_cast<void *>(&pa_decode_mma_kernel<T, D, BS, true, kOwnPass>)
-                   : reinterpret_cast<void *>(&pa_decode_mma_kernel<T, D, BS, false, kOwnPass>);
+                   ? reinterpret_cast<void *>(&pa_decode_mma_kernel<T, D, BS, true, kMode>)
+                   : reinterpret_cast<void *>(&pa_decode_mma_kernel<T, D, BS, false, kMode>);
     }
     static void *get(const DecodeParams &p)
     {
-        return own_blocks_pass(p) ? pick<true>(p) : pick<false>(p);
+        const int mode = launch_mode(p);
+        return mode == kModeOwn ? pick<kModeOwn>(p)
+               : mode == kModePrefix ? pick<kModePrefix>(p)
+                                     : pick<kModePlain>(p);
     }
 };
 template <int D, int BS>
 struct KernelOf<float, D, BS> {
     // by the launch's row capacity (its widest item)
-    template <bool kOwnPass>
+    template <int kMode>
     static void *pick(const DecodeParams &p)
     {
         const int rows_cap = item_rows_cap(p);
         return rows_cap <= 1
-                   ? reinterpret_cast<void *>(&pa_decode_f32_kernel<D, BS, 1, kOwnPass>)
+                   ? reinterpret_cast<void *>(&pa_decode_f32_kernel<D, BS, 1, kMode>)
                : rows_cap <= 4
-                   ? reinterpret_cast<void *>(&pa_decode_f32_kernel<D, BS, 4, kOwnPass>)
-                   : reinterpret_cast<void *>(&pa_decode_f32_kernel<D, BS, kHeadsPerItem, kOwnPass>);
+                   ? reinterpret_cast<void *>(&pa_decode_f32_kernel<D, BS, 4, kMode>)
+                   : reinterpret_cast<void *>(&pa_decode_f32_kernel<D, BS, kHeadsPerItem, kMode>);
     }
     static void *get(const DecodeParams &p)
     {
-        return own_blocks_pass(p) ? pick<true>(p) : pick<false>(p);
+        const int mode = launch_mode(p);
+        return mode == kModeOwn ? pick<kModeOwn>(p)
+               : mode == kModePrefix ? pick<kModePrefix>(p)
+                                     : pick<kModePlain>(p);
     }
 };
 

@@ -110,13 +110,13 @@ def test_mha_fp16():
 
 
 def test_gqa_bf16():
-    _check_workload(W.gqa_bf16(), sample=_sample(16, 3))
+    _check_workload(W.gqa_bf16())
 
 
 @pytest.mark.parametrize("shared", [False, True])
 @pytest.mark.parametrize("prompt", [1024, 1032])
 def test_shared_prefix_fp16(prompt, shared):
-    _check_workload(W.shared_prefix_fp16(prompt_len=prompt), sample=_sample(24, 4), shared=shared)
+    _check_workload(W.shared_prefix_fp16(prompt_len=prompt), shared=shared)
 
 
 def test_long_multiturn_bf16():
@@ -131,7 +131,8 @@ def test_long_multiturn_bf16():
     bt, cl = runner.tables_for(alloc, w.decode_seqs)
     obt, ocl = oracle.tables_for(oalloc, w.decode_seqs)
     assert np.array_equal(bt, obt) and np.array_equal(cl, ocl)
-    seqs = _sample(30, 5)(cl)
+    seqs = _sample(32, 5)(cl)      # at least 32 sequences, the longest among them
+    assert len(seqs) >= 32 and int(np.argmax(cl)) in seqs
     used = sorted({int(b) for s in seqs for b in obt[s, :(ocl[s] + w.block_size - 1) // w.block_size]})
     remap = {b: i for i, b in enumerate(used)}
     idx = torch.tensor(used, dtype=torch.long, device=DEV)

@@ -91,6 +91,9 @@ CASES = [
     ("f16", 128, 16, 40, 40, [(lens_for(8, 8, 16, 13), 8)] * 2 + [([17, 1], 0)]),
     ("bf16", 128, 16, 8, 1, [(lens_for(2, 3000, 16, 14), 3000)]),                   # long prefix over many CTAs
     ("f32", 128, 16, 8, 8, [([16 * 3 + 1, 16 * 3 + 1], 3)]),                          # own part = 1 token
+    # 322 sequences: the own-block launch's (kv head, sequence) walk over many batches
+    # of 32 sequences, with own parts of 1 to 48 tokens
+    ("f16", 64, 16, 4, 4, [(lens_for(8, 2, 16, 100 + i), 2) for i in range(40)] + [([5, 70], 0)]),
 ]
 
 

@@ -7,7 +7,11 @@ tokens' K/V append fused with the decode attention (pa_decode_append: append +
 partition kernel with the split-KV merge inside), on inputs already resident in
 HBM.  The workload's allocator script (untimed) prepares the caches and tables.
 The split is the balanced one (partition_size 0) unless --partition-size says
-otherwise.
+otherwise.  The default workload is the long-context multi-turn batch (256
+sequences, 32 q / 8 kv heads, bf16, block size 32, contexts log-uniform in
+[128, 131072], 20.6 GB of unique K/V per step): the largest configuration that
+fits one GPU.  The step time reported is the median of the timed steps (the mean
+is reported beside it).
 
 Metric: KV GB/s (algorithmic bytes of the step / device time of the step); the
 line also carries seq*layers/s (one pa_decode call = one layer), the roofline of
@@ -21,6 +25,10 @@ cold, clean L2.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
   python bench.py --impl reference ...     (the fp64 CPU oracle on the host cores)
+
+With --gpus N > 1 outside torchrun, the script starts N ranks itself (one per GPU,
+torch.distributed.run on 127.0.0.1) and rank 0 prints the line; every rank decodes
+its own batch (replicas, no collective on the data path).
 """
 from __future__ import annotations
 
@@ -37,7 +45,7 @@ import time
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-DEFAULT_WORKLOAD = "mha_fp16"
+DEFAULT_WORKLOAD = "long_multiturn_bf16"
 METRIC = "paged decode attention KV GB/s and % of GB300 HBM peak; seq-layers/s at 1 GPU"
 FALLBACK_HBM_GBS = 6800.0
 DECODE_SOURCES = ["pa_decode.cuh", "pa_device.cuh", "pa_api.cu", "pa_internal.h"]
@@ -187,10 +195,20 @@ class ClockSampler:
 # ----------------------------------------------------------------------------
 # our arm
 # ----------------------------------------------------------------------------
-def prepare(name, device, seed_offset=0, partition_size=None):
+def workload_kw(args):
+    """--workload-kw key=value pairs (integers): parameters of the workload's
+    generator, for a smaller case of the same workload (profiling)."""
+    kw = {}
+    for item in getattr(args, "workload_kw", None) or []:
+        k, v = item.split("=", 1)
+        kw[k] = int(v)
+    return kw
+
+
+def prepare(name, device, seed_offset=0, partition_size=None, kw=None):
     import workloads as W
     from paged_kv_cache_79_gb300 import runner
-    w = W.by_name(name)
+    w = W.by_name(name, **(kw or {}))
     if partition_size is not None:
         w.partition_size = partition_size
     if seed_offset:
@@ -205,51 +223,101 @@ def prepare(name, device, seed_offset=0, partition_size=None):
 # the workloads whose oracle is also timed on one host core (tiny, MHA, GQA)
 ONE_CORE_WORKLOADS = ("tiny", "mha_fp16", "gqa_bf16")
 
+# The oracle legs (cpu_baseline and the reference arm) decode every sequence of a
+# workload whose unique K/V fits in ORACLE_FULL_BYTES; a larger one (the long
+# multi-turn batch: 20.6 GB) is sampled: ORACLE_SAMPLE_SEQS seeded sequences plus
+# the longest, with only the blocks they reference gathered to the host.
+ORACLE_FULL_BYTES = 2 << 30
+ORACLE_SAMPLE_SEQS = 32
 
-def workload_config(w, cl):
-    """The workload's own keys of the JSON line's config (both arms)."""
+L2_NOTE = ("GPU arm: the 129 MB L2 is flushed before every timed step (512 MB written, "
+           "then 1 GB read)")
+
+
+def workload_config(w, cl, world=1):
+    """The JSON line's config: the workload and the job layout, the same in both arms."""
     import numpy as np
     return {"workload": w.name, "num_seqs": len(cl), "num_q_heads": w.num_q_heads,
             "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim, "block_size": w.block_size,
             "num_blocks": w.num_blocks, "context_tokens": int(np.sum(cl)),
-            "max_context": int(np.max(cl))}
+            "max_context": int(np.max(cl)), "l2": L2_NOTE,
+            "parallelism": f"replica x{world} (independent batches, one per GPU)"}
+
+
+def oracle_subset(w, bt, cl):
+    """Indices of the sequences the oracle legs decode: all of them, or (workloads
+    whose unique K/V exceeds ORACLE_FULL_BYTES) a seeded sample of
+    ORACLE_SAMPLE_SEQS plus the longest."""
+    import numpy as np
+    S = len(cl)
+    if step_bytes(w, bt, cl, 0, 0)["kv_unique"] <= ORACLE_FULL_BYTES or S <= ORACLE_SAMPLE_SEQS:
+        return list(range(S))
+    rng = np.random.default_rng(w.data_seed)
+    pick = set(rng.choice(S, size=ORACLE_SAMPLE_SEQS, replace=False).tolist())
+    pick.add(int(np.argmax(cl)))
+    return sorted(pick)
+
+
+def subset_tables(w, bt, cl, seqs):
+    """(blocks the sequences reference, sorted; their tables renumbered into that
+    list; their context lengths)."""
+    import numpy as np
+    B = w.block_size
+    bt = np.asarray(bt)[seqs]
+    cl = np.asarray(cl)[seqs].astype(np.int32)
+    nbs = [(int(t) + B - 1) // B for t in cl]
+    used = sorted({int(bt[i, j]) for i in range(len(seqs)) for j in range(nbs[i])})
+    remap = {b: i for i, b in enumerate(used)}
+    sbt = np.full(bt.shape, -1, dtype=np.int32)
+    for i in range(len(seqs)):
+        sbt[i, :nbs[i]] = [remap[int(b)] for b in bt[i, :nbs[i]]]
+    return used, sbt, cl
 
 
 def cpu_baseline(w, ds, bt, cl, budget_s=10.0, threads=None):
     """Time the fp64 oracle (as it stands) on the host cores on a bounded sample:
-    whole decode steps over the sequences' blocks, repeated until ~budget_s.
-    threads: the oracle's thread count for this timing (None: all host cores)."""
+    decodes of the oracle subset's sequences (every sequence unless the workload is
+    too large, see oracle_subset) over their blocks, repeated until ~budget_s.
+    threads: the oracle's thread count for this timing (None: all host cores).
+    Returns (repetitions, seconds, threads used, bytes per repetition, sample note)."""
     import numpy as np
     import torch
     import oracle
-    B = w.block_size
-    nbs = [(int(t) + B - 1) // B for t in cl]
-    used = sorted({int(bt[s, j]) for s in range(len(cl)) for j in range(nbs[s])})
-    remap = {b: i for i, b in enumerate(used)}
+    seqs = oracle_subset(w, bt, cl)
+    used, sbt, scl = subset_tables(w, bt, cl, seqs)
     idx = torch.tensor(used, dtype=torch.long, device=ds.k_cache.device)
     kh, vh = raw(ds.k_cache.index_select(0, idx)), raw(ds.v_cache.index_select(0, idx))
-    sbt = np.full(bt.shape, -1, dtype=np.int32)
-    for s in range(len(cl)):
-        sbt[s, :nbs[s]] = [remap[int(b)] for b in bt[s, :nbs[s]]]
-    q = raw(ds.q)
+    q = raw(ds.q)[seqs]
+    nbytes = step_bytes(w, sbt, scl, 0, 0)["decode"]
+    note = sample_text(w, seqs, len(cl), scl, nbytes)
     before = oracle.num_threads()
     if threads is not None:
         oracle.set_num_threads(threads)
     try:
-        # bound the sample: whole decode steps until ~budget_s of work (at least one)
+        # bound the sample: whole decodes until ~budget_s of work (at least one)
         t0 = time.perf_counter()
         reps = 0
         while True:
-            oracle.decode(q, kh, vh, sbt, cl, w.softmax_scale, w.dtype, w.num_q_heads,
-                          w.num_kv_heads, w.head_dim, B)
+            oracle.decode(q, kh, vh, sbt, scl, w.softmax_scale, w.dtype, w.num_q_heads,
+                          w.num_kv_heads, w.head_dim, w.block_size)
             reps += 1
             el = time.perf_counter() - t0
             if el >= budget_s:
                 break
-        used = oracle.num_threads()
+        used_threads = oracle.num_threads()
     finally:
         oracle.set_num_threads(before)
-    return reps, el, used
+    return reps, el, used_threads, nbytes, note
+
+
+def sample_text(w, seqs, S, scl, nbytes):
+    """What one oracle repetition decodes, for the line's `sample` fields."""
+    import numpy as np
+    if len(seqs) == S:
+        what = "the step's one sequence" if S == 1 else f"all {S} sequences of the step"
+        return f"{what} ({int(np.sum(scl))} tokens, {nbytes / 1e9:.3f} GB)"
+    return (f"a seeded sample of {len(seqs)} of the {S} sequences, the longest among them "
+            f"({int(np.sum(scl))} tokens, {nbytes / 1e9:.2f} GB of K/V)")
 
 
 class L2Flush:
@@ -293,6 +361,8 @@ def run_ours(args):
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world != args.gpus:
+        raise SystemExit(f"bench.py: --gpus {args.gpus} but {world} ranks were started")
     if world > 1 and not dist.is_initialized():
         dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
     torch.cuda.set_device(local)
@@ -300,7 +370,8 @@ def run_ours(args):
 
     from paged_kv_cache_79_gb300 import build as libbuild
     libbuild.build()
-    w, ds, bt, cl = prepare(args.workload, device, seed_offset=rank, partition_size=args.partition_size)
+    w, ds, bt, cl = prepare(args.workload, device, seed_offset=rank, partition_size=args.partition_size,
+                            kw=workload_kw(args))
     n_tok = int(ds.slots.shape[0])
     n_pairs = int(ds.pairs.shape[0])
     by = step_bytes(w, bt, cl, n_tok, n_pairs)
@@ -367,8 +438,12 @@ def run_ours(args):
 
     step_ms = [a.elapsed_time(c) for a, b, c in ev]
     dec_ms = [b.elapsed_time(c) for a, b, c in ev]
-    t_step = sum(step_ms) / len(step_ms)
+    # the step time is the median of the timed steps; the decode launch's mean
+    # duration gives the roofline
+    t_step = statistics.median(step_ms)
+    t_step_mean = sum(step_ms) / len(step_ms)
     t_dec = sum(dec_ms) / len(dec_ms)
+    t_dec_med = statistics.median(dec_ms)
 
     # secondary: warm steps, back to back with no flush (whatever of the step the
     # 129 MB L2 still holds from the step before is read from there)
@@ -382,8 +457,9 @@ def run_ours(args):
             step(stream)
             b.record(stream)
         torch.cuda.synchronize(device)
-    t_warm = sum(a.elapsed_time(b) for a, b in wev) / len(wev)
-    t_step, t_dec, t_warm = max_over_ranks([t_step, t_dec, t_warm], device)
+    t_warm = statistics.median([a.elapsed_time(b) for a, b in wev])
+    t_step, t_step_mean, t_dec, t_dec_med, t_warm = max_over_ranks(
+        [t_step, t_step_mean, t_dec, t_dec_med, t_warm], device)
 
     # end to end through the public API with host buffers
     e2e = run_e2e(ds, stream, device, args, by, shared, world)
@@ -407,20 +483,20 @@ def run_ours(args):
         "vs_baseline": None,
         "dtype": w.dtype,
         "data": "synthetic (seeded N(0,1) q/K/V; seeded allocator script)",
-        "config": {**workload_config(w, cl),
-                   "split": "balanced" if parts == 0 else f"fixed partitions of {parts} tokens",
-                   "append": "fused into the decode launch" if fused else "separate launch",
-                   "prefix_sharing": (f"{int((ds.share[:, 0] >= 0).sum())} sequences in groups that "
-                                      "read their shared leading blocks once (two-pass decode)"
-                                      if shared else "not used (groups save too few reads)"
-                                      if ds.share is not None and not args.no_share else "none"),
-                   "appended_tokens": n_tok,
-                   "cow_pairs": n_pairs,
-                   "l2": "flushed before every timed step (512 MB write, then 1 GB read)",
-                   "parallelism": f"replica x{world} (independent batches)"},
+        "config": workload_config(w, cl, world),
+        "path": {"split": "balanced" if parts == 0 else f"fixed partitions of {parts} tokens",
+                 "append": "fused into the decode launch" if fused else "separate launch",
+                 "prefix_sharing": (f"{int((ds.share[:, 0] >= 0).sum())} sequences in groups that "
+                                    "read their shared leading blocks once (two-pass decode)"
+                                    if shared else "not used (groups save too few reads)"
+                                    if ds.share is not None and not args.no_share else "none"),
+                 "appended_tokens": n_tok,
+                 "cow_pairs": n_pairs},
+        "ms_per_step_mean": round(t_step_mean, 5),
         "seq_layers_per_s": round(world * S / (t_step * 1e-3), 1),
         "pct_of_hbm_peak": round(100 * value / world / peak, 2),
         "decode_ms": round(t_dec, 5),
+        "decode_ms_median": round(t_dec_med, 5),
         "bytes_per_step": by,
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_kind": f"{peak_kind} copy bandwidth",
@@ -438,18 +514,16 @@ def run_ours(args):
         "wall_s_timed_region": round(wall, 4),
     }
     if world == 1 and not args.no_cpu_baseline:
-        reps, el, cores = cpu_baseline(w, ds, bt, cl, args.cpu_budget)
-        line["cpu_baseline"] = {"value": round(reps * by["decode"] / el / 1e9, 4), "unit": "GB/s",
+        reps, el, cores, nbytes, note = cpu_baseline(w, ds, bt, cl, args.cpu_budget)
+        line["cpu_baseline"] = {"value": round(reps * nbytes / el / 1e9, 4), "unit": "GB/s",
                                 "cores": cores, "kind": "oracle",
-                                "sample": f"{reps} full decode steps of this workload ({S} sequences), "
-                                          f"fp64 C oracle, {el:.1f} s"}
+                                "sample": f"{reps} decodes of {note}, fp64 C oracle, {el:.1f} s"}
         if w.name in ONE_CORE_WORKLOADS:
-            reps, el, cores = cpu_baseline(w, ds, bt, cl, args.cpu_budget / 2, threads=1)
+            reps, el, cores, nbytes, note = cpu_baseline(w, ds, bt, cl, args.cpu_budget / 2, threads=1)
             line["cpu_baseline_one_core"] = {
-                "value": round(reps * by["decode"] / el / 1e9, 4), "unit": "GB/s", "cores": cores,
+                "value": round(reps * nbytes / el / 1e9, 4), "unit": "GB/s", "cores": cores,
                 "kind": "oracle",
-                "sample": f"{reps} full decode steps of this workload, fp64 C oracle on one core, "
-                          f"{el:.1f} s"}
+                "sample": f"{reps} decodes of {note}, fp64 C oracle on one core, {el:.1f} s"}
     return line
 
 
@@ -496,48 +570,62 @@ def run_e2e(ds, stream, device, args, by, shared=False, world=1):
 # reference arm: the fp64 CPU oracle on the host cores
 # ----------------------------------------------------------------------------
 def run_reference(args):
+    """The oracle as the reference arm, on rank 0's host cores: each timed step
+    decodes the oracle subset of the workload (every sequence, or for the long
+    multi-turn batch a seeded sample of 32 plus the longest; see oracle_subset),
+    over pool data generated on the host for the blocks those sequences use."""
     import numpy as np
     rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", str(args.gpus)))
+    if world != args.gpus:
+        raise SystemExit(f"bench.py: --gpus {args.gpus} but {world} ranks were started")
     if rank != 0:
         return None
     import oracle
     import workloads as W
-    w = W.by_name(args.workload)
-    # the oracle executes the workload's script with its own allocator on a host
-    # pool; the pool holds N(0,1) data drawn on the CPU (same recipe, CPU generator)
+    w = W.by_name(args.workload, **workload_kw(args))
+    # the oracle executes the workload's script with its own allocator; the pool
+    # data is N(0,1) drawn on the CPU (same recipe, CPU generator) for the blocks
+    # the decoded sequences reference
     oalloc, _ = oracle.run_script(w.events, w.num_blocks, w.block_size, w.free_order)
     bt, cl = oracle.tables_for(oalloc, w.decode_seqs)
-    B = w.block_size
-    nbs = [(int(t) + B - 1) // B for t in cl]
-    used = sorted({int(bt[s, j]) for s in range(len(cl)) for j in range(nbs[s])})
-    remap = {b: i for i, b in enumerate(used)}
-    sbt = np.full(bt.shape, -1, dtype=np.int32)
-    for s in range(len(cl)):
-        sbt[s, :nbs[s]] = [remap[int(b)] for b in bt[s, :nbs[s]]]
-    shape = (len(used), B, w.num_kv_heads, w.head_dim)
+    seqs = oracle_subset(w, bt, cl)
+    used, sbt, scl = subset_tables(w, bt, cl, seqs)
+    shape = (len(used), w.block_size, w.num_kv_heads, w.head_dim)
     kh = raw(W.randn(shape, w.dtype, w.data_seed * 10 + 1))
     vh = raw(W.randn(shape, w.dtype, w.data_seed * 10 + 2))
-    q = raw(W.query_tensor(w, 0))
-    by = step_bytes(w, sbt, cl, 0, 0)
+    q = raw(W.query_tensor(w, 0))[seqs]
+    nbytes = step_bytes(w, sbt, scl, 0, 0)["decode"]
+    note = sample_text(w, seqs, len(cl), scl, nbytes)
+    # every host core (torch.distributed.run sets OMP_NUM_THREADS=1 for its ranks;
+    # only rank 0 works here)
+    before = oracle.num_threads()
+    oracle.set_num_threads(os.cpu_count() or 1)
     times = []
-    for i in range(args.warmup + args.steps):
-        t0 = time.perf_counter()
-        oracle.decode(q, kh, vh, sbt, cl, w.softmax_scale, w.dtype, w.num_q_heads, w.num_kv_heads,
-                      w.head_dim, B)
-        if i >= args.warmup:
-            times.append(time.perf_counter() - t0)
-    t = sum(times) / len(times)
-    value = by["decode"] / t / 1e9
-    cores = oracle.num_threads()
-    return {"metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": args.gpus,
+    try:
+        for i in range(args.warmup + args.steps):
+            t0 = time.perf_counter()
+            oracle.decode(q, kh, vh, sbt, scl, w.softmax_scale, w.dtype, w.num_q_heads,
+                          w.num_kv_heads, w.head_dim, w.block_size)
+            if i >= args.warmup:
+                times.append(time.perf_counter() - t0)
+        cores = oracle.num_threads()
+    finally:
+        oracle.set_num_threads(before)
+    t = statistics.median(times)
+    value = nbytes / t / 1e9
+    return {"metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world,
             "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": round(t * 1e3, 3), "higher_is_better": True,
+            "warmup": args.warmup, "ms_per_step": round(t * 1e3, 3),
+            "ms_per_step_mean": round(1e3 * sum(times) / len(times), 3), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "impl": "reference",
-            "config": {**workload_config(w, cl),
-                       "parallelism": "the oracle on rank 0's host cores (no GPU)"},
+            "config": workload_config(w, cl, world),
+            "path": {"oracle": "fp64 C, plain definition (gather the valid rows, dense softmax "
+                               "attention), OpenMP over (sequence, head)",
+                     "sample": f"each step decodes {note}"},
             "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
-                             "sample": f"one full decode step of {w.name} per timed step (fp64 C oracle)"},
+                             "sample": f"each timed step decodes {note} (fp64 C oracle)"},
             "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
 
@@ -623,12 +711,31 @@ def run_memory(args):
     return {"op": "memory", "data": "synthetic allocator traces", "results": res}
 
 
+def free_port() -> int:
+    import socket
+    with socket.socket() as sk:
+        sk.bind(("127.0.0.1", 0))
+        return sk.getsockname()[1]
+
+
+def spawn_ranks(n: int, argv) -> int:
+    """Run this script as n ranks on this node (torch.distributed.run, rendezvous on
+    127.0.0.1, one process per GPU); rank 0 prints the line.  Returns the exit code."""
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", f"--nproc-per-node={n}",
+           "--master-addr", "127.0.0.1", f"--master-port={free_port()}",
+           os.path.abspath(__file__)] + list(argv)
+    return subprocess.run(cmd).returncode
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--workload-kw", action="append", default=[], metavar="KEY=INT",
+                    help="a parameter of the workload's generator (e.g. groups=4 for a 16-sequence "
+                         "long_multiturn_bf16): a smaller case of the same workload, for profiling")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--partition-size", type=int, default=0,
@@ -642,6 +749,8 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
+    if args.op == "decode" and args.gpus > 1 and "WORLD_SIZE" not in os.environ:
+        sys.exit(spawn_ranks(args.gpus, sys.argv[1:]))
     if args.op == "blocks":
         line = run_blocks(args)
     elif args.op == "memory":

@@ -160,11 +160,16 @@ pa_status pa_decode_append(void *out, const void *q, void *k_cache, void *v_cach
  *
  *   share   device int32 [S][2]: share[s][0] = batch index of the first member of
  *           s's group, or -1 when s shares nothing; share[s][1] = number of leading
- *           blocks the group shares.  Preconditions (not checked on the device):
- *           members are consecutive in the batch; all have the same share[s][1] =
- *           P; their block-table rows agree on entries 0 .. P-1; and every member's
- *           context is longer than P * block_size (the newest token is never in a
- *           shared block: the allocator copies such a block on write).
+ *           blocks the group shares.  Preconditions: members are consecutive in the
+ *           batch; all have the same share[s][1] = P; their block-table rows agree
+ *           on entries 0 .. P-1; and every member's context is longer than
+ *           P * block_size (the newest token is never in a shared block: the
+ *           allocator copies such a block on write).  The last one is checked on
+ *           the device: a member that breaks it raises PA_DEVERR_SHARE and is
+ *           decoded as if it shared nothing (its own result stays correct without
+ *           k_new/v_new; with them its append writes into a block the group
+ *           shares, which the others may read either way).  The others are not
+ *           checked.
  *   k_new, v_new   both null (plain decode) or as in pa_decode_append.
  * Requires num_q_heads / num_kv_heads <= 16 (PA_ERR_UNSUPPORTED otherwise).  Always
  * uses the balanced split.  Workspace: pa_decode_shared_workspace_size bytes.
@@ -332,13 +337,36 @@ int pa_kv_transfer_worthwhile(long long reusable_tokens, long long threshold_tok
 
 /*
  * Device-side error flags of the current device (bitwise OR of PA_DEVERR_*), read
- * and cleared with a synchronous copy after `stream` drains.  A kernel that gives
- * up on a wait (a TMA transfer that never lands, ~2 s) sets a flag and returns
- * instead of hanging.
+ * and cleared with a synchronous copy after `stream` drains.  Every wait inside a
+ * decode kernel is bounded: a CTA whose wait runs out (a TMA transfer that never
+ * lands, a warp that stopped) sets a flag, stops issuing copies, lets the copies
+ * it already issued land, and returns instead of hanging (its other waits end at
+ * their own limit at the latest); the launch's output is then incomplete.  The pages have no counterpart: this is
+ * the library's own failure detection.
+ * Returns PA_ERR_TIMEOUT when a timeout flag was set, else PA_ERR_INVALID when
+ * PA_DEVERR_SHARE was (*flags holds the flags, now cleared); PA_OK when none was;
+ * PA_ERR_CUDA if the stream or the copy failed.
+ * After a timeout the split-KV merge counters of an aborted launch may be left
+ * non-zero: a later call is unaffected (each call tags its counters anew), but a
+ * captured CUDA graph replays its tag, so clear its workspace before replaying it.
  */
 #define PA_DEVERR_TIMEOUT_FULL  1u   /* consumer waited too long for a K/V tile   */
 #define PA_DEVERR_TIMEOUT_EMPTY 2u   /* producer waited too long for a free stage */
+#define PA_DEVERR_SHARE         4u   /* pa_decode_shared: a member's context ends
+                                        inside its group's shared blocks          */
 pa_status pa_device_errors(unsigned int *flags, void *stream);
+
+/*
+ * Limit, in ns, of the bounded device-side waits of decode launches enqueued after
+ * this call, by any thread (0 restores the default, 2 s).  Returns the previous
+ * limit.  A shorter limit makes a stalled launch give up sooner; a limit shorter
+ * than the launch's own waits for memory (microseconds) makes it give up at once,
+ * which the tests use to exercise the timeout path.  The wait for copies already
+ * in flight when a CTA stops always takes the default bound.  The pages have no
+ * counterpart (failure detection of this library).
+ */
+#define PA_WAIT_LIMIT_DEFAULT_NS 2000000000ull
+unsigned long long pa_set_wait_limit_ns(unsigned long long ns);
 
 /* ------------------------------------------------------------------------- *
  * Host block allocator ([S] "vLLM": free list, reference counts, copy-on-write;  *

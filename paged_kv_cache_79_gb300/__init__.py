@@ -78,6 +78,28 @@ def _stream(stream) -> int:
     return s.cuda_stream if hasattr(s, "cuda_stream") else int(s)
 
 
+def _torch_stream(stream, device):
+    """`stream` (None: torch's current stream; a torch stream; or a raw cudaStream_t)
+    as a torch stream object."""
+    import torch
+    if stream is None:
+        return torch.cuda.current_stream(device)
+    if hasattr(stream, "cuda_stream"):
+        return stream
+    return torch.cuda.ExternalStream(int(stream), device=device)
+
+
+def _launch_scratch(nbytes: int, device, stream):
+    """A uint8 workspace for a launch on `stream`, taken from torch's caching
+    allocator on that stream.  The tensor is dropped when the call returns, while
+    the launch may still be running; allocated on the launch's own stream, its
+    block is handed out again only to later work on that stream, which runs after
+    the launch."""
+    import torch
+    with torch.cuda.stream(_torch_stream(stream, device)):
+        return torch.empty(nbytes, dtype=torch.uint8, device=device)
+
+
 # ----------------------------------------------------------------------------
 # decode
 # ----------------------------------------------------------------------------
@@ -97,12 +119,12 @@ def pa_decode_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim, bloc
 
 
 def alloc_workspace(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq,
-                    partition_size=0, device="cuda"):
-    """A caller-owned workspace tensor of the size pa_decode needs (None if 0)."""
-    import torch
+                    partition_size=0, device="cuda", stream=None):
+    """A caller-owned workspace tensor of the size pa_decode needs (None if 0),
+    allocated on `stream` (default: torch's current stream)."""
     n = pa_decode_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
                                  max_blocks_per_seq, partition_size)
-    return torch.empty(n, dtype=torch.uint8, device=device) if n > 0 else None
+    return _launch_scratch(n, device, stream) if n > 0 else None
 
 
 def pa_decode(out, q, k_cache, v_cache, block_tables, context_lens, scale: float,
@@ -117,7 +139,7 @@ def pa_decode(out, q, k_cache, v_cache, block_tables, context_lens, scale: float
     W = block_tables.shape[1]
     if workspace is None:
         workspace = alloc_workspace(S, num_q_heads, num_kv_heads, head_dim, block_size, W,
-                                    partition_size, q.device)
+                                    partition_size, q.device, stream)
     ws_ptr = _cuda(workspace, "workspace") if workspace is not None else None
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     if block_tables.dtype != torch.int32 or context_lens.dtype != torch.int32:
@@ -142,7 +164,7 @@ def pa_decode_append(out, q, k_cache, v_cache, k_new, v_new, block_tables, conte
     W = block_tables.shape[1]
     if workspace is None:
         workspace = alloc_workspace(S, num_q_heads, num_kv_heads, head_dim, block_size, W,
-                                    partition_size, q.device)
+                                    partition_size, q.device, stream)
     ws_ptr = _cuda(workspace, "workspace") if workspace is not None else None
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     if block_tables.dtype != torch.int32 or context_lens.dtype != torch.int32:
@@ -177,7 +199,7 @@ def pa_decode_shared(out, q, k_cache, v_cache, block_tables, context_lens, share
     W = block_tables.shape[1]
     if workspace is None:
         n = pa_decode_shared_workspace_size(S, num_q_heads, num_kv_heads, head_dim, block_size, W)
-        workspace = torch.empty(n, dtype=torch.uint8, device=q.device)
+        workspace = _launch_scratch(n, q.device, stream)
     if share.dtype != torch.int32 or block_tables.dtype != torch.int32 or context_lens.dtype != torch.int32:
         raise TypeError("share, block_tables and context_lens must be int32")
     st = _load().pa_decode_shared(_cuda(out, "out"), _cuda(q, "q"), _cuda(k_cache, "k_cache"),
@@ -281,9 +303,24 @@ def pa_copy_blocks(k_cache, v_cache, src_dst_pairs, stream=None):
 
 
 def pa_device_errors(stream=None) -> int:
+    """The device-side error flags (PA_DEVERR_*) raised since the last read, after
+    `stream` drains; reading clears them.  Set flags are returned, not raised (the
+    C call's PA_ERR_TIMEOUT / PA_ERR_INVALID status); a CUDA failure raises."""
     flags = ctypes.c_uint(0)
-    _check(_load().pa_device_errors(ctypes.byref(flags), _stream(stream)), "pa_device_errors")
+    st = _load().pa_device_errors(ctypes.byref(flags), _stream(stream))
+    if st not in (PA_ERR_TIMEOUT, PA_ERR_INVALID) or flags.value == 0:
+        _check(st, "pa_device_errors")
     return flags.value
+
+
+PA_DEVERR_TIMEOUT_FULL, PA_DEVERR_TIMEOUT_EMPTY, PA_DEVERR_SHARE = 1, 2, 4
+PA_WAIT_LIMIT_DEFAULT_NS = 2_000_000_000
+
+
+def pa_set_wait_limit_ns(ns: int) -> int:
+    """Limit (ns) of the device-side waits of decode launches enqueued from now on
+    (0: the default, 2 s); returns the previous limit."""
+    return int(_load().pa_set_wait_limit_ns(int(ns)))
 
 
 def pa_status_string(status: int) -> str:
@@ -481,5 +518,6 @@ def pa_kv_transfer_worthwhile(reusable_tokens: int, threshold_tokens: int = 64) 
 __all__ = ["pa_decode", "pa_decode_append", "pa_decode_shared", "pa_decode_shared_workspace_size",
            "share_groups", "share_saving", "SHARE_MIN_SAVING", "pa_decode_noalloc", "pa_decode_workspace_size", "pa_decode_partition_size", "alloc_workspace",
            "pa_reshape_and_cache", "pa_copy_blocks", "pa_swap_blocks", "pa_gather_blocks",
-           "pa_scatter_blocks", "pa_kv_transfer_worthwhile", "pa_device_errors", "pa_status_string",
+           "pa_scatter_blocks", "pa_kv_transfer_worthwhile", "pa_device_errors", "pa_set_wait_limit_ns",
+           "PA_DEVERR_TIMEOUT_FULL", "PA_DEVERR_TIMEOUT_EMPTY", "PA_DEVERR_SHARE", "PA_WAIT_LIMIT_DEFAULT_NS", "pa_status_string",
            "BlockAllocator", "PagedKVError", "OutOfBlocks", "library_path"]

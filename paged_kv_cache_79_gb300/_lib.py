@@ -39,6 +39,7 @@ SIGNATURES = {
                                      c_int, c_int, c_int, c_int, c_void_p]),
     "pa_copy_blocks": (c_int, [c_void_p, c_void_p, c_void_p, c_int, c_int, c_size_t, c_void_p]),
     "pa_device_errors": (c_int, [ctypes.POINTER(ctypes.c_uint), c_void_p]),
+    "pa_set_wait_limit_ns": (ctypes.c_ulonglong, [ctypes.c_ulonglong]),
     "pa_alloc_create": (c_int, [ctypes.POINTER(c_void_p), c_int, c_int, c_void_p]),
     "pa_alloc_destroy": (None, [c_void_p]),
     "pa_alloc_new_seq": (c_int, [c_void_p, c_int_p]),

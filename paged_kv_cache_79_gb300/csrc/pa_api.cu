@@ -140,6 +140,9 @@ size_t counter_bytes(int sms) { return (balanced_ctas(sms) * 8 + 255) & ~size_t(
 // value a workspace kept from another process is unlikely to match.
 std::atomic<unsigned int> g_epoch{std::random_device{}()};
 
+// Limit of the device-side waits of decode launches (pa_set_wait_limit_ns).
+std::atomic<unsigned long long> g_wait_limit_ns{kWaitTimeoutNs};
+
 unsigned int next_epoch()
 {
     unsigned int e = ++g_epoch;
@@ -161,6 +164,8 @@ int current_sms()
 }  // namespace
 
 void note_cuda_error(cudaError_t e) { cuda_fail(e); }
+
+unsigned long long wait_limit_ns() { return g_wait_limit_ns.load(); }
 
 int sm_count(int device)
 {
@@ -359,6 +364,7 @@ pa_status decode_impl(void *out, const void *q, const void *k_cache, const void 
     p.errors = device_error_word(dev, &ce);
     if (!p.errors)
         return cuda_fail(ce);
+    p.wait_ns = wait_limit_ns();
     p.scale_log2 = scale * 1.4426950408889634f;
     p.num_seqs = num_seqs;
     p.max_blocks = max_blocks_per_seq;
@@ -630,7 +636,14 @@ pa_status pa_device_errors(unsigned int *flags, void *stream)
     if (e != cudaSuccess)
         return cuda_fail(e);
     *flags = v;
-    return PA_OK;
+    if (v & (PA_DEVERR_TIMEOUT_FULL | PA_DEVERR_TIMEOUT_EMPTY))
+        return PA_ERR_TIMEOUT;
+    return (v & PA_DEVERR_SHARE) ? PA_ERR_INVALID : PA_OK;
+}
+
+unsigned long long pa_set_wait_limit_ns(unsigned long long ns)
+{
+    return g_wait_limit_ns.exchange(ns == 0 ? kWaitTimeoutNs : ns);
 }
 
 }  // extern "C"

@@ -421,18 +421,26 @@ __device__ __forceinline__ void raise_error(const DecodeParams &p, volatile int 
     *abort = 1;
 }
 
-// Bounded wait on an mbarrier phase by every lane of a warp; warp-uniform result.
-__device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity)
+// Bounded wait on an mbarrier phase by every lane of a consumer warp; warp-uniform
+// result.  It gives up after the launch's wait limit and raises
+// PA_DEVERR_TIMEOUT_FULL.  (It does not watch the CTA's abort flag: with that
+// check in this wait the shared-prefix decode took 221 us instead of 215.  A
+// consumer left waiting after another warp gave up runs to its own limit.)
+__device__ __forceinline__ bool warp_wait(const DecodeParams &p, const CtaState &c, uint64_t *bar,
+                                          uint32_t parity)
 {
-    const bool ok = dev::mbar_wait(dev::smem_addr(bar), parity, kWaitTimeoutNs);
-    return __all_sync(0xffffffffu, ok);
+    const bool ok = __all_sync(0xffffffffu, dev::mbar_wait(dev::smem_addr(bar), parity, p.wait_ns));
+    if (!ok && (threadIdx.x & 31) == 0)
+        raise_error(p, c.abort, PA_DEVERR_TIMEOUT_FULL);
+    return ok;
 }
 
 // Barrier among the consumer warps only (the producer runs ahead), bounded.
-__device__ __forceinline__ bool consumer_sync(const CtaState &c, uint32_t &phase)
+__device__ __forceinline__ bool consumer_sync(const DecodeParams &p, const CtaState &c,
+                                              uint32_t &phase)
 {
     dev::mbar_arrive(dev::smem_addr(c.csync));
-    const bool ok = warp_wait(c.csync, phase & 1u);
+    const bool ok = warp_wait(p, c, c.csync, phase & 1u);
     ++phase;
     return ok;
 }
@@ -469,7 +477,8 @@ struct Producer {
         }
     }
 
-    // Publish `it` and stream its blocks; false once something timed out.
+    // Publish `it` and stream its blocks; false once the CTA is stopping early (a
+    // wait gave up, here or in a consumer warp).
     __device__ bool emit(const Item &it)
     {
         constexpr uint32_t kQSlotBytes = kHeadsPerItem * D * sizeof(T);
@@ -481,8 +490,7 @@ struct Producer {
                 PA_TRACE_SET(15, dev::global_timer_ns());  // first item found
 #endif
             if (lane == 0) {
-                ok = dev::mbar_wait(dev::smem_addr(&c.item_empty[slot]),
-                                    ((n / kItemSlots) & 1u) ^ 1u, kWaitTimeoutNs);
+                ok = wait_slot(&c.item_empty[slot], ((n / kItemSlots) & 1u) ^ 1u);
                 if (ok) {
                     c.items[slot] = it;
                     // query rows: rpm contiguous heads of each member sequence
@@ -497,8 +505,6 @@ struct Producer {
                 }
             }
             if (!__shfl_sync(0xffffffffu, ok, 0)) {
-                if (lane == 0)
-                    raise_error(p, c.abort, PA_DEVERR_TIMEOUT_EMPTY);
                 failed = true;
                 return false;
             }
@@ -517,8 +523,7 @@ struct Producer {
                 const unsigned long long t_w0 = dev::global_timer_ns();
 #endif
                 if (lane == 0)
-                    ok = dev::mbar_wait(dev::smem_addr(&c.empty[st]), ((g / kStages) & 1u) ^ 1u,
-                                        kWaitTimeoutNs);
+                    ok = wait_slot(&c.empty[st], ((g / kStages) & 1u) ^ 1u);
 #ifdef PA_TRACE
                 if (lane == 0) {
                     const unsigned long long t_w1 = dev::global_timer_ns();
@@ -528,8 +533,6 @@ struct Producer {
                 }
 #endif
                 if (!__shfl_sync(0xffffffffu, ok, 0)) {
-                    if (lane == 0)
-                        raise_error(p, c.abort, PA_DEVERR_TIMEOUT_EMPTY);
                     failed = true;
                     return false;
                 }
@@ -586,7 +589,27 @@ struct Producer {
         return true;
     }
 
-    // End-of-work marker for the consumers; on failure, let issued copies land.
+    // Lane 0: wait for the consumers to free a ring stage or item slot (the phase
+    // before `parity`).  Gives up after the launch's wait limit, raising
+    // PA_DEVERR_TIMEOUT_EMPTY, or once a consumer warp has given up.
+    __device__ bool wait_slot(uint64_t *bar, uint32_t parity)
+    {
+        const int r = dev::mbar_wait_abortable(dev::smem_addr(bar), parity, p.wait_ns, c.abort);
+        if (r == 0)
+            raise_error(p, c.abort, PA_DEVERR_TIMEOUT_EMPTY);
+        return r == 1;
+    }
+
+    // End of the walk: publish the end-of-work marker for the consumers (unless the
+    // CTA is stopping early), and let every copy this warp issued land before it
+    // exits.  The CTA's shared memory stays allocated while any of its threads is
+    // alive, and consumers that gave up (a timeout anywhere in the CTA) exit without
+    // waiting for their stages; in a normal launch the consumers wait for the same
+    // phases, so this wait costs nothing.  It waits for the last kItemSlots items'
+    // query rows before the marker is published (the marker completes one more phase
+    // of an item slot) and for the last kStages stages after it, each with the full
+    // bound kWaitTimeoutNs: neither the launch's wait limit nor the abort flag cuts
+    // it short.
     __device__ void finish()
     {
 #ifdef PA_TRACE
@@ -597,24 +620,21 @@ struct Producer {
 #endif
         if (lane != 0)
             return;
-        const uint32_t slot = n % kItemSlots;
-        if (dev::mbar_wait(dev::smem_addr(&c.item_empty[slot]), ((n / kItemSlots) & 1u) ^ 1u,
-                           failed ? kWaitTimeoutNs / 8 : kWaitTimeoutNs)) {
-            c.items[slot].seq = -1;
-            dev::mbar_arrive(dev::smem_addr(&c.item_full[slot]));
-        } else if (!failed) {
-            raise_error(p, c.abort, PA_DEVERR_TIMEOUT_EMPTY);
-            failed = true;
+        for (uint32_t k = n > kItemSlots ? n - kItemSlots : 0; k < n; ++k)
+            dev::mbar_wait(dev::smem_addr(&c.item_full[k % kItemSlots]), (k / kItemSlots) & 1u,
+                           kWaitTimeoutNs);
+        if (!failed) {
+            const uint32_t slot = n % kItemSlots;
+            if (wait_slot(&c.item_empty[slot], ((n / kItemSlots) & 1u) ^ 1u)) {
+                c.items[slot].seq = -1;
+                dev::mbar_arrive(dev::smem_addr(&c.item_full[slot]));
+            } else {
+                failed = true;
+            }
         }
-        if (failed) {
-            const uint32_t first = g > kStages ? g - kStages : 0;
-            for (uint32_t q = first; q < g; ++q)
-                dev::mbar_wait(dev::smem_addr(&c.full[q % kStages]), (q / kStages) & 1u,
-                               kWaitTimeoutNs / 8);
-            if (n > 0)
-                dev::mbar_wait(dev::smem_addr(&c.item_full[(n - 1) % kItemSlots]),
-                               ((n - 1) / kItemSlots) & 1u, kWaitTimeoutNs / 8);
-        }
+        for (uint32_t q = g > kStages ? g - kStages : 0; q < g; ++q)
+            dev::mbar_wait(dev::smem_addr(&c.full[q % kStages]), (q / kStages) & 1u,
+                           kWaitTimeoutNs);
     }
 };
 
@@ -706,7 +726,15 @@ __device__ __forceinline__ SeqUnits seq_units(const DecodeParams &p, int s, int 
         return u;
     }
     const int nb = (len + bs - 1) / bs;
-    const int P = min(shared, nb);
+    int P = min(shared, nb);
+    if (kShare && P > 0 && len <= shared * bs) {
+        // the context ends inside the group's shared blocks (its newest token would
+        // sit in a shared block, which the allocator copies on write): an input
+        // error, reported; the sequence's own launch reads all its blocks itself and
+        // ignores the prefix rows the shared launch computes for it
+        atomicOr(p.errors, PA_DEVERR_SHARE);
+        P = 0;
+    }
     u.nunits = p.num_kv_heads * p.head_groups;
     u.ns = (nb - P + bps - 1) / bps;
     u.start = P;
@@ -1299,7 +1327,7 @@ __device__ __forceinline__ bool finish_item(const DecodeParams &p, const Item &i
                                             uint32_t &sph, int warp, int lane, const float *pfx_s)
 {
     const bool split = p.balanced && it.partial;
-    if (!consumer_sync(c, sph))
+    if (!consumer_sync(p, c, sph))
         return false;
     if (!split)
         return true;
@@ -1307,7 +1335,7 @@ __device__ __forceinline__ bool finish_item(const DecodeParams &p, const Item &i
         // completes the unit (probe_split_last): own rows from shared memory, then a
         // barrier before the next item may overwrite them
         merge_split_unit<T, D, kShare>(p, it, warp, lane, pfx_s, c.macc, c.mml);
-        return consumer_sync(c, sph);
+        return consumer_sync(p, c, sph);
     }
     if (threadIdx.x == 0) {
         // release: this CTA's partial rows (observed through the barrier above)
@@ -1320,7 +1348,7 @@ __device__ __forceinline__ bool finish_item(const DecodeParams &p, const Item &i
             dev::fence_acq_rel_gpu();
         *c.merge = last ? 1 : 0;
     }
-    if (!consumer_sync(c, sph))
+    if (!consumer_sync(p, c, sph))
         return false;
     if (*c.merge)
         merge_split_unit<T, D, kShare>(p, it, warp, lane, pfx_s);
@@ -1435,9 +1463,7 @@ __device__ __forceinline__ bool consume_item_n8(const DecodeParams &p, const Cta
 #ifdef PA_TRACE
         const unsigned long long t_sw = dev::global_timer_ns();
 #endif
-        if (!warp_wait(&c.full[st], (g / C::kStages) & 1u)) {
-            if (lane == 0)
-                raise_error(p, c.abort, PA_DEVERR_TIMEOUT_FULL);
+        if (!warp_wait(p, c, &c.full[st], (g / C::kStages) & 1u)) {
             return false;
         }
 #ifdef PA_TRACE
@@ -1654,9 +1680,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 #ifdef PA_TRACE
         const unsigned long long t_iw = dev::global_timer_ns();
 #endif
-        if (!warp_wait(&c.item_full[slot], (n / kItemSlots) & 1u)) {
-            if (lane == 0)
-                raise_error(p, c.abort, PA_DEVERR_TIMEOUT_FULL);
+        if (!warp_wait(p, c, &c.item_full[slot], (n / kItemSlots) & 1u)) {
             break;
         }
 #ifdef PA_TRACE
@@ -1723,9 +1747,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 #ifdef PA_TRACE
             const unsigned long long t_sw = dev::global_timer_ns();
 #endif
-            if (!warp_wait(&c.full[st], (g / C::kStages) & 1u)) {
-                if (lane == 0)
-                    raise_error(p, c.abort, PA_DEVERR_TIMEOUT_FULL);
+            if (!warp_wait(p, c, &c.full[st], (g / C::kStages) & 1u)) {
                 alive = false;
                 break;
             }
@@ -1890,15 +1912,11 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
         if (threadIdx.x == 0)
             probe_split_last(p, it, c);
-        if (!consumer_sync(c, sph)) {
-            if (lane == 0)
-                raise_error(p, c.abort, PA_DEVERR_TIMEOUT_FULL);
+        if (!consumer_sync(p, c, sph)) {
             break;
         }
         finalize_item<T, D, kShare>(p, it, c.macc, c.mml, rows_cap, threadIdx.x, pfx_s, *c.merge == 2);
         if (!finish_item<T, D, kShare>(p, it, c, sph, warp, lane, pfx_s)) {
-            if (lane == 0)
-                raise_error(p, c.abort, PA_DEVERR_TIMEOUT_FULL);
             break;
         }
 #ifdef PA_TRACE
@@ -1911,6 +1929,9 @@ __global__ void __launch_bounds__(kThreads, 2)
         if (*c.abort)
             break;
     }
+    // after an early stop, prefix-row copies this thread started land before it exits
+    if constexpr (kShare)
+        dev::cp_async_wait_all();
 #ifdef PA_TRACE
     if (threadIdx.x == 0)
         PA_TRACE_SET(2, dev::global_timer_ns());
@@ -1972,9 +1993,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool pfx_ready = !kShare || !defers_dependency(p);  // prefix rows may be read
     for (uint32_t n = 0;; ++n) {
         const uint32_t slot = n % kItemSlots;
-        if (!warp_wait(&c.item_full[slot], (n / kItemSlots) & 1u)) {
-            if (lane == 0)
-                raise_error(p, c.abort, PA_DEVERR_TIMEOUT_FULL);
+        if (!warp_wait(p, c, &c.item_full[slot], (n / kItemSlots) & 1u)) {
             break;
         }
         const Item it = load_item(&c.items[slot]);
@@ -2005,9 +2024,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #ifdef PA_TRACE
             const unsigned long long t_sw = dev::global_timer_ns();
 #endif
-            if (!warp_wait(&c.full[st], (g / C::kStages) & 1u)) {
-                if (lane == 0)
-                    raise_error(p, c.abort, PA_DEVERR_TIMEOUT_FULL);
+            if (!warp_wait(p, c, &c.full[st], (g / C::kStages) & 1u)) {
                 alive = false;
                 break;
             }
@@ -2152,9 +2169,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #endif
         if (threadIdx.x == 0)
             probe_split_last(p, it, c);
-        if (!consumer_sync(c, sph)) {
-            if (lane == 0)
-                raise_error(p, c.abort, PA_DEVERR_TIMEOUT_FULL);
+        if (!consumer_sync(p, c, sph)) {
             break;
         }
 #ifdef PA_TRACE
@@ -2164,8 +2179,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         finalize_item<float, D, kShare>(p, it, c.macc, c.mml, rows_cap, threadIdx.x, pfx_s,
                                 *c.merge == 2);
         if (!finish_item<float, D, kShare>(p, it, c, sph, warp, lane, pfx_s)) {
-            if (lane == 0)
-                raise_error(p, c.abort, PA_DEVERR_TIMEOUT_FULL);
             break;
         }
 #ifdef PA_TRACE
@@ -2175,6 +2188,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (*c.abort)
             break;
     }
+    // after an early stop, prefix-row copies this thread started land before it exits
+    if constexpr (kShare)
+        dev::cp_async_wait_all();
 #ifdef PA_TRACE
     if (threadIdx.x == 0)
         PA_TRACE_SET(2, dev::global_timer_ns());

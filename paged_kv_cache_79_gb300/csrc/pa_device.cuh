@@ -58,17 +58,38 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
 }
 
 // Wait for the phase with the given parity to complete; give up after
-// `timeout_ns` of wall time and return false.
+// `timeout_ns` of wall time and return false.  A failed try_wait has already
+// suspended the thread for an interval the hardware picks, so the clock is read
+// after every one: a wait that outlasts two such intervals notices a limit
+// shorter than that.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t timeout_ns)
 {
     if (mbar_try_wait(bar, parity))
         return true;
     const uint64_t t0 = global_timer_ns();
-    for (uint32_t i = 1;; ++i) {
+    for (;;) {
         if (mbar_try_wait(bar, parity))
             return true;
-        if ((i & 31u) == 0 && global_timer_ns() - t0 > timeout_ns)
+        if (global_timer_ns() - t0 > timeout_ns)
             return false;
+    }
+}
+
+// Wait like mbar_wait, but also give up as soon as *abort is set (another warp of
+// the CTA gave up).  1: the phase completed; 0: timed out; -1: aborted.
+__device__ __forceinline__ int mbar_wait_abortable(uint32_t bar, uint32_t parity, uint64_t timeout_ns,
+                                                   const volatile int *abort)
+{
+    if (mbar_try_wait(bar, parity))
+        return 1;
+    const uint64_t t0 = global_timer_ns();
+    for (;;) {
+        if (mbar_try_wait(bar, parity))
+            return 1;
+        if (*abort)
+            return -1;
+        if (global_timer_ns() - t0 > timeout_ns)
+            return 0;
     }
 }
 

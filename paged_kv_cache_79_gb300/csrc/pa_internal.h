@@ -16,8 +16,10 @@ constexpr int kHeadsPerItem = 16;
 // Consumer warps per CTA; one more warp issues the TMA copies.
 constexpr int kConsumerWarps = 4;
 constexpr int kThreads = 32 * (kConsumerWarps + 1);
-// A device-side wait gives up after this long (ns) and raises an error flag.
-constexpr unsigned long long kWaitTimeoutNs = 2000000000ull;
+// A device-side wait gives up after this long (ns) and raises an error flag.  The
+// limit a launch uses is DecodeParams::wait_ns (pa_set_wait_limit_ns); the wait for
+// copies still in flight when a CTA stops early always takes this one.
+constexpr unsigned long long kWaitTimeoutNs = PA_WAIT_LIMIT_DEFAULT_NS;
 
 // Everything the decode kernels read besides the two tensor maps.
 struct DecodeParams {
@@ -57,7 +59,13 @@ struct DecodeParams {
     const int32_t *share;
     int pass;
     float *pfx;  // rows of head_dim + 4 floats: the row's o, then its log2-sum-exp
+    // Limit of every bounded wait of the launch (ns), but for the drain of copies in
+    // flight; kWaitTimeoutNs unless pa_set_wait_limit_ns changed it.
+    unsigned long long wait_ns;
 };
+
+// The wait limit decode launches take (pa_set_wait_limit_ns).
+unsigned long long wait_limit_ns();
 
 // Balanced split: partial slots are reserved for at most this many CTAs per SM.
 constexpr int kMaxCtasPerSm = 4;

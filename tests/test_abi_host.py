@@ -36,6 +36,13 @@ def test_binding_declares_every_function():
     assert set(declared_functions()) == set(_lib.SIGNATURES)
 
 
+def test_wait_limit_round_trip():
+    """pa_set_wait_limit_ns returns the previous limit; 0 restores the 2 s default."""
+    assert P.pa_set_wait_limit_ns(1000) == P.PA_WAIT_LIMIT_DEFAULT_NS
+    assert P.pa_set_wait_limit_ns(0) == 1000
+    assert P.pa_set_wait_limit_ns(0) == P.PA_WAIT_LIMIT_DEFAULT_NS
+
+
 def test_status_strings():
     for s in range(6):
         assert P.pa_status_string(s)

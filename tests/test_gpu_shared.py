@@ -168,3 +168,20 @@ def test_empty_batch():
                        torch.zeros(0, dtype=torch.int32, device=DEV),
                        torch.zeros(0, 2, dtype=torch.int32, device=DEV), 0.1, 8, 8, 64, 16)
     torch.cuda.synchronize()
+
+
+@pytest.mark.parametrize("short", [1, 20 * 16, 20 * 16 - 5])
+def test_member_ending_inside_the_shared_blocks_is_flagged_and_decoded_alone(short):
+    """A member whose context does not extend past its group's shared blocks breaks
+    the decode's precondition: the device reports PA_DEVERR_SHARE, and the member
+    is decoded as if it shared nothing, so every output still matches the oracle."""
+    dtype, D, B, Hq, Hkv, Pb = "bf16", 128, 16, 16, 4, 20
+    lens = lens_for(5, Pb, B, 9)
+    q, kc, vc, bt, cl, share = shared_case(31, dtype, D, B, Hq, Hkv, [(lens, Pb)], stale=0.0)
+    cl[2] = short                      # member 2 now ends inside the 20 shared blocks
+    bt[2, (short + B - 1) // B:] = -1
+    assert share[2, 0] == 0 and share[2, 1] == Pb
+    assert P.pa_device_errors() == 0
+    got = shared_decode(q, kc.to(DEV), vc.to(DEV), bt, cl, share, 0.09, Hq, Hkv, D, B)
+    assert P.pa_device_errors() == P.PA_DEVERR_SHARE
+    assert_close(got, ora(q, kc, vc, bt, cl, 0.09, dtype, Hq, Hkv, D, B), dtype, f"member of {short} tokens")

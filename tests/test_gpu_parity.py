@@ -36,6 +36,10 @@ for dtype in ("f32", "f16", "bf16"):
 SHAPES.append(("bf16", 128, 16, 12, 3, [3000, 1, 17, 4096, 2222, 16], 0))
 SHAPES.append(("f16", 128, 16, 5, 5, [1], 0))
 SHAPES.append(("bf16", 128, 32, 64, 8, [2049, 513], 512))
+# the long multi-turn batch's shape (bf16, d 128, B 32, G 4) on the balanced split:
+# short units whole, the 40000-token one cut over ~37 CTAs of the persistent grid
+SHAPES.append(("bf16", 128, 32, 32, 8, [1, 31, 32, 33, 5000, 40000], 0))
+SHAPES.append(("bf16", 128, 32, 32, 8, [129, 7777, 3], 0))
 
 
 @pytest.mark.parametrize("dtype,D,B,Hq,Hkv,lens,part", SHAPES,
@@ -207,6 +211,10 @@ FUSED = [
     ("f32", 64, 16, 4, 2, [1, 2, 40, 300], 0),
     ("bf16", 64, 16, 40, 2, [18, 257, 1024], 128),
     ("f16", 128, 16, 12, 3, [0, 5, 3000, 0], 0),
+    # the benched step of the long multi-turn batch: bf16, d 128, B 32, G 4, balanced
+    # split, newest token appended in the decode launch; the 20000-token units are
+    # cut over many CTAs
+    ("bf16", 128, 32, 32, 8, [1, 32, 33, 777, 20000, 20001], 0),
 ]
 
 

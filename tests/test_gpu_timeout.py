@@ -2,15 +2,16 @@
 
 Every wait inside the decode kernels is bounded.  With the wait limit cut to 1 ns
 (pa_set_wait_limit_ns), any wait that lasts longer than a couple of the hardware's
-try_wait suspend intervals runs out.  The batches here carry 4096 empty sequences
-behind the real ones: every CTA's producer walks all of them (a few hundred memory
-round trips) before it publishes its first work item, so the consumers' first
-wait surely runs out.  The launch must then give up: the CTA stops issuing
+try_wait suspend intervals runs out.  The balanced-split batches here carry 4096
+empty sequences behind the real ones: every CTA's producer sums the stream over
+all of them (a few hundred memory round trips) before it publishes its first work
+item, so the consumers' first wait surely runs out.  The launch must then give up: the CTA stops issuing
 copies, lets the copies it issued land, and returns.  The call returns, nothing
 hangs or faults, pa_device_errors reports the timeout (PA_ERR_TIMEOUT from the C
 call), and the next decode with the default limit matches the oracle.  Batches of
 long contexts without the padding time out in mid-stream, with copies in flight,
-when they time out at all."""
+when they time out at all; so do fixed partitions, whose CTAs find their first
+items among the first sequences of the batch."""
 import ctypes
 import math
 
@@ -33,12 +34,12 @@ CASES = [
     ("bf16", 128, 16, 64, 8, [30000, 5000, 17, 9000] + PAD, 0),   # tensor-core consumers, 8-row items
     ("f16", 128, 32, 32, 2, [20000, 3] + PAD, 0),                 # 16-row items
     ("f32", 64, 16, 8, 8, [6000, 40] + PAD, 0),                   # CUDA-core consumers
-    ("bf16", 128, 32, 32, 8, [9000, 129] + PAD, 512),             # fixed partitions + merge kernel
 ]
 MIDSTREAM = [
     ("bf16", 128, 16, 64, 8, [30000, 5000, 17, 9000], 0),
     ("f16", 128, 16, 40, 40, [3000, 2048, 1500, 999, 1200, 64, 2000, 1800], 0),
-    ("bf16", 128, 32, 32, 8, [9000, 129], 512),
+    ("bf16", 128, 32, 32, 8, [9000, 129], 512),                   # fixed partitions + merge kernel
+    ("bf16", 128, 32, 32, 8, [9000, 129] + PAD, 512),
 ]
 
 

@@ -2,10 +2,10 @@
 
 Every wait inside the decode kernels is bounded.  With the wait limit cut to 1 ns
 (pa_set_wait_limit_ns), any wait that lasts longer than a couple of the hardware's
-try_wait suspend intervals runs out.  The balanced-split batches here carry 4096
+try_wait suspend intervals runs out.  The balanced-split batches here carry 16384
 empty sequences behind the real ones: every CTA's producer sums the stream over
-all of them (a few hundred memory round trips) before it publishes its first work
-item, so the consumers' first wait surely runs out.  The launch must then give up: the CTA stops issuing
+all of them (hundreds of memory round trips, tens of microseconds) before it
+publishes its first work item, so the consumers' first wait surely runs out.  The launch must then give up: the CTA stops issuing
 copies, lets the copies it issued land, and returns.  The call returns, nothing
 hangs or faults, pa_device_errors reports the timeout (PA_ERR_TIMEOUT from the C
 call), and the next decode with the default limit matches the oracle.  Batches of
@@ -27,7 +27,7 @@ pytestmark = pytest.mark.gpu
 DEV = "cuda"
 TIMEOUTS = P.PA_DEVERR_TIMEOUT_FULL | P.PA_DEVERR_TIMEOUT_EMPTY
 
-PAD = [0] * 4096     # empty sequences: a long walk before any work item
+PAD = [0] * 16384    # empty sequences: a long walk before any work item
 
 CASES = [
     # dtype, head_dim, block_size, Hq, Hkv, context lengths, partition size

@@ -386,8 +386,10 @@ def run_ours(args):
     merge = parts > 0 and -(-bt.shape[1] // (parts // w.block_size)) > 1
     fused = ds.fusable
     # the shared-prefix decode where the groups save enough reads to pay for its
-    # second launch (parallel sampling: ~69%; multi-turn groups here: ~3%)
-    shared = ds.share is not None and ds.share_pays and not args.no_share
+    # second launch (parallel sampling: 69% of the reads; the long multi-turn
+    # batch: 2.7%, 580 MB)
+    share_mode = "never" if getattr(args, "no_share", False) else getattr(args, "share", "auto")
+    shared = ds.share is not None and (share_mode == "always" or (share_mode == "auto" and ds.share_pays))
     if shared:
         merge = False
         parts = 0
@@ -489,7 +491,8 @@ def run_ours(args):
                  "prefix_sharing": (f"{int((ds.share[:, 0] >= 0).sum())} sequences in groups that "
                                     "read their shared leading blocks once (two-pass decode)"
                                     if shared else "not used (groups save too few reads)"
-                                    if ds.share is not None and not args.no_share else "none"),
+                                    if ds.share is not None and share_mode == "auto" else
+                                    "not used (--share never)" if ds.share is not None else "none"),
                  "appended_tokens": n_tok,
                  "cow_pairs": n_pairs},
         "ms_per_step_mean": round(t_step_mean, 5),
@@ -741,8 +744,10 @@ def main():
     ap.add_argument("--partition-size", type=int, default=0,
                     help="0: balanced split (default); >0: fixed partitions of that many tokens")
     ap.add_argument("--cpu-budget", type=float, default=10.0)
-    ap.add_argument("--no-share", action="store_true",
-                    help="decode every sequence's blocks separately even where groups share a prefix")
+    ap.add_argument("--share", default="auto", choices=["auto", "always", "never"],
+                    help="the two-pass shared-prefix decode for batches whose sequences share leading "
+                         "blocks: where it saves enough reads (auto), always, or never")
+    ap.add_argument("--no-share", action="store_true", help="the same as --share never")
     ap.add_argument("--op", default="decode", choices=["decode", "blocks", "memory"],
                     help="decode: the headline step (default); blocks: block-move GB/s; "
                          "memory: pool accounting on allocator traces")

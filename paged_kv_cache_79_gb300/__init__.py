@@ -232,9 +232,8 @@ def share_groups(block_tables, context_lens, block_size: int, min_shared_blocks:
 
 def share_saving(share, context_lens, block_size: int) -> float:
     """Fraction of the batch's block reads that pa_decode_shared saves over pa_decode:
-    each group of m members sharing P blocks reads (m - 1) * P blocks fewer.  The
-    second launch and the merge cost a few percent, so sharing pays from roughly
-    10% saved (SHARE_MIN_SAVING)."""
+    each group of m members sharing P blocks reads (m - 1) * P blocks fewer (when
+    one item holds all m members' query rows)."""
     import numpy as np
     share = np.asarray(share)
     cl = np.asarray(context_lens).astype(np.int64)
@@ -246,7 +245,22 @@ def share_saving(share, context_lens, block_size: int) -> float:
     return saved / logical if logical else 0.0
 
 
+# pa_decode_shared pays for its second launch and its merges (a fixed ~10-15 us)
+# once the groups save 10% of the block reads, or 256 MB of them (~37 us at
+# 7 TB/s) on a large batch: the long multi-turn batch saves 2.7%, 580 MB, and
+# decodes ~1% faster shared.
 SHARE_MIN_SAVING = 0.10
+SHARE_MIN_BYTES = 256 << 20
+
+
+def share_pays(share, context_lens, block_size: int, block_bytes: int) -> bool:
+    """Whether pa_decode_shared is expected to beat pa_decode on this batch.
+    block_bytes: bytes of one block of K and V over all kv heads."""
+    import numpy as np
+    f = share_saving(share, context_lens, block_size)
+    cl = np.asarray(context_lens).astype(np.int64)
+    logical = int(((cl + block_size - 1) // block_size).sum()) * int(block_bytes)
+    return f >= SHARE_MIN_SAVING or f * logical >= SHARE_MIN_BYTES
 
 
 def pa_decode_noalloc(out, q, k_cache, v_cache, block_tables, context_lens, scale: float,
@@ -516,7 +530,8 @@ def pa_kv_transfer_worthwhile(reusable_tokens: int, threshold_tokens: int = 64) 
 
 
 __all__ = ["pa_decode", "pa_decode_append", "pa_decode_shared", "pa_decode_shared_workspace_size",
-           "share_groups", "share_saving", "SHARE_MIN_SAVING", "pa_decode_noalloc", "pa_decode_workspace_size", "pa_decode_partition_size", "alloc_workspace",
+           "share_groups", "share_saving", "share_pays", "SHARE_MIN_SAVING", "SHARE_MIN_BYTES",
+           "pa_decode_noalloc", "pa_decode_workspace_size", "pa_decode_partition_size", "alloc_workspace",
            "pa_reshape_and_cache", "pa_copy_blocks", "pa_swap_blocks", "pa_gather_blocks",
            "pa_scatter_blocks", "pa_kv_transfer_worthwhile", "pa_device_errors", "pa_set_wait_limit_ns",
            "PA_DEVERR_TIMEOUT_FULL", "PA_DEVERR_TIMEOUT_EMPTY", "PA_DEVERR_SHARE", "PA_WAIT_LIMIT_DEFAULT_NS", "pa_status_string",

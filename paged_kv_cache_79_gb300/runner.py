@@ -13,9 +13,9 @@ from typing import Callable, List, Optional
 
 import numpy as np
 
-from . import (SHARE_MIN_SAVING, BlockAllocator, alloc_workspace, pa_copy_blocks, pa_decode,
-               pa_decode_append, pa_decode_shared, pa_decode_shared_workspace_size,
-               pa_reshape_and_cache, share_groups, share_saving)
+from . import (BlockAllocator, alloc_workspace, pa_copy_blocks, pa_decode, pa_decode_append,
+               pa_decode_shared, pa_decode_shared_workspace_size, pa_reshape_and_cache,
+               share_groups, share_pays)
 
 
 def _kind(ev) -> str:
@@ -55,7 +55,7 @@ class DecodeStep:
     partition_size: int = 0
     fusable: bool = True        # step rows are the batch's newest tokens, in batch order
     share: "object" = None      # int32 [S, 2] shared-prefix groups, None if none share
-    share_pays: bool = False    # the groups save at least SHARE_MIN_SAVING of the reads
+    share_pays: bool = False    # the groups save enough reads for pa_decode_shared (share_pays)
 
     def run_shared(self, stream=None):
         """copy-on-write pairs, then the shared-prefix decode (which also appends the new
@@ -191,7 +191,9 @@ def execute(w, k_cache, v_cache, step_kv: Callable, query: Callable,
                 head_dim=w.head_dim, block_size=w.block_size, partition_size=w.partition_size,
                 fusable=fusable,
                 share=torch.from_numpy(share).to(dev) if has_share else None,
-                share_pays=has_share and share_saving(share, cl, w.block_size) >= SHARE_MIN_SAVING)
+                share_pays=has_share and share_pays(
+                    share, cl, w.block_size,
+                    2 * w.block_size * w.num_kv_heads * w.head_dim * k_cache.element_size()))
             if ds.pairs.shape[0]:
                 pa_copy_blocks(k_cache, v_cache, ds.pairs, stream)
             pa_reshape_and_cache(k, v, k_cache, v_cache, ds.slots, stream)

@@ -125,10 +125,12 @@ def test_shared_prefix_fp16(prompt, shared):
 def test_long_multiturn_bf16():
     """Full-size pool (~19 GB on the device); oracle on sampled sequences whose
     blocks are gathered to the host (block permutation invariance is pinned).
-    Three decodes of the step are checked: the workload's fixed 512-token
+    Four decodes of the step are checked: the workload's fixed 512-token
     partitions (partition kernel + merge kernel), the two-pass shared-prefix decode,
-    and the step the bench times -- the newest tokens appended inside the decode
-    launch on the balanced split (pa_decode_append, partition_size 0)."""
+    the step the bench times -- the two-pass shared-prefix decode with the newest
+    tokens appended inside its second launch (the groups save 580 MB of reads) --
+    and the same step on the plain balanced split (pa_decode_append, partition
+    size 0), which the bench times with --no-share."""
     import dataclasses
     w = W.long_multiturn_bf16()
     kc, vc = _gpu_tensors(w)
@@ -159,18 +161,27 @@ def test_long_multiturn_bf16():
     torch.cuda.synchronize()
     err, _ = assert_close(out_s[seqs], want, "bf16", w.name + " shared")
     assert err <= TOL_16
-    # the benched step: copy-on-write pairs (none here), then the append of every
-    # sequence's newest token fused with the balanced-split decode.  The rows it
-    # appends are the ones the script already wrote, so the caches do not change.
-    assert ds.fusable and ds.pairs.shape[0] == 0
+    # the benched step: copy-on-write pairs (none here), then the shared-prefix
+    # decode with every sequence's newest token appended in its own-block launch.
+    # The rows it appends are the ones the script already wrote, so the caches do
+    # not change.
+    assert ds.fusable and ds.pairs.shape[0] == 0 and ds.share_pays
+    dss = dataclasses.replace(ds, out=torch.full_like(ds.out, float("nan")))
+    dss.run_shared()
+    torch.cuda.synchronize()
+    err, rel = assert_close(dss.out[seqs], want, "bf16", w.name + " benched step")
+    assert err <= TOL_16
+    print(f"[parity] {w.name} benched step (shared prefixes, fused append): max abs err {err:.3e}, "
+          f"normwise rel {rel:.3e}")
+    # the same step without prefix sharing: append fused with the balanced split
     ws0 = P.alloc_workspace(len(cl), w.num_q_heads, w.num_kv_heads, w.head_dim, w.block_size,
                             bt.shape[1], 0, DEV)
     dsb = dataclasses.replace(ds, partition_size=0, workspace=ws0, out=torch.full_like(ds.out, float("nan")))
     dsb.run_fused()
     torch.cuda.synchronize()
-    err, rel = assert_close(dsb.out[seqs], want, "bf16", w.name + " benched step")
+    err, rel = assert_close(dsb.out[seqs], want, "bf16", w.name + " plain step")
     assert err <= TOL_16
-    print(f"[parity] {w.name} benched step (fused append, balanced split): max abs err {err:.3e}, "
+    print(f"[parity] {w.name} step without sharing (fused append, balanced split): max abs err {err:.3e}, "
           f"normwise rel {rel:.3e}")
     # the step's appended rows are where the oracle's allocator put them, bit for bit
     k_new, v_new = W.step_tensors(w, w.step_events()[-1], DEV)

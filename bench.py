@@ -111,15 +111,16 @@ def decode_source_hash():
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(workload):
-    """DRAM bytes per decode launch from the committed ncu summary, if it was taken
-    on the current decode sources; else None."""
+def profiled_traffic(workload, launches=1):
+    """DRAM bytes of one step's decode launches from the committed ncu summary, if
+    it was taken on the current decode sources and on the same path (its number
+    of decode launches per step: 2 for the shared-prefix decode); else None."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
             d = json.load(f)
         e = d.get(workload)
-        if e and e.get("source_hash") == decode_source_hash():
+        if e and e.get("source_hash") == decode_source_hash() and e.get("launches_per_step", 1) == launches:
             return e.get("dram_bytes_per_launch")
     except Exception:
         pass
@@ -503,7 +504,7 @@ def run_ours(args):
         "bytes_per_step": by,
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_kind": f"{peak_kind} copy bandwidth",
-                     "traffic": profiled_traffic(w.name),
+                     "traffic": profiled_traffic(w.name, 2 if shared else 1),
                      "kernel": ("pa_decode_shared (partition kernel twice: shared prefixes, then own "
                                 "blocks" + (" + append" if fused else "") + ", merges inside)" if shared
                                 else "pa_decode_append (append + decode partition kernel, merge inside)"

@@ -394,11 +394,15 @@ def run_ours(args):
     if shared:
         merge = False
         parts = 0
+    # the plain balanced split starts each CTA from the host plan (pa_decode_plan)
+    planned = (not shared and parts == 0 and ds.plan is not None and
+               getattr(args, "plan", "auto") != "never")
     launches_per_step = ((1 if n_pairs else 0) + (0 if fused or not n_tok else 1) +
                          (2 if shared else 1) + (1 if merge else 0))
 
     with torch.cuda.stream(stream):
-        step = ds.run_shared if shared else (ds.run_fused if fused else ds.run)
+        step = (ds.run_shared if shared else ds.run_planned if planned else
+                ds.run_fused if fused else ds.run)
         ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
                torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
         # the sampler starts first: warm-up runs right before the timed steps, so the
@@ -425,6 +429,13 @@ def run_ours(args):
             e1.record(stream)
             if shared:
                 ds.decode_shared(stream, append=fused)
+            elif planned:
+                P.pa_decode_planned(ds.out, ds.q, ds.k_cache, ds.v_cache, ds.block_tables,
+                                    ds.context_lens, ds.plan, ds.scale, ds.num_q_heads,
+                                    ds.num_kv_heads, ds.head_dim, ds.block_size,
+                                    k_new=ds.step_k if fused else None,
+                                    v_new=ds.step_v if fused else None,
+                                    workspace=ds.workspace, stream=stream)
             elif fused:
                 P.pa_decode_append(ds.out, ds.q, ds.k_cache, ds.v_cache, ds.step_k, ds.step_v,
                                    ds.block_tables, ds.context_lens, ds.scale, ds.num_q_heads,
@@ -465,7 +476,7 @@ def run_ours(args):
         [t_step, t_step_mean, t_dec, t_dec_med, t_warm], device)
 
     # end to end through the public API with host buffers
-    e2e = run_e2e(ds, stream, device, args, by, shared, world)
+    e2e = run_e2e(ds, stream, device, args, by, shared, world, planned)
 
     if rank != 0:
         return None
@@ -494,6 +505,8 @@ def run_ours(args):
                                     if shared else "not used (groups save too few reads)"
                                     if ds.share is not None and share_mode == "auto" else
                                     "not used (--share never)" if ds.share is not None else "none"),
+                 "cta_starts": ("planned on the host (pa_decode_plan, uploaded with the tables)"
+                                if planned else "walked on the device"),
                  "appended_tokens": n_tok,
                  "cow_pairs": n_pairs},
         "ms_per_step_mean": round(t_step_mean, 5),
@@ -507,6 +520,8 @@ def run_ours(args):
                      "traffic": profiled_traffic(w.name, 2 if shared else 1),
                      "kernel": ("pa_decode_shared (partition kernel twice: shared prefixes, then own "
                                 "blocks" + (" + append" if fused else "") + ", merges inside)" if shared
+                                else "pa_decode_planned (append + decode partition kernel from the host "
+                                "plan, merge inside)" if planned and fused
                                 else "pa_decode_append (append + decode partition kernel, merge inside)"
                                 if fused else
                                 "pa_decode (partition kernel; split-KV merge fused or second kernel)")},
@@ -531,7 +546,7 @@ def run_ours(args):
     return line
 
 
-def run_e2e(ds, stream, device, args, by, shared=False, world=1):
+def run_e2e(ds, stream, device, args, by, shared=False, world=1, planned=False):
     """Same step through the public API with inputs in pinned host memory: H2D of
     the step's inputs (packed into one buffer, one copy), the step, D2H of the
     output -- all inside the timed region."""
@@ -541,6 +556,8 @@ def run_e2e(ds, stream, device, args, by, shared=False, world=1):
     names = ["q", "step_k", "step_v", "slots", "pairs", "block_tables", "context_lens"]
     if shared:
         names.append("share")
+    if planned:
+        names.append("plan")
     packed = runner.PackedInputs({n: getattr(ds, n) for n in names}, device)
     dsv = dataclasses.replace(ds, **packed.views)
     out_h = torch.empty(ds.out.shape, dtype=ds.out.dtype).pin_memory()
@@ -557,6 +574,8 @@ def run_e2e(ds, stream, device, args, by, shared=False, world=1):
             packed.upload(stream)
             if shared:
                 dsv.run_shared(stream)
+            elif planned:
+                dsv.run_planned(stream)
             else:
                 dsv.run_fused(stream) if dsv.fusable else dsv.run(stream)
             out_h.copy_(dsv.out, non_blocking=True)
@@ -749,6 +768,9 @@ def main():
                     help="the two-pass shared-prefix decode for batches whose sequences share leading "
                          "blocks: where it saves enough reads (auto), always, or never")
     ap.add_argument("--no-share", action="store_true", help="the same as --share never")
+    ap.add_argument("--plan", default="auto", choices=["auto", "never"],
+                    help="start the plain balanced split's CTAs from a host plan (auto) or walk the "
+                         "stream on the device (never)")
     ap.add_argument("--op", default="decode", choices=["decode", "blocks", "memory"],
                     help="decode: the headline step (default); blocks: block-move GB/s; "
                          "memory: pool accounting on allocator traces")

@@ -148,6 +148,57 @@ pa_status pa_decode_append(void *out, const void *q, void *k_cache, void *v_cach
                            void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * pa_decode_plan / pa_decode_planned -- the balanced-split decode with each CTA's
+ * start computed on the host.
+ *
+ * The pages have no counterpart: this is a way to run pa_decode (balanced split),
+ * with or without the fused append of pa_decode_append, for a caller that holds
+ * the context lengths and block tables on the host (its block allocator made
+ * them).  Unplanned, every CTA of the persistent grid first reads the lengths,
+ * sums the stream of (sequence, kv head, head group) units, finds its own range,
+ * and reads the block-table row of its first item: two dependent memory round
+ * trips before its first K/V copy.  pa_decode_plan does that work on the host,
+ * once per step.  It writes, per CTA, the stream total, the CTA's range, its first
+ * sequence with that sequence's first position and length, and the first
+ * 16 block ids of its first item.  A planned launch reads its entry and issues
+ * its first copies at once.  Output, caches and workspace use are bit-identical to
+ * the unplanned call's: the walk and the arithmetic are the same.
+ *
+ * pa_decode_plan_bytes: size of the plan for these arguments on the current
+ *   device: 128 bytes per CTA of the persistent grid (about 2 per SM).
+ *   (size_t)-1 for invalid arguments.
+ * pa_decode_plan: plan (host int32, plan_bytes = pa_decode_plan_bytes) <- the
+ *   schedule for block_tables [num_seqs][max_blocks_per_seq] and context_lens
+ *   [num_seqs], both HOST arrays with the values the launch will read on the
+ *   device.  The plan covers plan_bytes / 128 CTAs, the grid the size was computed
+ *   for.  Host only: no CUDA call, no device work, no allocation.  Errors:
+ *   PA_ERR_INVALID (null pointer, bad sizes, plan_bytes not a positive multiple of
+ *   128).
+ * pa_decode_planned: as pa_decode with partition_size 0 (k_new = v_new = NULL) or
+ *   pa_decode_append (both set), plus `plan`: a DEVICE copy of the plan (16-byte
+ *   aligned, plan_bytes = pa_decode_plan_bytes for the same arguments, made from
+ *   the same lengths and tables).  A plan made from other lengths or tables gives
+ *   a wrong output but no access outside the arguments, and the appended rows
+ *   still go where the block table says; where its positions cannot match the
+ *   lengths the launch reads, the walk stops and PA_DEVERR_PLAN is raised
+ *   (pa_device_errors).  Errors: as pa_decode_append; PA_ERR_INVALID also for a
+ *   null or misaligned plan or a plan_bytes that does not match.
+ */
+size_t pa_decode_plan_bytes(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                            int block_size, int max_blocks_per_seq, pa_dtype dtype);
+pa_status pa_decode_plan(int32_t *plan, size_t plan_bytes, const int32_t *block_tables,
+                         int max_blocks_per_seq, const int32_t *context_lens, int num_seqs,
+                         int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                         pa_dtype dtype);
+pa_status pa_decode_planned(void *out, const void *q, void *k_cache, void *v_cache,
+                            const void *k_new, const void *v_new, const int32_t *block_tables,
+                            int max_blocks_per_seq, const int32_t *context_lens, int num_seqs,
+                            int num_blocks, float scale, int num_q_heads, int num_kv_heads,
+                            int head_dim, int block_size, pa_dtype dtype, const int32_t *plan,
+                            size_t plan_bytes, void *workspace, size_t workspace_bytes,
+                            void *stream);
+
+/*
  * pa_decode_shared -- decode a batch whose sequences share prefix blocks.
  *
  * Same result as pa_decode (or, with k_new/v_new, pa_decode_append), but each
@@ -344,7 +395,8 @@ int pa_kv_transfer_worthwhile(long long reusable_tokens, long long threshold_tok
  * their own limit at the latest); the launch's output is then incomplete.  The pages have no counterpart: this is
  * the library's own failure detection.
  * Returns PA_ERR_TIMEOUT when a timeout flag was set, else PA_ERR_INVALID when
- * PA_DEVERR_SHARE was (*flags holds the flags, now cleared); PA_OK when none was;
+ * PA_DEVERR_SHARE or PA_DEVERR_PLAN was (*flags holds the flags, now cleared);
+ * PA_OK when none was;
  * PA_ERR_CUDA if the stream or the copy failed.
  * After a timeout the split-KV merge counters of an aborted launch may be left
  * non-zero: a later call is unaffected (each call tags its counters anew), but a
@@ -354,6 +406,8 @@ int pa_kv_transfer_worthwhile(long long reusable_tokens, long long threshold_tok
 #define PA_DEVERR_TIMEOUT_EMPTY 2u   /* producer waited too long for a free stage */
 #define PA_DEVERR_SHARE         4u   /* pa_decode_shared: a member's context ends
                                         inside its group's shared blocks          */
+#define PA_DEVERR_PLAN          8u   /* pa_decode_planned: the plan does not match
+                                        the context lengths the launch read       */
 pa_status pa_device_errors(unsigned int *flags, void *stream);
 
 /*

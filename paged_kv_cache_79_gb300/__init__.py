@@ -7,6 +7,8 @@ calls on tensors that are not CUDA tensors raise.
 
     pa_decode               paged single-query attention (partition + merge kernels)
     pa_decode_append        the newest tokens' append fused with the decode
+    pa_decode_plan /        the balanced split's CTA starts computed on the host, and
+      pa_decode_planned       the decode (and append) that starts from them
     pa_decode_shared        decode reading each shared prefix block once per group
     pa_reshape_and_cache    write new tokens' K/V rows through a slot mapping
     pa_copy_blocks          copy-on-write block copies
@@ -179,6 +181,78 @@ def pa_decode_append(out, q, k_cache, v_cache, k_new, v_new, block_tables, conte
     return out
 
 
+_DTYPE_NAMES = {"f32": PA_F32, "f16": PA_F16, "bf16": PA_BF16}
+
+
+def _dtype_arg(dtype) -> int:
+    """A pa_dtype code from a code, a name ('f32', 'f16', 'bf16') or a torch dtype."""
+    if isinstance(dtype, int):
+        return dtype
+    if isinstance(dtype, str):
+        return _DTYPE_NAMES[dtype]
+    import torch
+    return {torch.float32: PA_F32, torch.float16: PA_F16, torch.bfloat16: PA_BF16}[dtype]
+
+
+def pa_decode_plan_bytes(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq,
+                         dtype) -> int:
+    """Size of a pa_decode_plan for these arguments on the current device."""
+    n = _load().pa_decode_plan_bytes(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+                                     max_blocks_per_seq, _dtype_arg(dtype))
+    if n == ctypes.c_size_t(-1).value:
+        raise PagedKVError(PA_ERR_INVALID, "pa_decode_plan_bytes")
+    return n
+
+
+def pa_decode_plan(block_tables, context_lens, num_q_heads: int, num_kv_heads: int, head_dim: int,
+                   block_size: int, dtype, plan_bytes: Optional[int] = None):
+    """Host-side schedule of the balanced-split decode (see pa_decode_plan in
+    include/pagedkv.h): int32 numpy array of plan_bytes / 4 entries, from HOST block
+    tables [S, W] and context lengths [S] (numpy arrays or CPU tensors).  plan_bytes
+    defaults to pa_decode_plan_bytes(...) on the current device."""
+    import numpy as np
+    bt = np.ascontiguousarray(np.asarray(block_tables, dtype=np.int32))
+    cl = np.ascontiguousarray(np.asarray(context_lens, dtype=np.int32))
+    S = cl.shape[0]
+    W = bt.shape[1] if bt.ndim == 2 else 1
+    if plan_bytes is None:
+        plan_bytes = pa_decode_plan_bytes(S, num_q_heads, num_kv_heads, head_dim, block_size, W, dtype)
+    plan = np.empty(plan_bytes // 4, dtype=np.int32)
+    st = _load().pa_decode_plan(plan.ctypes.data, plan_bytes, bt.ctypes.data if S else None, W,
+                                cl.ctypes.data if S else None, S, num_q_heads, num_kv_heads, head_dim,
+                                block_size, _dtype_arg(dtype))
+    _check(st, "pa_decode_plan")
+    return plan
+
+
+def pa_decode_planned(out, q, k_cache, v_cache, block_tables, context_lens, plan, scale: float,
+                      num_q_heads: int, num_kv_heads: int, head_dim: int, block_size: int,
+                      k_new=None, v_new=None, workspace=None, stream=None):
+    """pa_decode (balanced split), or with k_new/v_new pa_decode_append, whose CTAs
+    start where `plan` (a CUDA int32 copy of pa_decode_plan's output for the same
+    lengths and tables) says; bit-identical to the unplanned call."""
+    import torch
+    S = q.shape[0]
+    W = block_tables.shape[1]
+    if workspace is None:
+        workspace = alloc_workspace(S, num_q_heads, num_kv_heads, head_dim, block_size, W, 0, q.device,
+                                    stream)
+    if block_tables.dtype != torch.int32 or context_lens.dtype != torch.int32 or plan.dtype != torch.int32:
+        raise TypeError("block_tables, context_lens and plan must be int32")
+    st = _load().pa_decode_planned(_cuda(out, "out"), _cuda(q, "q"), _cuda(k_cache, "k_cache"),
+                                   _cuda(v_cache, "v_cache"),
+                                   _cuda(k_new, "k_new") if k_new is not None else None,
+                                   _cuda(v_new, "v_new") if v_new is not None else None,
+                                   _cuda(block_tables, "block_tables"), W,
+                                   _cuda(context_lens, "context_lens"), S, k_cache.shape[0], float(scale),
+                                   num_q_heads, num_kv_heads, head_dim, block_size, _dtype_code(q),
+                                   _cuda(plan, "plan"), plan.numel() * 4,
+                                   _cuda(workspace, "workspace") if workspace is not None else None,
+                                   workspace.numel() if workspace is not None else 0, _stream(stream))
+    _check(st, "pa_decode_planned")
+    return out
+
+
 def pa_decode_shared_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
                                     max_blocks_per_seq) -> int:
     n = _load().pa_decode_shared_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim,
@@ -327,7 +401,8 @@ def pa_device_errors(stream=None) -> int:
     return flags.value
 
 
-PA_DEVERR_TIMEOUT_FULL, PA_DEVERR_TIMEOUT_EMPTY, PA_DEVERR_SHARE = 1, 2, 4
+PA_DEVERR_TIMEOUT_FULL, PA_DEVERR_TIMEOUT_EMPTY, PA_DEVERR_SHARE, PA_DEVERR_PLAN = 1, 2, 4, 8
+PLAN_BYTES_PER_CTA = 128
 PA_WAIT_LIMIT_DEFAULT_NS = 2_000_000_000
 
 
@@ -529,7 +604,9 @@ def pa_kv_transfer_worthwhile(reusable_tokens: int, threshold_tokens: int = 64) 
     return bool(_load().pa_kv_transfer_worthwhile(int(reusable_tokens), int(threshold_tokens)))
 
 
-__all__ = ["pa_decode", "pa_decode_append", "pa_decode_shared", "pa_decode_shared_workspace_size",
+__all__ = ["pa_decode", "pa_decode_append", "pa_decode_plan_bytes", "pa_decode_plan", "pa_decode_planned",
+           "PA_DEVERR_PLAN", "PLAN_BYTES_PER_CTA",
+           "pa_decode_shared", "pa_decode_shared_workspace_size",
            "share_groups", "share_saving", "share_pays", "SHARE_MIN_SAVING", "SHARE_MIN_BYTES",
            "pa_decode_noalloc", "pa_decode_workspace_size", "pa_decode_partition_size", "alloc_workspace",
            "pa_reshape_and_cache", "pa_copy_blocks", "pa_swap_blocks", "pa_gather_blocks",

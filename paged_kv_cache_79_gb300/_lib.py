@@ -28,6 +28,12 @@ SIGNATURES = {
     "pa_decode_shared": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
                                  c_int, c_void_p, c_void_p, c_int, c_int, c_float, c_int, c_int, c_int,
                                  c_int, c_int, c_void_p, c_size_t, c_void_p]),
+    "pa_decode_plan_bytes": (c_size_t, [c_int] * 7),
+    "pa_decode_plan": (c_int, [c_void_p, c_size_t, c_void_p, c_int, c_void_p, c_int, c_int, c_int, c_int,
+                               c_int, c_int]),
+    "pa_decode_planned": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
+                                  c_int, c_void_p, c_int, c_int, c_float, c_int, c_int, c_int, c_int,
+                                  c_int, c_void_p, c_size_t, c_void_p, c_size_t, c_void_p]),
     "pa_decode_shared_workspace_size": (c_size_t, [c_int] * 6),
     "pa_share_groups": (c_int, [c_void_p, c_int, c_int, c_void_p, c_int, c_int, c_void_p]),
     "pa_decode_noalloc": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_void_p,

@@ -1,6 +1,7 @@
 // extern "C" entry points of libpagedkv.so: argument validation, tensor-map
 // encoding, partition sizing and kernel dispatch.  Declarations and the contract
 // of every function are in include/pagedkv.h.
+#include <algorithm>
 #include <atomic>
 #include <cmath>
 #include <cstring>
@@ -8,6 +9,7 @@
 #include <mutex>
 #include <random>
 #include <tuple>
+#include <vector>
 
 #include "pa_internal.h"
 
@@ -290,7 +292,7 @@ pa_status decode_impl(void *out, const void *q, const void *k_cache, const void 
                       int num_q_heads, int num_kv_heads, int head_dim, int block_size,
                       pa_dtype dtype, int partition_size, void *workspace, size_t workspace_bytes,
                       const void *k_new, const void *v_new, void *stream,
-                      const int32_t *share = nullptr)
+                      const int32_t *share = nullptr, const int32_t *plan = nullptr)
 {
     if (num_seqs == 0)
         return PA_OK;
@@ -365,6 +367,7 @@ pa_status decode_impl(void *out, const void *q, const void *k_cache, const void 
     if (!p.errors)
         return cuda_fail(ce);
     p.wait_ns = wait_limit_ns();
+    p.plan = (balanced && share == nullptr) ? plan : nullptr;
     p.scale_log2 = scale * 1.4426950408889634f;
     p.num_seqs = num_seqs;
     p.max_blocks = max_blocks_per_seq;
@@ -451,6 +454,164 @@ pa_status pa_decode_append(void *out, const void *q, void *k_cache, void *v_cach
     return decode_impl(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
                        num_seqs, num_blocks, scale, num_q_heads, num_kv_heads, head_dim, block_size,
                        dtype, partition_size, workspace, workspace_bytes, k_new, v_new, stream);
+}
+
+}  // extern "C"
+
+namespace {
+
+// Persistent grid of the planned decode's kernel instance on the current device
+// (0: cannot launch or no device).
+int plan_grid_for(pa_dtype dtype, int num_q_heads, int num_kv_heads, int head_dim, int block_size)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    const int sms = sm_count(dev);
+    if (sms <= 0)
+        return 0;
+    static const int32_t kSelectPlanned = 0;  // any non-null plan selects the instance
+    DecodeLaunch L;
+    std::memset(&L, 0, sizeof L);
+    L.p.plan = &kSelectPlanned;
+    L.p.balanced = 1;
+    L.p.num_q_heads = num_q_heads;
+    L.p.num_kv_heads = num_kv_heads;
+    L.p.group = num_q_heads / num_kv_heads;
+    L.p.head_groups = (L.p.group + kHeadsPerItem - 1) / kHeadsPerItem;
+    L.head_dim = head_dim;
+    L.block_size = block_size;
+    L.sm_count = sms;
+    L.grid = 0;
+    return dtype == PA_F32 ? plan_grid_f32(L) : dtype == PA_F16 ? plan_grid_f16(L) : plan_grid_bf16(L);
+}
+
+bool plan_args_ok(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                  int max_blocks_per_seq, int dtype)
+{
+    return dtype_ok(dtype) && num_seqs >= 0 &&
+           decode_shape_ok(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+                           max_blocks_per_seq, 0);
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t pa_decode_plan_bytes(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                            int block_size, int max_blocks_per_seq, pa_dtype dtype)
+{
+    if (!plan_args_ok(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq,
+                      dtype))
+        return (size_t)-1;
+    const int grid = plan_grid_for(dtype, num_q_heads, num_kv_heads, head_dim, block_size);
+    if (grid <= 0)
+        return (size_t)-1;
+    return (size_t)grid * kPlanInts * sizeof(int32_t);
+}
+
+pa_status pa_decode_plan(int32_t *plan, size_t plan_bytes, const int32_t *block_tables,
+                         int max_blocks_per_seq, const int32_t *context_lens, int num_seqs,
+                         int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                         pa_dtype dtype)
+{
+    if (!plan || (num_seqs > 0 && (!block_tables || !context_lens)))
+        return PA_ERR_INVALID;
+    if (!plan_args_ok(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq,
+                      dtype))
+        return PA_ERR_INVALID;
+    // one entry per CTA of the persistent grid: the plan's size gives the grid
+    const size_t entry = (size_t)kPlanInts * sizeof(int32_t);
+    if (plan_bytes == 0 || plan_bytes % entry != 0 || plan_bytes / entry > (1u << 20))
+        return PA_ERR_INVALID;
+    const int grid = (int)(plan_bytes / entry);
+    // the stream of the plain balanced split, as the kernel's walk builds it:
+    // sequence s contributes U units of kUnitCost + ceil(nb_s / bps) positions
+    const int W = max_blocks_per_seq, B = block_size;
+    const long long U = (long long)num_kv_heads * ((num_q_heads / num_kv_heads + kHeadsPerItem - 1) /
+                                                   kHeadsPerItem);
+    const int bps = blocks_per_stage(dtype == PA_F32 ? 4 : 2, B);
+    std::vector<long long> start((size_t)num_seqs + 1, 0);
+    std::vector<int> len((size_t)num_seqs), ns((size_t)num_seqs);
+    for (int s = 0; s < num_seqs; ++s) {
+        const long long t = context_lens[s];
+        len[s] = (int)std::min<long long>(std::max<long long>(t, 0), (long long)W * B);
+        const int nb = (len[s] + B - 1) / B;
+        ns[s] = (nb + bps - 1) / bps;
+        start[s + 1] = start[s] + U * (kUnitCost + ns[s]);
+    }
+    const long long total = start[num_seqs];
+    const int div = balanced_divisor(total, (long long)num_seqs * U);
+    const long long G = num_seqs > 0 ? balanced_grid_of(total, div, grid) : 0;
+    std::memset(plan, 0, (size_t)grid * kPlanInts * sizeof(int32_t));
+    auto put64 = [](int32_t *e, int f, long long v) {
+        e[f] = (int32_t)(uint32_t)(v & 0xffffffffll);
+        e[f + 1] = (int32_t)(v >> 32);
+    };
+    for (int c = 0; c < grid; ++c) {
+        int32_t *e = plan + (size_t)c * kPlanInts;
+        e[kPlanSeq] = -1;
+        put64(e, kPlanTotal, total);
+        e[kPlanDiv] = div;
+        e[kPlanG] = (int32_t)G;
+        e[kPlanGrid] = grid;
+        e[kPlanSeqs] = num_seqs;
+        if (c >= G)
+            continue;
+        const long long s_c = c * total / G, e_c = (c + 1) * total / G;
+        // the sequence whose positions hold s_c
+        const int s = (int)(std::upper_bound(start.begin(), start.end(), s_c) - start.begin()) - 1;
+        const long long base = start[s];
+        e[kPlanSeq] = s;
+        put64(e, kPlanBase, base);
+        e[kPlanLen] = len[s];
+        put64(e, kPlanStart, s_c);
+        put64(e, kPlanEnd, e_c);
+        // the first item's first block, when it is in unit (s_c - base) / span of s
+        const long long span = kUnitCost + ns[s];
+        const long long a = base + (s_c > base ? (s_c - base) / span : 0) * span;
+        const long long ra = a + kUnitCost;
+        const int nb = (len[s] + B - 1) / B;
+        const int j0 = (int)std::min<long long>((std::max(ra, s_c) - ra) * bps, nb);
+        e[kPlanJ0] = j0;
+        for (int k = 0; k < kPlanWindow; ++k) {
+            const int j = j0 + k;
+            e[kPlanBlocks + k] = j < W ? block_tables[(size_t)s * W + j] : -1;
+        }
+    }
+    return PA_OK;
+}
+
+pa_status pa_decode_planned(void *out, const void *q, void *k_cache, void *v_cache,
+                            const void *k_new, const void *v_new, const int32_t *block_tables,
+                            int max_blocks_per_seq, const int32_t *context_lens, int num_seqs,
+                            int num_blocks, float scale, int num_q_heads, int num_kv_heads,
+                            int head_dim, int block_size, pa_dtype dtype, const int32_t *plan,
+                            size_t plan_bytes, void *workspace, size_t workspace_bytes, void *stream)
+{
+    if (num_seqs == 0)
+        return PA_OK;
+    if ((k_new == nullptr) != (v_new == nullptr) ||
+        (k_new && (!aligned(k_new, 16) || !aligned(v_new, 16))))
+        return PA_ERR_INVALID;
+    if (!plan || !aligned(plan, 16))
+        return PA_ERR_INVALID;
+    const size_t need = pa_decode_plan_bytes(num_seqs, num_q_heads, num_kv_heads, head_dim,
+                                             block_size, max_blocks_per_seq, dtype);
+    if (need == (size_t)-1) {
+        // invalid sizes: let the common validation report them
+        return decode_impl(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq,
+                           context_lens, num_seqs, num_blocks, scale, num_q_heads, num_kv_heads,
+                           head_dim, block_size, dtype, 0, workspace, workspace_bytes, k_new, v_new,
+                           stream);
+    }
+    if (plan_bytes != need)
+        return PA_ERR_INVALID;
+    return decode_impl(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
+                       num_seqs, num_blocks, scale, num_q_heads, num_kv_heads, head_dim, block_size,
+                       dtype, 0, workspace, workspace_bytes, k_new, v_new, stream, nullptr, plan);
 }
 
 size_t pa_decode_shared_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads,
@@ -638,7 +799,7 @@ pa_status pa_device_errors(unsigned int *flags, void *stream)
     *flags = v;
     if (v & (PA_DEVERR_TIMEOUT_FULL | PA_DEVERR_TIMEOUT_EMPTY))
         return PA_ERR_TIMEOUT;
-    return (v & PA_DEVERR_SHARE) ? PA_ERR_INVALID : PA_OK;
+    return (v & (PA_DEVERR_SHARE | PA_DEVERR_PLAN)) ? PA_ERR_INVALID : PA_OK;
 }
 
 unsigned long long pa_set_wait_limit_ns(unsigned long long ns)

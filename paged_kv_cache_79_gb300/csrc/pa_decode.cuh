@@ -47,9 +47,6 @@
 
 namespace pagedkv {
 
-#ifndef PA_STAGE_TOKENS
-#define PA_STAGE_TOKENS 32  // tokens per ring stage (fp16/bf16): blocks of 16 go two per stage
-#endif
 #ifndef PA_RING_BYTES
 #define PA_RING_BYTES 65536  // shared memory of the stage ring (two CTAs per SM)
 #endif
@@ -251,6 +248,7 @@ constexpr int kMergePrefix = 2;  // result rows are merged with the shared-prefi
 constexpr int kModePlain = 0;   // pa_decode, pa_decode_append
 constexpr int kModePrefix = 1;  // shared-prefix decode, pass 1: the groups' shared blocks
 constexpr int kModeOwn = 2;     // shared-prefix decode, pass 0: every sequence's own blocks
+constexpr int kModePlan = 3;    // pa_decode_planned: the plain decode, each CTA's start planned on the host
 
 // A work item: blocks [j0, j1) of one unit.  Row r of the item is query head
 // qrow0 + r % rpm of sequence seq + r / rpm (several sequences only in the
@@ -460,13 +458,19 @@ struct Producer {
     uint32_t g;  // stages issued
     uint32_t n;  // items published
     bool failed;
+    // pa_decode_planned: the block ids of the CTA's first item's first window, one
+    // per lane from lane 16 on (kPlanWindow of them); plan_seq < 0 once used
+    int plan_blk;
+    int plan_seq;
+    int plan_j0;
 #ifdef PA_TRACE
     unsigned long long t_last_issue;
 #endif
 
     __device__ Producer(const DecodeParams &p_, const CUtensorMap *tk_, const CUtensorMap *tv_,
                         const CtaState &c_, int lane_)
-        : p(p_), tk(tk_), tv(tv_), c(c_), lane(lane_), g(0), n(0), failed(false)
+        : p(p_), tk(tk_), tv(tv_), c(c_), lane(lane_), g(0), n(0), failed(false), plan_blk(0),
+          plan_seq(-1), plan_j0(0)
     {
 #ifdef PA_TRACE
         t_last_issue = 0;
@@ -511,10 +515,20 @@ struct Producer {
             ++n;
         }
         const int32_t *row = p.block_tables + (size_t)it.tseq * p.max_blocks;
-        for (int jb = it.j0; jb < it.j1; jb += 32) {
+        // a planned first item takes its first kPlanWindow block ids from the plan
+        // (no block-table round trip before its first copies), then 32 at a time
+        const bool planned = plan_seq == it.tseq && plan_j0 == it.j0;
+        plan_seq = -1;
+        for (int jb = it.j0, wnd = 32; jb < it.j1; jb += wnd) {
+            const bool from_plan = planned && jb == it.j0;
+            wnd = from_plan ? kPlanWindow : 32;
             const int j = jb + lane;
-            const int phys = (j < it.j1) ? row[j] : 0;  // one coalesced read per 32 blocks
-            const int cnt = min(32, it.j1 - jb);
+            int phys;
+            if (from_plan)
+                phys = __shfl_sync(0xffffffffu, plan_blk, (lane % kPlanWindow) + kPlanBlocks);
+            else
+                phys = (j < it.j1) ? row[j] : 0;  // one coalesced read per 32 blocks
+            const int cnt = min(wnd, it.j1 - jb);
             for (int i = 0; i < cnt; i += kBPS, ++g) {
                 const int nbs = min(kBPS, cnt - i);  // blocks in this stage
                 const uint32_t st = g % kStages;
@@ -547,8 +561,10 @@ struct Producer {
                     const int newest = it.len - 1 - (jb + i) * BS;
                     const bool has_new = p.k_new != nullptr && newest >= 0 && newest < nbs * BS;
                     c.newinfo[2 * st] = has_new ? newest : -1;
+                    // the block the newest token is written to always comes from the
+                    // table, so a stale plan cannot direct the append elsewhere
                     if (has_new)
-                        c.newinfo[2 * st + 1] = ph[newest / BS];
+                        c.newinfo[2 * st + 1] = from_plan ? row[jb + i + newest / BS] : ph[newest / BS];
                     constexpr uint32_t kRowBytes = D * sizeof(T);
                     dev::mbar_arrive_expect_tx(
                         fb, 2u * (uint32_t)nbs * (kTileBytes / kBPS) + (has_new ? 2u * kRowBytes : 0u));
@@ -647,11 +663,6 @@ struct Producer {
 // prefixes, (kv head, head group, sequence) -- form one stream of `total`
 // positions; CTA c of G takes positions [c * total / G, (c + 1) * total / G).
 // ---------------------------------------------------------------------------
-#ifndef PA_UNIT_COST
-#define PA_UNIT_COST 4
-#endif
-constexpr int kUnitCost = PA_UNIT_COST;
-static_assert(kUnitCost >= 1, "every unit needs a start position");
 // The units a sequence contributes to the stream of the current pass.
 //   pass 0: (kv head, head group) units over blocks [start, nb) -- start is the
 //           shared prefix length of a grouped sequence (its rows then merge with the
@@ -743,6 +754,21 @@ __device__ __forceinline__ SeqUnits seq_units(const DecodeParams &p, int s, int 
     return u;
 }
 
+// Units of a sequence of the plain decode from its (clamped) context length.
+__device__ __forceinline__ SeqUnits seq_units_of_len(const DecodeParams &p, int len, int bs, int bps)
+{
+    SeqUnits u;
+    u.members = 1;
+    u.mgroups = 1;
+    const int nb = (len + bs - 1) / bs;
+    u.nunits = p.num_kv_heads * p.head_groups;
+    u.ns = (nb + bps - 1) / bps;
+    u.start = 0;
+    u.nb = nb;
+    u.len = len;
+    return u;
+}
+
 __device__ __forceinline__ long long warp_sum_ll(long long v)
 {
 #pragma unroll
@@ -821,22 +847,10 @@ __device__ __forceinline__ int find_seq_at(const DecodeParams &p, int bs, int bp
 // grid exits at once.  (Cutting the stream into more, dynamically claimed chunks
 // than CTAs evens out the end of a launch but costs more than it saves here: each
 // extra cut adds a split unit, with its fences and count, and a claim round trip.)
-#ifndef PA_MIN_POSITIONS
-#define PA_MIN_POSITIONS 4
-#endif
-constexpr long long kMinPositions = PA_MIN_POSITIONS;
-// Positions per CTA at least: kMinPositions, or, for a batch of short units (8
-// positions or fewer on average), the average unit, so that a few short units give
-// each CTA about one whole unit instead of cutting every unit in two.
-__device__ __forceinline__ int balanced_divisor(long long total, long long units)
-{
-    const long long avg = units > 0 ? (total + units - 1) / units : 1;
-    return (int)(avg <= 8 && avg > kMinPositions ? avg : kMinPositions);
-}
+// (kMinPositions, balanced_divisor: pa_internal.h.)
 __device__ __forceinline__ long long balanced_grid(long long total, int divisor)
 {
-    const long long g = (total + divisor - 1) / divisor;
-    return g < 1 ? 1 : (g < (long long)gridDim.x ? g : (long long)gridDim.x);
+    return balanced_grid_of(total, divisor, (long long)gridDim.x);
 }
 
 // CTA of a G-CTA grid whose stage range contains stream stage x.
@@ -975,6 +989,58 @@ __device__ __forceinline__ bool walk_chunk_unit_major(const DecodeParams &p, int
     return !*pr.c.abort;
 }
 
+// pa_decode_planned: the walk of the plain balanced split from the CTA's start as
+// the host computed it (pa_decode_plan).  The stream total, the CTA's range, its
+// first sequence with that sequence's first position and length, and the block ids
+// of its first item's first window come from the plan, so the first copies need
+// no pass over the context lengths and no block-table read.  Later sequences'
+// lengths are read as the walk reaches them.  The items are the ones the walk from
+// scratch emits.  A plan made for other lengths gives wrong rows but never an
+// access outside the arguments: every field is bounded before use, the CTA count
+// is recomputed from the total as the merge recomputes it, and a walk whose
+// positions would pass the total stops and raises PA_DEVERR_PLAN.
+template <class Prod>
+__device__ __forceinline__ void walk_planned(const DecodeParams &p, int bs, int bps, Prod &pr,
+                                             int lane)
+{
+    const int v = p.plan[(size_t)blockIdx.x * kPlanInts + lane];
+    auto get = [&](int f) { return __shfl_sync(0xffffffffu, v, f); };
+    auto get64 = [&](int f) {
+        return (long long)(unsigned)get(f) | ((long long)get(f + 1) << 32);
+    };
+    const long long total = max(get64(kPlanTotal), 1ll);
+    const int div = min(max(get(kPlanDiv), (int)kMinPositions), 8);
+    const long long G = balanced_grid(total, div);
+    const int seq = get(kPlanSeq);
+    if ((long long)blockIdx.x >= G || seq < 0 || seq >= p.num_seqs)
+        return;
+    const long long e_c = min(max(get64(kPlanEnd), 0ll), total);
+    const long long s_c = min(max(get64(kPlanStart), 0ll), e_c);
+    long long base = min(max(get64(kPlanBase), 0ll), s_c);
+    const int len0 = min(max(get(kPlanLen), 0), p.max_blocks * bs);
+    pr.plan_blk = v;
+    pr.plan_seq = seq;
+    pr.plan_j0 = get(kPlanJ0);
+    const long long cta = blockIdx.x;
+    for (int s = seq; s < p.num_seqs && base < e_c && !*pr.c.abort; ++s) {
+        const SeqUnits su =
+            s == seq ? seq_units_of_len(p, len0, bs, bps) : seq_units<false>(p, s, bs, bps);
+        const long long span = kUnitCost + su.ns;
+        if (base + (long long)su.nunits * span > total) {
+            if (lane == 0)
+                atomicOr(p.errors, PA_DEVERR_PLAN);
+            return;
+        }
+        const long long u_lo = s_c > base ? (s_c - base) / span : 0;
+        const long long u_hi = min((long long)su.nunits - 1, (e_c - 1 - base) / span);
+        for (long long u = u_lo; u <= u_hi; ++u)
+            if (!emit_unit<false>(p, pr, su, s, u, base + u * span, s_c, e_c, total, G, cta, bps,
+                                  div))
+                return;
+        base += (long long)su.nunits * span;
+    }
+}
+
 // The producer's walk of the balanced split: CTA c streams positions
 // [c * total / G, (c + 1) * total / G).  The own-block launch of the shared-prefix
 // decode takes the (unit, sequence) order when the batch has shared prefixes.
@@ -982,7 +1048,7 @@ template <int kMode, class Prod>
 __device__ __forceinline__ void walk_balanced(const DecodeParams &p, int bs, int bps, Prod &pr,
                                               int lane)
 {
-    constexpr bool kShare = kMode != kModePlain;
+    constexpr bool kShare = kMode == kModePrefix || kMode == kModeOwn;
     constexpr bool kOwn = kMode == kModeOwn;
     long long units = 0;
     bool prefix = false;
@@ -1016,7 +1082,9 @@ __device__ __forceinline__ void producer_loop(const DecodeParams &p, const CUten
                                               const CUtensorMap *tv, const CtaState &c, int lane)
 {
     Producer<T, D, BS, kBPS, kChunks, kTileBytes, kStages> pr(p, tk, tv, c, lane);
-    if (p.balanced)
+    if constexpr (kMode == kModePlan)
+        walk_planned(p, BS, kBPS, pr, lane);
+    else if (p.balanced)
         walk_balanced<kMode>(p, BS, kBPS, pr, lane);
     else
         walk_fixed(p, BS, pr, lane);
@@ -1360,12 +1428,14 @@ __device__ __forceinline__ bool finish_item(const DecodeParams &p, const Item &i
 // to the stage) into row `r` of the stage's swizzled tiles, and store them into the
 // cache at (physical block, r % block_size).  Nothing else in the launch reads those
 // cache bytes: only this (sequence, kv head) unit covers them, and it uses the
-// staged copy.  One 16-byte unit per lane per pass.
+// staged copy.  One 16-byte unit per lane per pass.  append_ok false (a planned
+// item whose context length is not the one the launch reads): the tile is patched
+// but nothing is stored to the cache, and PA_DEVERR_PLAN is raised.
 // ---------------------------------------------------------------------------
 template <typename T, int D, int TS, int BS>
 __device__ __forceinline__ void patch_newest_row(const DecodeParams &p, const Item &it,
                                               const CtaState &c, uint32_t st, uint8_t *ktile,
-                                              uint8_t *vtile, int lane)
+                                              uint8_t *vtile, int lane, bool append_ok)
 {
     constexpr int kUnits = D * (int)sizeof(T) / 16;  // 16-byte units per row
     constexpr int kUnitElems = 16 / (int)sizeof(T);
@@ -1374,7 +1444,9 @@ __device__ __forceinline__ void patch_newest_row(const DecodeParams &p, const It
     const int blk = c.newinfo[2 * st + 1];
     const uint8_t *staged = c.newrow + (size_t)st * 2 * D * sizeof(T);
     const size_t dst = (((size_t)blk * BS + r % BS) * p.num_kv_heads + it.kvh) * D;
-    const bool store = it.hg == 0 && blk >= 0 && blk < p.num_blocks;
+    const bool store = append_ok && it.hg == 0 && blk >= 0 && blk < p.num_blocks;
+    if (!append_ok && lane == 0)
+        atomicOr(p.errors, PA_DEVERR_PLAN);
     for (int idx = lane; idx < 2 * kUnits; idx += 32) {
         const bool isv = idx >= kUnits;
         const int u = isv ? idx - kUnits : idx;
@@ -1403,7 +1475,7 @@ __device__ __forceinline__ void patch_newest_row(const DecodeParams &p, const It
 template <typename T, int D, int BS>
 __device__ __forceinline__ bool consume_item_n8(const DecodeParams &p, const CtaState &c,
                                                 const Item &it, uint32_t slot, uint32_t &g,
-                                                int warp, int lane, int rows_cap)
+                                                int warp, int lane, int rows_cap, bool append_ok)
 {
     using C = Cfg<T, D, BS>;
     constexpr int kCE = C::kChunkElems;
@@ -1482,7 +1554,7 @@ __device__ __forceinline__ bool consume_item_n8(const DecodeParams &p, const Cta
         if (c.newinfo[2 * st] >= 0)
             patch_newest_row<T, D, TS, BS>(p, it, c, st, c.ring + (size_t)st * C::kStageBytes,
                                            c.ring + (size_t)st * C::kStageBytes + C::kTileBytes,
-                                           lane);
+                                           lane, append_ok);
 
         // S^T = K Q^T: the K tile (rows = tokens) is the row-major A operand.
         // Two accumulators per token tile (even / odd k-steps) shorten the chains.
@@ -1643,7 +1715,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int rows_cap = item_rows_cap(p);
-    constexpr bool kShare = kMode != kModePlain;
+    constexpr bool kShare = kMode == kModePrefix || kMode == kModeOwn;
     const int pfx_rows = kShare ? item_pfx_rows(p) : 0;
     const SmemLayout lay =
         make_layout(C::kStages, C::kStageBytes, rows_cap, D, sizeof(T), pfx_rows);
@@ -1690,12 +1762,16 @@ __global__ void __launch_bounds__(kThreads, 2)
         const Item it = load_item(&c.items[slot]);
         if (it.seq < 0)
             break;
+        // a planned first item takes its length from the plan: its append is stored
+        // only if that is the length the launch reads (read here, used stages later)
+        const bool append_ok =
+            kMode != kModePlan || p.k_new == nullptr || clamp_len(p, it.tseq, BS) == it.len;
         const bool merge_pfx = kShare && (it.flags() & kMergePrefix) != 0;
         float *pfx_s = c.pfx + (n & 1) * pfx_rows * (D + kPfxPad);
         if (merge_pfx && pfx_ready)
             stage_prefix<D>(p, it, pfx_s, threadIdx.x);
         if constexpr (N8) {
-            if (!consume_item_n8<T, D, BS>(p, c, it, slot, g, warp, lane, rows_cap))
+            if (!consume_item_n8<T, D, BS>(p, c, it, slot, g, warp, lane, rows_cap, append_ok))
                 break;
         } else {
         const bool live0 = r0 < it.rows, live1 = r0 + 8 < it.rows;
@@ -1769,7 +1845,7 @@ __global__ void __launch_bounds__(kThreads, 2)
             if (c.newinfo[2 * st] >= 0)
                 patch_newest_row<T, D, TS, BS>(p, it, c, st, c.ring + (size_t)st * C::kStageBytes,
                                                c.ring + (size_t)st * C::kStageBytes + C::kTileBytes,
-                                               lane);
+                                               lane, append_ok);
 
             // S = Q K^T: K tile rows are tokens, so plain ldmatrix yields the
             // "col" B fragment (k = head dim, n = token).
@@ -1963,7 +2039,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int rows_cap = item_rows_cap(p);
-    constexpr bool kShare = kMode != kModePlain;
+    constexpr bool kShare = kMode == kModePrefix || kMode == kModeOwn;
     const int pfx_rows = kShare ? item_pfx_rows(p) : 0;
     const SmemLayout lay =
         make_layout(C::kStages, C::kStageBytes, rows_cap, D, sizeof(float), pfx_rows);
@@ -1999,6 +2075,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const Item it = load_item(&c.items[slot]);
         if (it.seq < 0)
             break;
+        // a planned first item takes its length from the plan: its append is stored
+        // only if that is the length the launch reads (read here, used stages later)
+        const bool append_ok =
+            kMode != kModePlan || p.k_new == nullptr || clamp_len(p, it.tseq, BS) == it.len;
         const bool merge_pfx = kShare && (it.flags() & kMergePrefix) != 0;
         float *pfx_s = c.pfx + (n & 1) * pfx_rows * (D + kPfxPad);
         if (merge_pfx && pfx_ready)
@@ -2044,7 +2124,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 patch_newest_row<float, D, BS, BS>(p, it, c, st, c.ring + (size_t)st * C::kStageBytes,
                                                    c.ring + (size_t)st * C::kStageBytes +
                                                        C::kTileBytes,
-                                                   lane);
+                                                   lane, append_ok);
 
             float sc[H];
 #pragma unroll
@@ -2264,10 +2344,12 @@ __global__ void __launch_bounds__(128)
 // ---------------------------------------------------------------------------
 // Launch helpers
 // ---------------------------------------------------------------------------
-// The kernel instance a launch takes: plain decode, or one of the shared-prefix
-// decode's two launches.
+// The kernel instance a launch takes: plain decode (walked or planned), or one of
+// the shared-prefix decode's two launches.
 inline int launch_mode(const DecodeParams &p)
 {
+    if (p.plan != nullptr)
+        return kModePlan;
     if (p.share == nullptr)
         return kModePlain;
     return p.pass == 1 ? kModePrefix : kModeOwn;
@@ -2289,6 +2371,7 @@ struct KernelOf {
         const int mode = launch_mode(p);
         return mode == kModeOwn ? pick<kModeOwn>(p)
                : mode == kModePrefix ? pick<kModePrefix>(p)
+               : mode == kModePlan ? pick<kModePlan>(p)
                                      : pick<kModePlain>(p);
     }
 };
@@ -2310,6 +2393,7 @@ struct KernelOf<float, D, BS> {
         const int mode = launch_mode(p);
         return mode == kModeOwn ? pick<kModeOwn>(p)
                : mode == kModePrefix ? pick<kModePrefix>(p)
+               : mode == kModePlan ? pick<kModePlan>(p)
                                      : pick<kModePlain>(p);
     }
 };
@@ -2324,23 +2408,47 @@ inline size_t smem_bytes_for(int rows, int pfx_rows = 0)
 
 int cached_occupancy(void *kernel, int device, size_t smem, size_t max_smem);
 
+// The persistent grid of a launch: its kernel instance's resident CTAs per SM (at
+// most kMaxCtasPerSm) times the SMs, or L.grid if that is smaller; 0 if the
+// configuration cannot launch.  pa_decode_plan sizes its plan with the same count.
+template <typename T, int D, int BS>
+long long persistent_grid(const DecodeLaunch &L, void *kern, size_t smem, cudaError_t *err)
+{
+    const size_t smem_max = smem_bytes_for<T, D, BS>(kHeadsPerItem, kHeadsPerItem);
+    int dev = 0;
+    *err = cudaGetDevice(&dev);
+    if (*err != cudaSuccess)
+        return 0;
+    const int per_sm = cached_occupancy(kern, dev, smem, smem_max);
+    if (per_sm <= 0)
+        return 0;
+    long long grid = (long long)min(per_sm, kMaxCtasPerSm) * L.sm_count;
+    if (L.grid > 0 && L.grid < grid)
+        grid = L.grid;
+    return grid;
+}
+
+template <typename T, int D, int BS>
+int plan_grid_impl(const DecodeLaunch &L)
+{
+    void *kern = KernelOf<T, D, BS>::get(L.p);
+    const size_t smem = smem_bytes_for<T, D, BS>(item_rows_cap(L.p), item_pfx_rows(L.p));
+    cudaError_t e = cudaSuccess;
+    return (int)persistent_grid<T, D, BS>(L, kern, smem, &e);
+}
+
 template <typename T, int D, int BS>
 cudaError_t launch_decode_impl(const DecodeLaunch &L, cudaStream_t stream)
 {
     const DecodeParams &p = L.p;
     void *kern = KernelOf<T, D, BS>::get(p);
     const size_t smem = smem_bytes_for<T, D, BS>(item_rows_cap(p), item_pfx_rows(p));
-    const size_t smem_max = smem_bytes_for<T, D, BS>(kHeadsPerItem, kHeadsPerItem);
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+    cudaError_t e = cudaSuccess;
+    long long grid = persistent_grid<T, D, BS>(L, kern, smem, &e);
     if (e != cudaSuccess)
         return e;
-    const int per_sm = cached_occupancy(kern, dev, smem, smem_max);
-    if (per_sm <= 0)
+    if (grid <= 0)
         return cudaErrorInvalidConfiguration;
-    long long grid = (long long)min(per_sm, kMaxCtasPerSm) * L.sm_count;
-    if (L.grid > 0 && L.grid < grid)
-        grid = L.grid;
     if (!p.balanced) {
         const long long items =
             (long long)p.num_seqs * p.max_parts * p.num_kv_heads * p.head_groups;
@@ -2396,6 +2504,20 @@ cudaError_t launch_decode_dispatch(const DecodeLaunch &L, cudaStream_t stream)
     if (L.head_dim == 64 && L.block_size == 32)
         return launch_decode_impl<T, 64, 32>(L, stream);
     return cudaErrorInvalidValue;
+}
+
+template <typename T>
+int plan_grid_dispatch(const DecodeLaunch &L)
+{
+    if (L.head_dim == 128 && L.block_size == 16)
+        return plan_grid_impl<T, 128, 16>(L);
+    if (L.head_dim == 128 && L.block_size == 32)
+        return plan_grid_impl<T, 128, 32>(L);
+    if (L.head_dim == 64 && L.block_size == 16)
+        return plan_grid_impl<T, 64, 16>(L);
+    if (L.head_dim == 64 && L.block_size == 32)
+        return plan_grid_impl<T, 64, 32>(L);
+    return 0;
 }
 
 template <typename T>

@@ -62,6 +62,9 @@ struct DecodeParams {
     // Limit of every bounded wait of the launch (ns), but for the drain of copies in
     // flight; kWaitTimeoutNs unless pa_set_wait_limit_ns changed it.
     unsigned long long wait_ns;
+    // Plain balanced-split decode: kPlanInts per CTA of the host-computed start
+    // (pa_decode_plan), or null to walk the stream on the device.
+    const int32_t *plan;
 };
 
 // The wait limit decode launches take (pa_set_wait_limit_ns).
@@ -69,6 +72,60 @@ unsigned long long wait_limit_ns();
 
 // Balanced split: partial slots are reserved for at most this many CTAs per SM.
 constexpr int kMaxCtasPerSm = 4;
+
+// Schedule constants shared by the kernels and the host-side plan
+// (pa_decode_plan), which replays the balanced split's walk.
+#ifndef PA_STAGE_TOKENS
+#define PA_STAGE_TOKENS 32  // tokens per ring stage (fp16/bf16): blocks of 16 go two per stage
+#endif
+#ifndef PA_UNIT_COST
+#define PA_UNIT_COST 4      // stream positions charged per unit for its fixed cost
+#endif
+#ifndef PA_MIN_POSITIONS
+#define PA_MIN_POSITIONS 4  // stream positions per CTA at least
+#endif
+constexpr int kUnitCost = PA_UNIT_COST;
+constexpr long long kMinPositions = PA_MIN_POSITIONS;
+static_assert(kUnitCost >= 1, "every unit needs a start position");
+
+// Blocks per ring stage of the partition kernel for a storage type of elem_bytes.
+inline int blocks_per_stage(int elem_bytes, int block_size)
+{
+    return (elem_bytes == 4 || PA_STAGE_TOKENS <= block_size) ? 1 : PA_STAGE_TOKENS / block_size;
+}
+
+// Balanced split: positions per CTA at least -- kMinPositions, or, for a batch of
+// short units (8 positions or fewer on average), the average unit -- and the CTAs
+// a stream of `total` positions is spread over (at most `grid`).
+__host__ __device__ __forceinline__ int balanced_divisor(long long total, long long units)
+{
+    const long long avg = units > 0 ? (total + units - 1) / units : 1;
+    return (int)(avg <= 8 && avg > kMinPositions ? avg : kMinPositions);
+}
+__host__ __device__ __forceinline__ long long balanced_grid_of(long long total, int divisor, long long grid)
+{
+    const long long g = (total + divisor - 1) / divisor;
+    return g < 1 ? 1 : (g < grid ? g : grid);
+}
+
+// Host-computed start of each CTA of a balanced-split launch (pa_decode_plan):
+// kPlanInts int32 per CTA of the persistent grid, in this order.
+constexpr int kPlanInts = 32;
+enum PlanField {
+    kPlanSeq = 0,       // sequence whose positions hold the CTA's first position
+    kPlanBase = 1,      // first position of that sequence (int64: lo, hi)
+    kPlanLen = 3,       // its context length, clamped to the table
+    kPlanTotal = 4,     // positions of the whole stream (int64: lo, hi)
+    kPlanDiv = 6,       // positions per CTA at least
+    kPlanG = 7,         // CTAs the stream is spread over
+    kPlanGrid = 8,      // persistent grid the plan was made for
+    kPlanStart = 9,     // the CTA's range [start, end) (int64 each: lo, hi)
+    kPlanEnd = 11,
+    kPlanJ0 = 13,       // first block of the CTA's first item
+    kPlanSeqs = 14,     // batch size the plan was made for
+    kPlanBlocks = 16,   // block ids j0 .. j0 + 15 of the first item's sequence (-1 past it)
+};
+constexpr int kPlanWindow = kPlanInts - kPlanBlocks;
 
 struct DecodeLaunch {
     DecodeParams p;
@@ -79,6 +136,12 @@ struct DecodeLaunch {
     int grid;                     // 0: let the launcher size it from occupancy
     int sm_count;
 };
+
+// Persistent grid (CTAs) of a balanced-split launch of the plain decode with a
+// plan; 0 if the configuration cannot launch.
+int plan_grid_f32(const DecodeLaunch &L);
+int plan_grid_f16(const DecodeLaunch &L);
+int plan_grid_bf16(const DecodeLaunch &L);
 
 // Per-dtype launchers (pa_decode_{f32,f16,bf16}.cu).  They size the persistent
 // grid from occupancy, launch the partition kernel and, when any sequence can

@@ -14,8 +14,8 @@ from typing import Callable, List, Optional
 import numpy as np
 
 from . import (BlockAllocator, alloc_workspace, pa_copy_blocks, pa_decode, pa_decode_append,
-               pa_decode_shared, pa_decode_shared_workspace_size, pa_reshape_and_cache,
-               share_groups, share_pays)
+               pa_decode_plan, pa_decode_planned, pa_decode_shared, pa_decode_shared_workspace_size,
+               pa_reshape_and_cache, share_groups, share_pays)
 
 
 def _kind(ev) -> str:
@@ -56,6 +56,22 @@ class DecodeStep:
     fusable: bool = True        # step rows are the batch's newest tokens, in batch order
     share: "object" = None      # int32 [S, 2] shared-prefix groups, None if none share
     share_pays: bool = False    # the groups save enough reads for pa_decode_shared (share_pays)
+    plan: "object" = None       # int32 device copy of pa_decode_plan for these tables and lengths
+
+    def run_planned(self, stream=None):
+        """copy-on-write pairs, then the balanced-split decode with its CTAs starting
+        where the host plan says (pa_decode_planned), the new tokens appended in the
+        launch when the step is fusable, else before it."""
+        if self.pairs.shape[0]:
+            pa_copy_blocks(self.k_cache, self.v_cache, self.pairs, stream)
+        if not self.fusable:
+            pa_reshape_and_cache(self.step_k, self.step_v, self.k_cache, self.v_cache, self.slots, stream)
+        return pa_decode_planned(self.out, self.q, self.k_cache, self.v_cache, self.block_tables,
+                                 self.context_lens, self.plan, self.scale, self.num_q_heads,
+                                 self.num_kv_heads, self.head_dim, self.block_size,
+                                 k_new=self.step_k if self.fusable else None,
+                                 v_new=self.step_v if self.fusable else None,
+                                 workspace=self.workspace, stream=stream)
 
     def run_shared(self, stream=None):
         """copy-on-write pairs, then the shared-prefix decode (which also appends the new
@@ -191,6 +207,8 @@ def execute(w, k_cache, v_cache, step_kv: Callable, query: Callable,
                 head_dim=w.head_dim, block_size=w.block_size, partition_size=w.partition_size,
                 fusable=fusable,
                 share=torch.from_numpy(share).to(dev) if has_share else None,
+                plan=torch.from_numpy(pa_decode_plan(bt, cl, w.num_q_heads, w.num_kv_heads, w.head_dim,
+                                                     w.block_size, k_cache.dtype)).to(dev),
                 share_pays=has_share and share_pays(
                     share, cl, w.block_size,
                     2 * w.block_size * w.num_kv_heads * w.head_dim * k_cache.element_size()))

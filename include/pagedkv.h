@@ -105,7 +105,12 @@ int pa_last_cuda_error(void);
  * Arguments
  *   out            device, [S][Hq][d], dtype `dtype`, written
  *   q              device, [S][Hq][d], dtype `dtype`
- *   k_cache/v_cache device, [num_blocks][B][Hkv][d], dtype `dtype`
+ *   k_cache/v_cache device, [num_blocks][B][Hkv][d], dtype `dtype`; two separate
+ *                  buffers or one.  When v_cache lies above k_cache, a multiple of
+ *                  16 bytes and less than 2^40 bytes away (for instance both halves
+ *                  of one [2][num_blocks][B][Hkv][d] buffer), every block's K and V
+ *                  tiles arrive with one copy instead of two, which streams faster;
+ *                  the results are the same either way.
  *   block_tables   device int32 [S][max_blocks_per_seq]; referenced entries must be
  *                  in [0, num_blocks) (an entry outside reads zeros, never faults)
  *   context_lens   device int32 [S]

@@ -84,28 +84,45 @@ EncodeTiledFn encode_fn()
     return fn;
 }
 
-// Cache [num_blocks][B][Hkv][d] seen as 4-D: (128-byte row of d, row index within
-// d, kv head, token slot).  One box = one kv head of one block, 128-byte swizzle.
-bool make_cache_map(CUtensorMap *map, const void *base, pa_dtype dt, int num_blocks, int B,
-                    int Hkv, int D)
+// Cache [num_blocks][B][Hkv][d] seen as 4-D: (element within a 128-byte row of d,
+// token slot, 128-byte row of d, kv head).  One box = one kv head of one block:
+// its B token rows, each d / (128 bytes) rows of 128 bytes, landing chunk-major
+// (all tokens' first 128 bytes of d, then the next), with 128-byte swizzle.
+// With `vbase` (above `base`, a multiple of 16 bytes away) a fifth dimension of
+// extent 2 steps from the K cache to the V cache: one box is then a block's K tile
+// followed by its V tile.
+bool make_cache_map(CUtensorMap *map, const void *base, const void *vbase, pa_dtype dt,
+                    int num_blocks, int B, int Hkv, int D)
 {
     EncodeTiledFn enc = encode_fn();
     if (!enc)
         return false;
     const int es = elem_size(dt);
     const int ce = 128 / es;
-    const cuuint64_t dims[4] = {(cuuint64_t)ce, (cuuint64_t)(D / ce), (cuuint64_t)Hkv,
-                                (cuuint64_t)num_blocks * (cuuint64_t)B};
-    const cuuint64_t strides[3] = {128, (cuuint64_t)D * es, (cuuint64_t)Hkv * D * es};
-    const cuuint32_t box[4] = {(cuuint32_t)ce, 1, 1, (cuuint32_t)B};
-    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    const uintptr_t kv_gap = vbase ? (uintptr_t)vbase - (uintptr_t)base : 0;
+    const cuuint32_t rank = vbase ? 5 : 4;
+    const cuuint64_t dims[5] = {(cuuint64_t)ce, (cuuint64_t)num_blocks * (cuuint64_t)B,
+                                (cuuint64_t)(D / ce), (cuuint64_t)Hkv, 2};
+    const cuuint64_t strides[4] = {(cuuint64_t)Hkv * D * es, 128, (cuuint64_t)D * es,
+                                   (cuuint64_t)kv_gap};
+    const cuuint32_t box[5] = {(cuuint32_t)ce, (cuuint32_t)B, (cuuint32_t)(D / ce), 1, 2};
+    const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
     const CUtensorMapDataType tdt = dt == PA_F32   ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
                                     : dt == PA_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
                                                    : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-    const CUresult r = enc(map, tdt, 4, const_cast<void *>(base), dims, strides, box, estr,
+    const CUresult r = enc(map, tdt, rank, const_cast<void *>(base), dims, strides, box, estr,
                            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                            (CUtensorMapL2promotion)PA_L2_PROMOTION, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
+}
+
+// Whether one tensor map can step from the K cache to the V cache: V above K, a
+// multiple of 16 bytes away, within the 2^40-byte stride limit.  (Caches allocated
+// as one [2][num_blocks][B][Hkv][d] buffer always qualify.)
+bool kv_joint_ok(const void *k, const void *v)
+{
+    const uintptr_t a = (uintptr_t)k, b = (uintptr_t)v;
+    return b > a && (b - a) % 16 == 0 && (b - a) < (1ull << 40);
 }
 
 // ---- partition sizing ------------------------------------------------------------
@@ -387,8 +404,17 @@ pa_status decode_impl(void *out, const void *q, const void *k_cache, const void 
     L.block_size = block_size;
     L.sm_count = sms;
     L.grid = 0;  // the occupancy-sized persistent grid
-    if (!make_cache_map(&L.tmap_k, k_cache, dtype, num_blocks, block_size, num_kv_heads, head_dim) ||
-        !make_cache_map(&L.tmap_v, v_cache, dtype, num_blocks, block_size, num_kv_heads, head_dim))
+    // one copy per block for K and V where the caches' placement allows it (the
+    // joint map), else one per cache
+    p.kv_joint = kv_joint_ok(k_cache, v_cache) &&
+                         make_cache_map(&L.tmap_k, k_cache, v_cache, dtype, num_blocks, block_size,
+                                        num_kv_heads, head_dim)
+                     ? 1
+                     : 0;
+    if ((!p.kv_joint && !make_cache_map(&L.tmap_k, k_cache, nullptr, dtype, num_blocks, block_size,
+                                        num_kv_heads, head_dim)) ||
+        !make_cache_map(&L.tmap_v, v_cache, nullptr, dtype, num_blocks, block_size, num_kv_heads,
+                        head_dim))
         return cuda_fail(cudaErrorInvalidValue);
 
     cudaStream_t st = static_cast<cudaStream_t>(stream);

@@ -52,23 +52,47 @@ namespace pagedkv {
 #endif
 
 // A ring stage holds the K and V tiles of kBPS consecutive blocks of one item
-// (kStageTokens token rows of one kv head); the consumer treats it as one tile.
+// (kStageTokens token rows of one kv head): per block its K tile, then its V tile,
+// so that one copy can fetch both (tile_at).  A tile is d / (128 bytes) runs of
+// BS rows of 128 bytes (chunk-major), 128-byte swizzled.
 template <typename T, int D, int BS>
 struct Cfg {
     static constexpr int kElem = (int)sizeof(T);
     static constexpr int kChunkElems = 128 / kElem;  // elements in one 128-byte swizzle row
-    static constexpr int kChunks = D / kChunkElems;  // TMA boxes per block tile
+    static constexpr int kChunks = D / kChunkElems;  // 128-byte rows per token row
     static constexpr int kStageTokens =
         (sizeof(T) == 4 || PA_STAGE_TOKENS <= BS) ? BS : PA_STAGE_TOKENS;
     static constexpr int kBPS = kStageTokens / BS;   // blocks per stage
     static constexpr int kTileBytes = kStageTokens * D * kElem;  // K (or V) of one stage
     static constexpr int kStageBytes = 2 * kTileBytes;
+    static constexpr int kBlockTile = BS * D * kElem;    // K (or V) of one block
+    static constexpr int kBlockStride = 2 * kBlockTile;  // one block's K and V tiles
     static constexpr int kStagesRaw = (PA_RING_BYTES / kStageBytes) / kConsumerWarps * kConsumerWarps;
     static constexpr int kStages = kStagesRaw < kConsumerWarps ? kConsumerWarps : kStagesRaw;
     static_assert(kStages % kConsumerWarps == 0, "stages must split evenly over consumers");
     static_assert(D % kChunkElems == 0, "head_dim must be a whole number of 128-byte rows");
     static_assert(kStageTokens % BS == 0 && 32 % kBPS == 0, "a stage is a whole number of blocks");
 };
+
+// Addressing a ring stage: the 128-byte row holding chunk ch (bytes 128 ch ..
+// 128 ch + 127 of the head dim) of token t16 + r's K row, for t16 a multiple of 16
+// and r < 16, lies at
+//     tile_at(t16) + ch * BS * 128 + r * 128        (V: + kBlockTile)
+// and its 16-byte units are swizzled by r % 8.  tile_at folds to a constant in the
+// consumers' unrolled token loops; the r and ch terms are hoisted out of them.
+template <int BS, int kBlockStride>
+__device__ __forceinline__ constexpr uint32_t tile_at(int t16)
+{
+    return (uint32_t)((t16 / BS) * kBlockStride + (t16 % BS) * 128);
+}
+
+// How the producer copies a block's K and V tiles: one copy through the joint
+// tensor map, one copy per cache, or (fp32 kernels) whichever the launch's
+// kv_joint says.  The fp16/bf16 kernels are built for the first two, so their
+// producer loop carries no test of it.
+constexpr int kCopyRuntime = 0;
+constexpr int kCopyJoint = 1;
+constexpr int kCopySplit = 2;
 
 constexpr int kAccPad = 8;  // floats of padding per merge row (spreads banks)
 
@@ -448,7 +472,7 @@ __device__ __forceinline__ bool consumer_sync(const DecodeParams &p, const CtaSt
 // query rows (one bulk copy) to an item slot, then looks the item's blocks up in
 // the block table and issues their K/V TMA tile loads into the stage ring.
 // ---------------------------------------------------------------------------
-template <typename T, int D, int BS, int kBPS, int kChunks, int kTileBytes, int kStages>
+template <typename T, int D, int BS, int kBPS, int kChunks, int kTileBytes, int kStages, int kCopy>
 struct Producer {
     const DecodeParams &p;
     const CUtensorMap *tk;
@@ -555,7 +579,7 @@ struct Producer {
                 for (int b = 0; b < kBPS; ++b)
                     ph[b] = __shfl_sync(0xffffffffu, phys, (i + b) & 31);
                 if (lane == 0) {
-                    constexpr int kRowsPerStage = kTileBytes / (kChunks * 128);
+                    constexpr int kBlockTile = kTileBytes / kBPS;
                     const uint32_t fb = dev::smem_addr(&c.full[st]);
                     // fused append: does this stage hold the sequence's newest token?
                     const int newest = it.len - 1 - (jb + i) * BS;
@@ -567,7 +591,7 @@ struct Producer {
                         c.newinfo[2 * st + 1] = from_plan ? row[jb + i + newest / BS] : ph[newest / BS];
                     constexpr uint32_t kRowBytes = D * sizeof(T);
                     dev::mbar_arrive_expect_tx(
-                        fb, 2u * (uint32_t)nbs * (kTileBytes / kBPS) + (has_new ? 2u * kRowBytes : 0u));
+                        fb, 2u * (uint32_t)nbs * kBlockTile + (has_new ? 2u * kRowBytes : 0u));
                     if (has_new) {
                         const size_t src = ((size_t)it.seq * p.num_kv_heads + it.kvh) * D;
                         const uint32_t nr = dev::smem_addr(c.newrow + (size_t)st * 2 * kRowBytes);
@@ -576,21 +600,18 @@ struct Producer {
                                        kRowBytes, fb);
                     }
                     const uint32_t kd = dev::smem_addr(c.ring + (size_t)st * 2 * kTileBytes);
-                    const uint32_t vd = kd + kTileBytes;
 #pragma unroll
                     for (int b = 0; b < kBPS; ++b) {
                         if (b < nbs) {
                             // an entry outside the pool reads zeros (fully out-of-bounds box)
                             const int y = (ph[b] >= 0 && ph[b] < p.num_blocks) ? ph[b] * BS : -BS;
-                            const uint32_t off = (uint32_t)b * BS * 128;
-#pragma unroll
-                            for (int ch = 0; ch < kChunks; ++ch)
-                                dev::tma_load_4d(kd + ch * kRowsPerStage * 128 + off, tk, 0, ch,
-                                                 it.kvh, y, fb);
-#pragma unroll
-                            for (int ch = 0; ch < kChunks; ++ch)
-                                dev::tma_load_4d(vd + ch * kRowsPerStage * 128 + off, tv, 0, ch,
-                                                 it.kvh, y, fb);
+                            const uint32_t dst = kd + (uint32_t)b * 2 * kBlockTile;
+                            if (kCopy == kCopyJoint || (kCopy == kCopyRuntime && p.kv_joint)) {
+                                dev::tma_load_5d(dst, tk, 0, y, 0, it.kvh, 0, fb);  // K and V
+                            } else {
+                                dev::tma_load_4d(dst, tk, 0, y, 0, it.kvh, fb);
+                                dev::tma_load_4d(dst + kBlockTile, tv, 0, y, 0, it.kvh, fb);
+                            }
                         }
                     }
 #ifdef PA_TRACE
@@ -1077,11 +1098,11 @@ __device__ __forceinline__ void walk_fixed(const DecodeParams &p, int bs, Prod &
 }
 
 template <typename T, int D, int BS, int kBPS, int kChunks, int kTileBytes, int kStages,
-          int kMode>
+          int kMode, int kCopy>
 __device__ __forceinline__ void producer_loop(const DecodeParams &p, const CUtensorMap *tk,
                                               const CUtensorMap *tv, const CtaState &c, int lane)
 {
-    Producer<T, D, BS, kBPS, kChunks, kTileBytes, kStages> pr(p, tk, tv, c, lane);
+    Producer<T, D, BS, kBPS, kChunks, kTileBytes, kStages, kCopy> pr(p, tk, tv, c, lane);
     if constexpr (kMode == kModePlan)
         walk_planned(p, BS, kBPS, pr, lane);
     else if (p.balanced)
@@ -1432,11 +1453,12 @@ __device__ __forceinline__ bool finish_item(const DecodeParams &p, const Item &i
 // item whose context length is not the one the launch reads): the tile is patched
 // but nothing is stored to the cache, and PA_DEVERR_PLAN is raised.
 // ---------------------------------------------------------------------------
-template <typename T, int D, int TS, int BS>
+template <typename T, int D, int BS>
 __device__ __forceinline__ void patch_newest_row(const DecodeParams &p, const Item &it,
-                                              const CtaState &c, uint32_t st, uint8_t *ktile,
-                                              uint8_t *vtile, int lane, bool append_ok)
+                                              const CtaState &c, uint32_t st, uint8_t *stage,
+                                              int lane, bool append_ok)
 {
+    using C = Cfg<T, D, BS>;
     constexpr int kUnits = D * (int)sizeof(T) / 16;  // 16-byte units per row
     constexpr int kUnitElems = 16 / (int)sizeof(T);
     constexpr int kCE = 128 / (int)sizeof(T);
@@ -1454,8 +1476,8 @@ __device__ __forceinline__ void patch_newest_row(const DecodeParams &p, const It
         const int d0 = u * kUnitElems;
         const int ch = d0 / kCE;
         const int uc = (d0 % kCE) / kUnitElems;
-        *reinterpret_cast<uint4 *>((isv ? vtile : ktile) + ch * (TS * 128) + r * 128 +
-                                   ((uc ^ (r & 7)) << 4)) = val;
+        *reinterpret_cast<uint4 *>(stage + (r / BS) * C::kBlockStride + (isv ? C::kBlockTile : 0) +
+                                   ch * (BS * 128) + (r % BS) * 128 + ((uc ^ (r & 7)) << 4)) = val;
         if (store)
             *reinterpret_cast<uint4 *>(reinterpret_cast<T *>(isv ? p.v_cache : p.k_cache) + dst + d0) =
                 val;
@@ -1550,14 +1572,14 @@ __device__ __forceinline__ bool consume_item_n8(const DecodeParams &p, const Cta
 #endif
         const int valid = min(min(C::kBPS, it.j1 - j) * BS, it.len - j * BS);
         const uint32_t kb = dev::smem_addr(c.ring + (size_t)st * C::kStageBytes);
-        const uint32_t vb = kb + C::kTileBytes;
+        const uint32_t vb = kb + C::kBlockTile;
         if (c.newinfo[2 * st] >= 0)
-            patch_newest_row<T, D, TS, BS>(p, it, c, st, c.ring + (size_t)st * C::kStageBytes,
-                                           c.ring + (size_t)st * C::kStageBytes + C::kTileBytes,
-                                           lane, append_ok);
+            patch_newest_row<T, D, BS>(p, it, c, st, c.ring + (size_t)st * C::kStageBytes, lane,
+                                       append_ok);
 
         // S^T = K Q^T: the K tile (rows = tokens) is the row-major A operand.
         // Two accumulators per token tile (even / odd k-steps) shorten the chains.
+        const uint32_t krow = kb + (uint32_t)(((mi & 1) * 8 + (lane & 7)) * 128);
         float s[MT][2][4];
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt)
@@ -1567,13 +1589,13 @@ __device__ __forceinline__ bool consume_item_n8(const DecodeParams &p, const Cta
 #pragma unroll
         for (int ks = 0; ks < KS; ++ks) {
             const int d = ks * 16 + (mi >> 1) * 8;
-            const uint32_t colpart = (uint32_t)(d / kCE) * (TS * 128) +
+            const uint32_t colpart = (uint32_t)(d / kCE) * (BS * 128) +
                                      (uint32_t)((((d % kCE) >> 3) ^ swz) << 4);
 #pragma unroll
             for (int mt = 0; mt < MT; ++mt) {
-                const int tok = mt * 16 + (mi & 1) * 8 + (lane & 7);
                 uint32_t a[4];
-                dev::ldsm_x4(kb + colpart + tok * 128, a[0], a[1], a[2], a[3]);
+                dev::ldsm_x4(krow + colpart + tile_at<BS, C::kBlockStride>(mt * 16), a[0], a[1],
+                             a[2], a[3]);
                 dev::Mma<T>::run(s[mt][ks & 1], a, qb[ks][0], qb[ks][1]);
             }
         }
@@ -1630,6 +1652,7 @@ __device__ __forceinline__ bool consume_item_n8(const DecodeParams &p, const Cta
         // O^T += V^T P^T: ldmatrix.trans of the V tile (rows = tokens) gives the
         // row-major A operand (m = head dim, k = token); P^T is the B operand.
         const bool partial = valid < TS;
+        const uint32_t vrow = vb + (uint32_t)(((mi >> 1) * 8 + (lane & 7)) * 128);
 #pragma unroll
         for (int kt = 0; kt < MT; ++kt) {
             const uint32_t pb0 = dev::movmatrix_trans(dev::Mma<T>::pack(sc[kt][0], sc[kt][1]));
@@ -1641,11 +1664,11 @@ __device__ __forceinline__ bool consume_item_n8(const DecodeParams &p, const Cta
                 mk0 = (t0 < valid ? 0x0000ffffu : 0u) | (t0 + 1 < valid ? 0xffff0000u : 0u);
                 mk1 = (t0 + 8 < valid ? 0x0000ffffu : 0u) | (t0 + 9 < valid ? 0xffff0000u : 0u);
             }
-            const int tok = kt * 16 + (mi >> 1) * 8 + (lane & 7);
 #pragma unroll
             for (int dm = 0; dm < DM; ++dm) {
                 const int d = dm * 16 + (mi & 1) * 8;
-                const uint32_t addr = vb + (uint32_t)(d / kCE) * (TS * 128) + tok * 128 +
+                const uint32_t addr = vrow + tile_at<BS, C::kBlockStride>(kt * 16) +
+                                      (uint32_t)(d / kCE) * (BS * 128) +
                                       (uint32_t)((((d % kCE) >> 3) ^ swz) << 4);
                 uint32_t a[4];
                 dev::ldsm_x4_trans(addr, a[0], a[1], a[2], a[3]);
@@ -1694,9 +1717,10 @@ __device__ __forceinline__ bool consume_item_n8(const DecodeParams &p, const Cta
 
 // ---------------------------------------------------------------------------
 // fp16 / bf16 partition kernel: tensor-core consumers.  kMode: the launch it is
-// built for (kModePlain, kModePrefix, kModeOwn).
+// built for (kModePlain, kModePlan, kModePrefix, kModeOwn); kCopy: kCopyJoint or
+// kCopySplit, by the caches' placement.
 // ---------------------------------------------------------------------------
-template <typename T, int D, int BS, bool N8, int kMode>
+template <typename T, int D, int BS, bool N8, int kMode, int kCopy>
 __global__ void __launch_bounds__(kThreads, 2)
     pa_decode_mma_kernel(const __grid_constant__ DecodeParams p,
                          const __grid_constant__ CUtensorMap tmap_k,
@@ -1725,7 +1749,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     if (warp == kConsumerWarps) {
-        producer_loop<T, D, BS, C::kBPS, C::kChunks, C::kTileBytes, C::kStages, kMode>(
+        producer_loop<T, D, BS, C::kBPS, C::kChunks, C::kTileBytes, C::kStages, kMode, kCopy>(
             p, &tmap_k, &tmap_v, c, lane);
         return;
     }
@@ -1841,14 +1865,14 @@ __global__ void __launch_bounds__(kThreads, 2)
             // tokens of this stage that count: the loaded blocks, up to the context
             const int valid = min(min(C::kBPS, it.j1 - j) * BS, it.len - j * BS);
             const uint32_t kb = dev::smem_addr(c.ring + (size_t)st * C::kStageBytes);
-            const uint32_t vb = kb + C::kTileBytes;
+            const uint32_t vb = kb + C::kBlockTile;
             if (c.newinfo[2 * st] >= 0)
-                patch_newest_row<T, D, TS, BS>(p, it, c, st, c.ring + (size_t)st * C::kStageBytes,
-                                               c.ring + (size_t)st * C::kStageBytes + C::kTileBytes,
-                                               lane, append_ok);
+                patch_newest_row<T, D, BS>(p, it, c, st, c.ring + (size_t)st * C::kStageBytes, lane,
+                                           append_ok);
 
             // S = Q K^T: K tile rows are tokens, so plain ldmatrix yields the
             // "col" B fragment (k = head dim, n = token).
+            const uint32_t krow = kb + (uint32_t)(((mi >> 1) * 8 + (lane & 7)) * 128);
             float sc[NT][4];
 #pragma unroll
             for (int i = 0; i < NT; ++i)
@@ -1856,13 +1880,13 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
             for (int ks = 0; ks < KS; ++ks) {
                 const int d = ks * 16 + (mi & 1) * 8;
-                const uint32_t colpart = (uint32_t)(d / kCE) * (TS * 128) +
+                const uint32_t colpart = (uint32_t)(d / kCE) * (BS * 128) +
                                          (uint32_t)((((d % kCE) >> 3) ^ swz) << 4);
 #pragma unroll
                 for (int np = 0; np < NT / 2; ++np) {
-                    const int tok = (2 * np + (mi >> 1)) * 8 + (lane & 7);
                     uint32_t b0, b1, b2, b3;
-                    dev::ldsm_x4(kb + colpart + tok * 128, b0, b1, b2, b3);
+                    dev::ldsm_x4(krow + colpart + tile_at<BS, C::kBlockStride>(np * 16), b0, b1,
+                                 b2, b3);
                     dev::Mma<T>::run(sc[2 * np], qa[ks], b0, b1);
                     dev::Mma<T>::run(sc[2 * np + 1], qa[ks], b2, b3);
                 }
@@ -1917,6 +1941,7 @@ __global__ void __launch_bounds__(kThreads, 2)
             // O += P V: V tile rows are tokens, so ldmatrix.trans yields the
             // "col" B fragment (k = token, n = head dim).
             const bool partial = valid < TS;
+            const uint32_t vrow = vb + (uint32_t)(((mi & 1) * 8 + (lane & 7)) * 128);
 #pragma unroll
             for (int kt = 0; kt < TS / 16; ++kt) {
                 uint32_t pa[4];
@@ -1931,11 +1956,11 @@ __global__ void __launch_bounds__(kThreads, 2)
                     mk0 = (t0 < valid ? 0x0000ffffu : 0u) | (t0 + 1 < valid ? 0xffff0000u : 0u);
                     mk1 = (t0 + 8 < valid ? 0x0000ffffu : 0u) | (t0 + 9 < valid ? 0xffff0000u : 0u);
                 }
-                const int tok = kt * 16 + (mi & 1) * 8 + (lane & 7);
 #pragma unroll
                 for (int dp = 0; dp < D / 16; ++dp) {
                     const int d = dp * 16 + (mi >> 1) * 8;
-                    const uint32_t addr = vb + (uint32_t)(d / kCE) * (TS * 128) + tok * 128 +
+                    const uint32_t addr = vrow + tile_at<BS, C::kBlockStride>(kt * 16) +
+                                          (uint32_t)(d / kCE) * (BS * 128) +
                                           (uint32_t)((((d % kCE) >> 3) ^ swz) << 4);
                     uint32_t v0, v1, v2, v3;
                     dev::ldsm_x4_trans(addr, v0, v1, v2, v3);
@@ -2049,8 +2074,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     if (warp == kConsumerWarps) {
-        producer_loop<float, D, BS, C::kBPS, C::kChunks, C::kTileBytes, C::kStages, kMode>(
-            p, &tmap_k, &tmap_v, c, lane);
+        producer_loop<float, D, BS, C::kBPS, C::kChunks, C::kTileBytes, C::kStages, kMode,
+                      kCopyRuntime>(p, &tmap_k, &tmap_v, c, lane);
         return;
     }
 
@@ -2118,13 +2143,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
 #endif
             const int valid = min(BS, it.len - j * BS);
+            static_assert(C::kBPS == 1, "fp32 stages hold one block");
             const uint8_t *kt = c.ring + (size_t)st * C::kStageBytes;
-            const uint8_t *vt = kt + C::kTileBytes;
+            const uint8_t *vt = kt + C::kBlockTile;
             if (c.newinfo[2 * st] >= 0)
-                patch_newest_row<float, D, BS, BS>(p, it, c, st, c.ring + (size_t)st * C::kStageBytes,
-                                                   c.ring + (size_t)st * C::kStageBytes +
-                                                       C::kTileBytes,
-                                                   lane, append_ok);
+                patch_newest_row<float, D, BS>(p, it, c, st, c.ring + (size_t)st * C::kStageBytes,
+                                               lane, append_ok);
 
             float sc[H];
 #pragma unroll
@@ -2356,15 +2380,21 @@ inline int launch_mode(const DecodeParams &p)
 }
 
 // Items of at most 8 query rows (group <= 8) take the transposed-product
-// consumers; wider items the 16-row form.
+// consumers; wider items the 16-row form.  Caches placed for the joint tensor map
+// take the instance that copies K and V together.
 template <typename T, int D, int BS>
 struct KernelOf {
+    template <int kMode, int kCopy>
+    static void *pick_copy(const DecodeParams &p)
+    {
+        return p.group <= kNarrowRows
+                   ? reinterpret_cast<void *>(&pa_decode_mma_kernel<T, D, BS, true, kMode, kCopy>)
+                   : reinterpret_cast<void *>(&pa_decode_mma_kernel<T, D, BS, false, kMode, kCopy>);
+    }
     template <int kMode>
     static void *pick(const DecodeParams &p)
     {
-        return p.group <= kNarrowRows
-                   ? reinterpret_cast<void *>(&pa_decode_mma_kernel<T, D, BS, true, kMode>)
-                   : reinterpret_cast<void *>(&pa_decode_mma_kernel<T, D, BS, false, kMode>);
+        return p.kv_joint ? pick_copy<kMode, kCopyJoint>(p) : pick_copy<kMode, kCopySplit>(p);
     }
     static void *get(const DecodeParams &p)
     {

@@ -65,6 +65,9 @@ struct DecodeParams {
     // Plain balanced-split decode: kPlanInts per CTA of the host-computed start
     // (pa_decode_plan), or null to walk the stream on the device.
     const int32_t *plan;
+    // 1: the K tensor map spans both caches (a fifth dimension of extent 2 steps from
+    // K to V), so one copy fetches a block's K and V tiles; 0: one copy per cache.
+    int kv_joint;
 };
 
 // The wait limit decode launches take (pa_set_wait_limit_ns).
@@ -129,7 +132,7 @@ constexpr int kPlanWindow = kPlanInts - kPlanBlocks;
 
 struct DecodeLaunch {
     DecodeParams p;
-    CUtensorMap tmap_k;
+    CUtensorMap tmap_k;  // K, or K and V together when p.kv_joint
     CUtensorMap tmap_v;
     int head_dim;
     int block_size;

@@ -332,9 +332,17 @@ def cache_shape(w: Workload):
 
 
 def pool_tensors(w: Workload, device="cpu"):
-    """Initial K and V pools: every block holds N(0,1) data (prefilled or stale)."""
-    return (randn(cache_shape(w), w.dtype, w.data_seed * 10 + 1, device),
-            randn(cache_shape(w), w.dtype, w.data_seed * 10 + 2, device))
+    """Initial K and V pools: every block holds N(0,1) data (prefilled or stale).
+
+    Both are views of one [2, num_blocks, block_size, num_kv_heads, head_dim] buffer,
+    V after K, the placement under which the decode fetches a block's K and V tiles
+    with one copy.  The values are those of two separate seeded draws."""
+    import torch
+    shape = cache_shape(w)
+    kv = torch.empty((2,) + shape, dtype=torch_dtype(w.dtype), device=device)
+    kv[0].copy_(randn(shape, w.dtype, w.data_seed * 10 + 1, device))
+    kv[1].copy_(randn(shape, w.dtype, w.data_seed * 10 + 2, device))
+    return kv[0], kv[1]
 
 
 def step_tensors(w: Workload, step: Step, device="cpu"):

@@ -79,7 +79,10 @@ struct Cfg {
 // and r < 16, lies at
 //     tile_at(t16) + ch * BS * 128 + r * 128        (V: + kBlockTile)
 // and its 16-byte units are swizzled by r % 8.  tile_at folds to a constant in the
-// consumers' unrolled token loops; the r and ch terms are hoisted out of them.
+// consumers' unrolled token loops.  With one block per stage (tile_at(t16) =
+// t16 * 128) the narrow consumers address a row as base + chunk term + token * 128,
+// the form the stage layout had before it held two blocks: code generated from the
+// two-block form measured 0.4% slower on the long-context decode there.
 template <int BS, int kBlockStride>
 __device__ __forceinline__ constexpr uint32_t tile_at(int t16)
 {
@@ -1594,8 +1597,12 @@ __device__ __forceinline__ bool consume_item_n8(const DecodeParams &p, const Cta
 #pragma unroll
             for (int mt = 0; mt < MT; ++mt) {
                 uint32_t a[4];
-                dev::ldsm_x4(krow + colpart + tile_at<BS, C::kBlockStride>(mt * 16), a[0], a[1],
-                             a[2], a[3]);
+                const int tok = mt * 16 + (mi & 1) * 8 + (lane & 7);
+                if constexpr (C::kBPS == 1)
+                    dev::ldsm_x4(kb + colpart + tok * 128, a[0], a[1], a[2], a[3]);
+                else
+                    dev::ldsm_x4(krow + colpart + tile_at<BS, C::kBlockStride>(mt * 16), a[0],
+                                 a[1], a[2], a[3]);
                 dev::Mma<T>::run(s[mt][ks & 1], a, qb[ks][0], qb[ks][1]);
             }
         }
@@ -1667,9 +1674,13 @@ __device__ __forceinline__ bool consume_item_n8(const DecodeParams &p, const Cta
 #pragma unroll
             for (int dm = 0; dm < DM; ++dm) {
                 const int d = dm * 16 + (mi & 1) * 8;
-                const uint32_t addr = vrow + tile_at<BS, C::kBlockStride>(kt * 16) +
-                                      (uint32_t)(d / kCE) * (BS * 128) +
-                                      (uint32_t)((((d % kCE) >> 3) ^ swz) << 4);
+                const int tok = kt * 16 + (mi >> 1) * 8 + (lane & 7);
+                const uint32_t addr =
+                    C::kBPS == 1 ? vb + (uint32_t)(d / kCE) * (TS * 128) + tok * 128 +
+                                       (uint32_t)((((d % kCE) >> 3) ^ swz) << 4)
+                                 : vrow + tile_at<BS, C::kBlockStride>(kt * 16) +
+                                       (uint32_t)(d / kCE) * (BS * 128) +
+                                       (uint32_t)((((d % kCE) >> 3) ^ swz) << 4);
                 uint32_t a[4];
                 dev::ldsm_x4_trans(addr, a[0], a[1], a[2], a[3]);
                 a[0] &= mk0;

@@ -155,7 +155,7 @@ __device__ __forceinline__ bool trace_first_tile(int pass)
 #endif
 
 struct SmemLayout {
-    uint32_t acc, ml, pfx, items, q, newrow, newinfo, bars, flag, total;
+    uint32_t acc, ml, pfx, items, q, newrow, newinfo, bars, flag, blk, total;
 };
 
 // Shared-prefix buffer rows: o (head_dim floats), then the log2-sum-exp, padded to
@@ -192,7 +192,8 @@ __host__ __device__ inline int members_per_item(int group)
 
 // Shared memory: stage ring | merge accumulators | merge (max, sum) | shared-prefix
 // rows (two item buffers; pass 0 of the shared-prefix decode only) | item
-// descriptors | query rows per item slot | mbarriers | abort flag.
+// descriptors | query rows per item slot | mbarriers | flags | the producer's block
+// ids.
 __host__ __device__ inline SmemLayout make_layout(int stages, int stage_bytes, int rows, int D,
                                                   int elem_bytes, int pfx_rows = 0)
 {
@@ -218,6 +219,9 @@ __host__ __device__ inline SmemLayout make_layout(int stages, int stage_bytes, i
     o += (2u * (uint32_t)stages + 2u * kItemSlots + 1u) * 8u;
     L.flag = o;  // abort flag, merge flag, counter seen, then a scratch word per consumer warp
     o += 16u + 4u * kConsumerWarps;
+    o = (o + 15u) & ~15u;
+    L.blk = o;  // the producer's current window of 32 block ids
+    o += 32u * 4u;
     L.total = o + 1024u;  // slack to align the base to 1024 bytes (128-byte swizzle)
     return L;
 }
@@ -356,6 +360,7 @@ struct CtaState {
     volatile int *merge;               // this CTA completes the current split unit
     unsigned long long *ctr_seen;      // the split unit's counter as the probe read it
     volatile uint32_t *sink;           // per consumer warp: see dev::settle_loads
+    int *blk;                          // the producer's window of 32 block ids
 };
 
 __device__ __forceinline__ CtaState cta_state(uint8_t *smem, const SmemLayout &lay, int stages)
@@ -378,6 +383,7 @@ __device__ __forceinline__ CtaState cta_state(uint8_t *smem, const SmemLayout &l
     c.merge = reinterpret_cast<volatile int *>(smem + lay.flag + 4);
     c.ctr_seen = reinterpret_cast<unsigned long long *>(smem + lay.flag + 8);
     c.sink = reinterpret_cast<volatile uint32_t *>(smem + lay.flag + 16);
+    c.blk = reinterpret_cast<int *>(smem + lay.blk);
     return c;
 }
 
@@ -543,7 +549,9 @@ struct Producer {
         }
         const int32_t *row = p.block_tables + (size_t)it.tseq * p.max_blocks;
         // a planned first item takes its first kPlanWindow block ids from the plan
-        // (no block-table round trip before its first copies), then 32 at a time
+        // (no block-table round trip before its first copies), then 32 at a time.
+        // The warp loads a window of ids into shared memory; lane 0 alone then
+        // waits for and fills the window's stages, with no warp-wide step per stage.
         const bool planned = plan_seq == it.tseq && plan_j0 == it.j0;
         plan_seq = -1;
         for (int jb = it.j0, wnd = 32; jb < it.j1; jb += wnd) {
@@ -556,77 +564,81 @@ struct Producer {
             else
                 phys = (j < it.j1) ? row[j] : 0;  // one coalesced read per 32 blocks
             const int cnt = min(wnd, it.j1 - jb);
-            for (int i = 0; i < cnt; i += kBPS, ++g) {
-                const int nbs = min(kBPS, cnt - i);  // blocks in this stage
-                const uint32_t st = g % kStages;
-                int ok = 1;
-#ifdef PA_TRACE
-                const unsigned long long t_w0 = dev::global_timer_ns();
-#endif
-                if (lane == 0)
-                    ok = wait_slot(&c.empty[st], ((g / kStages) & 1u) ^ 1u);
-#ifdef PA_TRACE
-                if (lane == 0) {
-                    const unsigned long long t_w1 = dev::global_timer_ns();
-                    PA_TRACE_ADD(6, t_w1 - t_w0);
-                    if (i == 0 && jb == it.j0 && t_last_issue)
-                        PA_TRACE_ADD(5, t_w0 - t_last_issue);
-                }
-#endif
-                if (!__shfl_sync(0xffffffffu, ok, 0)) {
-                    failed = true;
-                    return false;
-                }
-                int ph[kBPS];
-#pragma unroll
-                for (int b = 0; b < kBPS; ++b)
-                    ph[b] = __shfl_sync(0xffffffffu, phys, (i + b) & 31);
-                if (lane == 0) {
-                    constexpr int kBlockTile = kTileBytes / kBPS;
-                    const uint32_t fb = dev::smem_addr(&c.full[st]);
-                    // fused append: does this stage hold the sequence's newest token?
-                    const int newest = it.len - 1 - (jb + i) * BS;
-                    const bool has_new = p.k_new != nullptr && newest >= 0 && newest < nbs * BS;
-                    c.newinfo[2 * st] = has_new ? newest : -1;
-                    // the block the newest token is written to always comes from the
-                    // table, so a stale plan cannot direct the append elsewhere
-                    if (has_new)
-                        c.newinfo[2 * st + 1] = from_plan ? row[jb + i + newest / BS] : ph[newest / BS];
-                    constexpr uint32_t kRowBytes = D * sizeof(T);
-                    dev::mbar_arrive_expect_tx(
-                        fb, 2u * (uint32_t)nbs * kBlockTile + (has_new ? 2u * kRowBytes : 0u));
-                    if (has_new) {
-                        const size_t src = ((size_t)it.seq * p.num_kv_heads + it.kvh) * D;
-                        const uint32_t nr = dev::smem_addr(c.newrow + (size_t)st * 2 * kRowBytes);
-                        dev::bulk_load(nr, reinterpret_cast<const T *>(p.k_new) + src, kRowBytes, fb);
-                        dev::bulk_load(nr + kRowBytes, reinterpret_cast<const T *>(p.v_new) + src,
-                                       kRowBytes, fb);
-                    }
-                    const uint32_t kd = dev::smem_addr(c.ring + (size_t)st * 2 * kTileBytes);
-#pragma unroll
-                    for (int b = 0; b < kBPS; ++b) {
-                        if (b < nbs) {
-                            // an entry outside the pool reads zeros (fully out-of-bounds box)
-                            const int y = (ph[b] >= 0 && ph[b] < p.num_blocks) ? ph[b] * BS : -BS;
-                            const uint32_t dst = kd + (uint32_t)b * 2 * kBlockTile;
-                            if (kCopy == kCopyJoint || (kCopy == kCopyRuntime && p.kv_joint)) {
-                                dev::tma_load_5d(dst, tk, 0, y, 0, it.kvh, 0, fb);  // K and V
-                            } else {
-                                dev::tma_load_4d(dst, tk, 0, y, 0, it.kvh, fb);
-                                dev::tma_load_4d(dst + kBlockTile, tv, 0, y, 0, it.kvh, fb);
-                            }
-                        }
-                    }
-#ifdef PA_TRACE
-                    if (!t_last_issue)
-                        PA_TRACE_SET(14, dev::global_timer_ns());  // first tile issued
-                    t_last_issue = dev::global_timer_ns();
-                    PA_TRACE_ADD(7, 1);
-#endif
-                }
+            c.blk[lane] = phys;
+            __syncwarp();
+            uint32_t issued = 0;
+            int ok = 1;
+            if (lane == 0)
+                ok = fill_window(it, row, jb, cnt, from_plan, issued);
+            // lane 0 has read the window's ids once the warp passes these
+            g += __shfl_sync(0xffffffffu, issued, 0);
+            if (!__shfl_sync(0xffffffffu, ok, 0)) {
+                failed = true;
+                return false;
             }
         }
         return true;
+    }
+
+    // Lane 0: the stages of one window of cnt blocks (ids in c.blk) starting at block
+    // jb of the item.  Returns false once a wait gave up; *issued: stages issued.
+    __device__ int fill_window(const Item &it, const int32_t *row, int jb, int cnt,
+                               bool from_plan, uint32_t &issued)
+    {
+        constexpr int kBlockTile = kTileBytes / kBPS;
+        constexpr uint32_t kRowBytes = D * sizeof(T);
+        uint32_t gg = g;
+        for (int i = 0; i < cnt; i += kBPS, ++gg) {
+            const int nbs = min(kBPS, cnt - i);  // blocks in this stage
+            const uint32_t st = gg % kStages;
+            if (!wait_slot(&c.empty[st], ((gg / kStages) & 1u) ^ 1u)) {
+                issued = gg - g;
+                return 0;
+            }
+            const uint32_t fb = dev::smem_addr(&c.full[st]);
+            // fused append: does this stage hold the sequence's newest token?
+            const int newest = it.len - 1 - (jb + i) * BS;
+            const bool has_new = p.k_new != nullptr && newest >= 0 && newest < nbs * BS;
+            c.newinfo[2 * st] = has_new ? newest : -1;
+            // the block the newest token is written to always comes from the
+            // table, so a stale plan cannot direct the append elsewhere
+            if (has_new)
+                c.newinfo[2 * st + 1] =
+                    from_plan ? row[jb + i + newest / BS] : c.blk[(i + newest / BS) & 31];
+            dev::mbar_arrive_expect_tx(
+                fb, 2u * (uint32_t)nbs * kBlockTile + (has_new ? 2u * kRowBytes : 0u));
+            if (has_new) {
+                const size_t src = ((size_t)it.seq * p.num_kv_heads + it.kvh) * D;
+                const uint32_t nr = dev::smem_addr(c.newrow + (size_t)st * 2 * kRowBytes);
+                dev::bulk_load(nr, reinterpret_cast<const T *>(p.k_new) + src, kRowBytes, fb);
+                dev::bulk_load(nr + kRowBytes, reinterpret_cast<const T *>(p.v_new) + src, kRowBytes,
+                               fb);
+            }
+            const uint32_t kd = dev::smem_addr(c.ring + (size_t)st * 2 * kTileBytes);
+#pragma unroll
+            for (int b = 0; b < kBPS; ++b) {
+                if (b < nbs) {
+                    const int id = c.blk[(i + b) & 31];
+                    // an entry outside the pool reads zeros (fully out-of-bounds box)
+                    const int y = (id >= 0 && id < p.num_blocks) ? id * BS : -BS;
+                    const uint32_t dst = kd + (uint32_t)b * 2 * kBlockTile;
+                    if (kCopy == kCopyJoint || (kCopy == kCopyRuntime && p.kv_joint)) {
+                        dev::tma_load_5d(dst, tk, 0, y, 0, it.kvh, 0, fb);  // K and V
+                    } else {
+                        dev::tma_load_4d(dst, tk, 0, y, 0, it.kvh, fb);
+                        dev::tma_load_4d(dst + kBlockTile, tv, 0, y, 0, it.kvh, fb);
+                    }
+                }
+            }
+#ifdef PA_TRACE
+            if (!t_last_issue)
+                PA_TRACE_SET(14, dev::global_timer_ns());  // first tile issued
+            t_last_issue = dev::global_timer_ns();
+            PA_TRACE_ADD(7, 1);
+#endif
+        }
+        issued = gg - g;
+        return 1;
     }
 
     // Lane 0: wait for the consumers to free a ring stage or item slot (the phase

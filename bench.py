@@ -397,12 +397,15 @@ def run_ours(args):
     # the plain balanced split starts each CTA from the host plan (pa_decode_plan)
     planned = (not shared and parts == 0 and ds.plan is not None and
                getattr(args, "plan", "auto") != "never")
+    # ... and the shared-prefix decode's two launches from theirs (pa_decode_shared_plan)
+    shared_planned = shared and ds.shared_plan is not None and getattr(args, "plan", "auto") != "never"
+
     launches_per_step = ((1 if n_pairs else 0) + (0 if fused or not n_tok else 1) +
                          (2 if shared else 1) + (1 if merge else 0))
 
     with torch.cuda.stream(stream):
-        step = (ds.run_shared if shared else ds.run_planned if planned else
-                ds.run_fused if fused else ds.run)
+        step = ((lambda st: ds.run_shared(st, planned=shared_planned)) if shared else
+                ds.run_planned if planned else ds.run_fused if fused else ds.run)
         ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
                torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
         # the sampler starts first: warm-up runs right before the timed steps, so the
@@ -428,7 +431,7 @@ def run_ours(args):
                 P.pa_reshape_and_cache(ds.step_k, ds.step_v, ds.k_cache, ds.v_cache, ds.slots, stream)
             e1.record(stream)
             if shared:
-                ds.decode_shared(stream, append=fused)
+                ds.decode_shared(stream, append=fused, planned=shared_planned)
             elif planned:
                 P.pa_decode_planned(ds.out, ds.q, ds.k_cache, ds.v_cache, ds.block_tables,
                                     ds.context_lens, ds.plan, ds.scale, ds.num_q_heads,
@@ -476,7 +479,7 @@ def run_ours(args):
         [t_step, t_step_mean, t_dec, t_dec_med, t_warm], device)
 
     # end to end through the public API with host buffers
-    e2e = run_e2e(ds, stream, device, args, by, shared, world, planned)
+    e2e = run_e2e(ds, stream, device, args, by, shared, world, planned, shared_planned)
 
     if rank != 0:
         return None
@@ -506,7 +509,10 @@ def run_ours(args):
                                     if ds.share is not None and share_mode == "auto" else
                                     "not used (--share never)" if ds.share is not None else "none"),
                  "cta_starts": ("planned on the host (pa_decode_plan, uploaded with the tables)"
-                                if planned else "walked on the device"),
+                                if planned else
+                                "planned on the host for both launches (pa_decode_shared_plan, "
+                                "uploaded with the tables)" if shared_planned else
+                                "walked on the device"),
                  "appended_tokens": n_tok,
                  "cow_pairs": n_pairs},
         "ms_per_step_mean": round(t_step_mean, 5),
@@ -518,7 +524,8 @@ def run_ours(args):
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_kind": f"{peak_kind} copy bandwidth",
                      "traffic": profiled_traffic(w.name, 2 if shared else 1),
-                     "kernel": ("pa_decode_shared (partition kernel twice: shared prefixes, then own "
+                     "kernel": (("pa_decode_shared_planned" if shared_planned else "pa_decode_shared") +
+                                " (partition kernel twice: shared prefixes, then own "
                                 "blocks" + (" + append" if fused else "") + ", merges inside)" if shared
                                 else "pa_decode_planned (append + decode partition kernel from the host "
                                 "plan, merge inside)" if planned and fused
@@ -546,7 +553,7 @@ def run_ours(args):
     return line
 
 
-def run_e2e(ds, stream, device, args, by, shared=False, world=1, planned=False):
+def run_e2e(ds, stream, device, args, by, shared=False, world=1, planned=False, shared_planned=False):
     """Same step through the public API with inputs in pinned host memory: H2D of
     the step's inputs (packed into one buffer, one copy), the step, D2H of the
     output -- all inside the timed region."""
@@ -558,6 +565,8 @@ def run_e2e(ds, stream, device, args, by, shared=False, world=1, planned=False):
         names.append("share")
     if planned:
         names.append("plan")
+    if shared_planned:
+        names.append("shared_plan")
     packed = runner.PackedInputs({n: getattr(ds, n) for n in names}, device)
     dsv = dataclasses.replace(ds, **packed.views)
     out_h = torch.empty(ds.out.shape, dtype=ds.out.dtype).pin_memory()
@@ -573,7 +582,7 @@ def run_e2e(ds, stream, device, args, by, shared=False, world=1, planned=False):
             a.record(stream)
             packed.upload(stream)
             if shared:
-                dsv.run_shared(stream)
+                dsv.run_shared(stream, planned=shared_planned)
             elif planned:
                 dsv.run_planned(stream)
             else:

@@ -246,6 +246,56 @@ size_t pa_decode_shared_workspace_size(int num_seqs, int num_q_heads, int num_kv
                                        int head_dim, int block_size, int max_blocks_per_seq);
 
 /*
+ * pa_decode_shared_plan / pa_decode_shared_planned -- pa_decode_shared with each
+ * CTA's start in both launches computed on the host.
+ *
+ * The pages have no counterpart (see pa_decode_plan).  Unplanned, every CTA of
+ * each launch first reads all context lengths and group entries (and, for the
+ * shared blocks' launch, the member entries after each group's first member),
+ * sums the launch's stream, finds its range and reads its first block-table row:
+ * several dependent memory round trips before its first copy, in each launch.
+ * pa_decode_shared_plan replays both walks on the host and writes one 128-byte
+ * entry per CTA per launch: the shared blocks' launch's entries, then the own
+ * blocks' launch's.  An entry holds what pa_decode_plan's does, with the first
+ * sequence's units as that launch counts them (the group's member count and
+ * shared block count; the first own block, and whether the (kv head, sequence)
+ * order applies).  Output, caches and workspace use are bit-identical to the
+ * unplanned pa_decode_shared's.
+ *
+ * pa_decode_shared_plan_bytes: size of the plan on the current device: 2 x 128
+ *   bytes per CTA of the persistent grid of the launches (both launches run on
+ *   the same grid; (size_t)-1 where they would not, or for invalid arguments,
+ *   including num_q_heads / num_kv_heads > 16).
+ * pa_decode_shared_plan: plan (host int32) <- the schedule for HOST copies of
+ *   block_tables, context_lens and share (as pa_decode_shared reads them).  The
+ *   plan covers plan_bytes / 256 CTAs per launch.  Host only: no CUDA call, no
+ *   device work, no allocation.  Errors: PA_ERR_INVALID (null pointer, bad sizes,
+ *   plan_bytes not a positive multiple of 256).
+ * pa_decode_shared_planned: as pa_decode_shared, plus `plan`: a DEVICE copy of the
+ *   plan (16-byte aligned, plan_bytes = pa_decode_shared_plan_bytes for the same
+ *   arguments, made from the same lengths, tables and share entries).  A plan made
+ *   from other inputs gives wrong outputs but no access outside the arguments;
+ *   appended rows still go where the block table says, and only for a sequence
+ *   whose length the launch reads equals the plan's; a walk whose positions cannot
+ *   match raises PA_DEVERR_PLAN.  Errors: as pa_decode_shared; PA_ERR_INVALID also
+ *   for a null or misaligned plan or a plan_bytes that does not match.
+ */
+size_t pa_decode_shared_plan_bytes(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                                   int block_size, int max_blocks_per_seq, pa_dtype dtype);
+pa_status pa_decode_shared_plan(int32_t *plan, size_t plan_bytes, const int32_t *block_tables,
+                                int max_blocks_per_seq, const int32_t *context_lens,
+                                const int32_t *share, int num_seqs, int num_q_heads,
+                                int num_kv_heads, int head_dim, int block_size, pa_dtype dtype);
+pa_status pa_decode_shared_planned(void *out, const void *q, void *k_cache, void *v_cache,
+                                   const void *k_new, const void *v_new,
+                                   const int32_t *block_tables, int max_blocks_per_seq,
+                                   const int32_t *context_lens, const int32_t *share, int num_seqs,
+                                   int num_blocks, float scale, int num_q_heads, int num_kv_heads,
+                                   int head_dim, int block_size, pa_dtype dtype,
+                                   const int32_t *plan, size_t plan_bytes, void *workspace,
+                                   size_t workspace_bytes, void *stream);
+
+/*
  * Partition size pa_decode uses for these arguments: 0 for the balanced split,
  * else the fixed partition size (capped at the table capacity).  Returns -1 for
  * invalid arguments.
@@ -411,7 +461,7 @@ int pa_kv_transfer_worthwhile(long long reusable_tokens, long long threshold_tok
 #define PA_DEVERR_TIMEOUT_EMPTY 2u   /* producer waited too long for a free stage */
 #define PA_DEVERR_SHARE         4u   /* pa_decode_shared: a member's context ends
                                         inside its group's shared blocks          */
-#define PA_DEVERR_PLAN          8u   /* pa_decode_planned: the plan does not match
+#define PA_DEVERR_PLAN          8u   /* pa_decode_planned, pa_decode_shared_planned: the plan does not match
                                         the context lengths the launch read       */
 pa_status pa_device_errors(unsigned int *flags, void *stream);
 

@@ -289,6 +289,66 @@ def pa_decode_shared(out, q, k_cache, v_cache, block_tables, context_lens, share
     return out
 
 
+def pa_decode_shared_plan_bytes(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+                                max_blocks_per_seq, dtype) -> int:
+    """Size of a pa_decode_shared_plan for these arguments on the current device."""
+    n = _load().pa_decode_shared_plan_bytes(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+                                            max_blocks_per_seq, _dtype_arg(dtype))
+    if n == ctypes.c_size_t(-1).value:
+        raise PagedKVError(PA_ERR_INVALID, "pa_decode_shared_plan_bytes")
+    return n
+
+
+def pa_decode_shared_plan(block_tables, context_lens, share, num_q_heads: int, num_kv_heads: int,
+                          head_dim: int, block_size: int, dtype, plan_bytes: Optional[int] = None):
+    """Host-side schedule of both launches of the shared-prefix decode (see
+    pa_decode_shared_plan in include/pagedkv.h): int32 numpy array, from HOST block
+    tables [S, W], context lengths [S] and share entries [S, 2].  plan_bytes defaults
+    to pa_decode_shared_plan_bytes(...) on the current device."""
+    import numpy as np
+    bt = np.ascontiguousarray(np.asarray(block_tables, dtype=np.int32))
+    cl = np.ascontiguousarray(np.asarray(context_lens, dtype=np.int32))
+    sh = np.ascontiguousarray(np.asarray(share, dtype=np.int32))
+    S = cl.shape[0]
+    W = bt.shape[1] if bt.ndim == 2 else 1
+    if plan_bytes is None:
+        plan_bytes = pa_decode_shared_plan_bytes(S, num_q_heads, num_kv_heads, head_dim, block_size, W,
+                                                 dtype)
+    plan = np.empty(plan_bytes // 4, dtype=np.int32)
+    st = _load().pa_decode_shared_plan(plan.ctypes.data, plan_bytes, bt.ctypes.data if S else None, W,
+                                       cl.ctypes.data if S else None, sh.ctypes.data if S else None, S,
+                                       num_q_heads, num_kv_heads, head_dim, block_size, _dtype_arg(dtype))
+    _check(st, "pa_decode_shared_plan")
+    return plan
+
+
+def pa_decode_shared_planned(out, q, k_cache, v_cache, block_tables, context_lens, share, plan,
+                             scale: float, num_q_heads: int, num_kv_heads: int, head_dim: int,
+                             block_size: int, k_new=None, v_new=None, workspace=None, stream=None):
+    """pa_decode_shared whose CTAs, in both launches, start where `plan` (a CUDA int32
+    copy of pa_decode_shared_plan's output for the same inputs) says; bit-identical
+    to the unplanned call."""
+    import torch
+    S = q.shape[0]
+    W = block_tables.shape[1]
+    if workspace is None:
+        n = pa_decode_shared_workspace_size(S, num_q_heads, num_kv_heads, head_dim, block_size, W)
+        workspace = _launch_scratch(n, q.device, stream)
+    if (share.dtype != torch.int32 or block_tables.dtype != torch.int32 or
+            context_lens.dtype != torch.int32 or plan.dtype != torch.int32):
+        raise TypeError("share, block_tables, context_lens and plan must be int32")
+    st = _load().pa_decode_shared_planned(
+        _cuda(out, "out"), _cuda(q, "q"), _cuda(k_cache, "k_cache"), _cuda(v_cache, "v_cache"),
+        _cuda(k_new, "k_new") if k_new is not None else None,
+        _cuda(v_new, "v_new") if v_new is not None else None,
+        _cuda(block_tables, "block_tables"), W, _cuda(context_lens, "context_lens"), _cuda(share, "share"),
+        S, k_cache.shape[0], float(scale), num_q_heads, num_kv_heads, head_dim, block_size, _dtype_code(q),
+        _cuda(plan, "plan"), plan.numel() * 4, _cuda(workspace, "workspace"),
+        workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(st, "pa_decode_shared_planned")
+    return out
+
+
 def share_groups(block_tables, context_lens, block_size: int, min_shared_blocks: int = 1):
     """share int32 [S, 2] for pa_decode_shared, from host block tables [S, W] and
     context lengths [S] (numpy or CPU tensors); see pa_share_groups."""
@@ -605,6 +665,7 @@ def pa_kv_transfer_worthwhile(reusable_tokens: int, threshold_tokens: int = 64) 
 
 
 __all__ = ["pa_decode", "pa_decode_append", "pa_decode_plan_bytes", "pa_decode_plan", "pa_decode_planned",
+           "pa_decode_shared_plan_bytes", "pa_decode_shared_plan", "pa_decode_shared_planned",
            "PA_DEVERR_PLAN", "PLAN_BYTES_PER_CTA",
            "pa_decode_shared", "pa_decode_shared_workspace_size",
            "share_groups", "share_saving", "share_pays", "SHARE_MIN_SAVING", "SHARE_MIN_BYTES",

@@ -35,6 +35,13 @@ SIGNATURES = {
                                   c_int, c_void_p, c_int, c_int, c_float, c_int, c_int, c_int, c_int,
                                   c_int, c_void_p, c_size_t, c_void_p, c_size_t, c_void_p]),
     "pa_decode_shared_workspace_size": (c_size_t, [c_int] * 6),
+    "pa_decode_shared_plan_bytes": (c_size_t, [c_int] * 7),
+    "pa_decode_shared_plan": (c_int, [c_void_p, c_size_t, c_void_p, c_int, c_void_p, c_void_p, c_int, c_int,
+                                      c_int, c_int, c_int, c_int]),
+    "pa_decode_shared_planned": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
+                                         c_void_p, c_int, c_void_p, c_void_p, c_int, c_int, c_float, c_int,
+                                         c_int, c_int, c_int, c_int, c_void_p, c_size_t, c_void_p, c_size_t,
+                                         c_void_p]),
     "pa_share_groups": (c_int, [c_void_p, c_int, c_int, c_void_p, c_int, c_int, c_void_p]),
     "pa_decode_noalloc": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_void_p,
                                   c_int, c_int, c_float, c_int, c_int, c_int, c_int, c_int, c_int,

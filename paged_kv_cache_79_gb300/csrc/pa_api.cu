@@ -309,7 +309,8 @@ pa_status decode_impl(void *out, const void *q, const void *k_cache, const void 
                       int num_q_heads, int num_kv_heads, int head_dim, int block_size,
                       pa_dtype dtype, int partition_size, void *workspace, size_t workspace_bytes,
                       const void *k_new, const void *v_new, void *stream,
-                      const int32_t *share = nullptr, const int32_t *plan = nullptr)
+                      const int32_t *share = nullptr, const int32_t *plan = nullptr,
+                      int plan_grid = 0)
 {
     if (num_seqs == 0)
         return PA_OK;
@@ -384,6 +385,8 @@ pa_status decode_impl(void *out, const void *q, const void *k_cache, const void 
     if (!p.errors)
         return cuda_fail(ce);
     p.wait_ns = wait_limit_ns();
+    // a plan holds one entry per CTA of the grid it was made for (the shared-prefix
+    // decode's: pass 1's entries, then pass 0's); the launch must use that grid
     p.plan = (balanced && share == nullptr) ? plan : nullptr;
     p.scale_log2 = scale * 1.4426950408889634f;
     p.num_seqs = num_seqs;
@@ -403,7 +406,7 @@ pa_status decode_impl(void *out, const void *q, const void *k_cache, const void 
     L.head_dim = head_dim;
     L.block_size = block_size;
     L.sm_count = sms;
-    L.grid = 0;  // the occupancy-sized persistent grid
+    L.grid = plan ? plan_grid : 0;  // 0: the occupancy-sized persistent grid
     // one copy per block for K and V where the caches' placement allows it (the
     // joint map), else one per cache
     p.kv_joint = kv_joint_ok(k_cache, v_cache) &&
@@ -437,6 +440,7 @@ pa_status decode_impl(void *out, const void *q, const void *k_cache, const void 
         L1.p.pfx = pfx;
         L1.p.k_new = nullptr;
         L1.p.v_new = nullptr;
+        L1.p.plan = plan;
         cudaError_t e = launch(L1);
         if (e != cudaSuccess)
             return cuda_fail(e);
@@ -445,6 +449,7 @@ pa_status decode_impl(void *out, const void *q, const void *k_cache, const void 
         L.p.share = share;
         L.p.pfx = pfx;
         L.p.epoch = next_epoch();
+        L.p.plan = plan ? plan + (size_t)plan_grid * kPlanInts : nullptr;
     }
     cudaError_t e = launch(L);
     if (e != cudaSuccess)
@@ -637,7 +642,257 @@ pa_status pa_decode_planned(void *out, const void *q, void *k_cache, void *v_cac
         return PA_ERR_INVALID;
     return decode_impl(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
                        num_seqs, num_blocks, scale, num_q_heads, num_kv_heads, head_dim, block_size,
-                       dtype, 0, workspace, workspace_bytes, k_new, v_new, stream, nullptr, plan);
+                       dtype, 0, workspace, workspace_bytes, k_new, v_new, stream, nullptr, plan,
+                       (int)(plan_bytes / (kPlanInts * sizeof(int32_t))));
+}
+
+}  // extern "C"
+
+namespace {
+
+// One pass of the balanced split as the kernel's walk builds it: sequence s has
+// n[s] units of kUnitCost + ns[s] positions over blocks [first[s], nb[s]) of the
+// table row of sequence s; len[s] and aux[s] go to its plan entry.
+struct PassStream {
+    std::vector<int> n, ns, first, nb, len, aux;
+    bool unit_major = false;  // (unit, sequence) order: every n[s] is the same
+};
+
+// The plan entries of one pass for a grid of `grid` CTAs (see pa_decode_plan).
+void fill_pass_plan(int32_t *plan, int grid, const PassStream &ps, const int32_t *block_tables,
+                    int W, int bps)
+{
+    const int S = (int)ps.n.size();
+    auto put64 = [](int32_t *e, int f, long long v) {
+        e[f] = (int32_t)(uint32_t)(v & 0xffffffffll);
+        e[f + 1] = (int32_t)(v >> 32);
+    };
+    std::vector<long long> span((size_t)S), start((size_t)S + 1, 0), cum((size_t)S + 1, 0);
+    long long units = 0;
+    for (int s = 0; s < S; ++s) {
+        span[s] = kUnitCost + ps.ns[s];
+        start[s + 1] = start[s] + (long long)ps.n[s] * span[s];
+        cum[s + 1] = cum[s] + span[s];  // one unit of every sequence (unit-major rows)
+        units += ps.n[s];
+    }
+    const long long total = start[S];
+    const int div = balanced_divisor(total, units);
+    const long long G = S > 0 ? balanced_grid_of(total, div, grid) : 0;
+    const long long U = S > 0 ? ps.n[0] : 0;
+    const long long Wrow = ps.unit_major && U > 0 ? total / U : 0;
+    std::memset(plan, 0, (size_t)grid * kPlanInts * sizeof(int32_t));
+    for (int c = 0; c < grid; ++c) {
+        int32_t *e = plan + (size_t)c * kPlanInts;
+        e[kPlanSeq] = -1;
+        put64(e, kPlanTotal, total);
+        e[kPlanDiv] = div;
+        e[kPlanG] = (int32_t)G;
+        e[kPlanGrid] = grid;
+        e[kPlanSeqs] = S;
+        if (c >= G)
+            continue;
+        const long long s_c = c * total / G, e_c = (c + 1) * total / G;
+        int s;
+        long long base;
+        if (ps.unit_major) {
+            // unit u of every sequence is a row of Wrow positions
+            const long long u = s_c / Wrow, inner = s_c - u * Wrow;
+            s = (int)(std::upper_bound(cum.begin(), cum.end(), inner) - cum.begin()) - 1;
+            base = u * Wrow + cum[s];
+        } else {
+            s = (int)(std::upper_bound(start.begin(), start.end(), s_c) - start.begin()) - 1;
+            base = start[s];
+        }
+        if (s < 0 || s >= S)
+            continue;
+        e[kPlanSeq] = s;
+        put64(e, kPlanBase, base);
+        e[kPlanLen] = ps.len[s];
+        e[kPlanAux] = ps.aux[s];
+        put64(e, kPlanStart, s_c);
+        put64(e, kPlanEnd, e_c);
+        // the first item's first block, when it is in the unit holding s_c
+        const long long a =
+            ps.unit_major ? base : base + (s_c > base ? (s_c - base) / span[s] : 0) * span[s];
+        const long long ra = a + kUnitCost;
+        const long long into = std::max(ra, s_c) - ra;
+        const int j0 = ps.first[s] + (int)std::min<long long>(into * bps, ps.nb[s] - ps.first[s]);
+        e[kPlanJ0] = j0;
+        for (int k = 0; k < kPlanWindow; ++k) {
+            const int j = j0 + k;
+            e[kPlanBlocks + k] = j < W ? block_tables[(size_t)s * W + j] : -1;
+        }
+    }
+}
+
+// Persistent grid of one shared-prefix launch (pass 1 or 0) on the current device,
+// planned (0: cannot launch or no device).
+int plan_grid_shared(pa_dtype dtype, int num_q_heads, int num_kv_heads, int head_dim,
+                     int block_size, int pass)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    const int sms = sm_count(dev);
+    if (sms <= 0)
+        return 0;
+    static const int32_t kSelect = 0;  // any non-null share / plan selects the instance
+    DecodeLaunch L;
+    std::memset(&L, 0, sizeof L);
+    L.p.plan = &kSelect;
+    L.p.share = &kSelect;
+    L.p.pass = pass;
+    L.p.balanced = 1;
+    L.p.num_q_heads = num_q_heads;
+    L.p.num_kv_heads = num_kv_heads;
+    L.p.group = num_q_heads / num_kv_heads;
+    L.p.head_groups = (L.p.group + kHeadsPerItem - 1) / kHeadsPerItem;
+    L.head_dim = head_dim;
+    L.block_size = block_size;
+    L.sm_count = sms;
+    L.grid = 0;
+    return dtype == PA_F32 ? plan_grid_f32(L) : dtype == PA_F16 ? plan_grid_f16(L) : plan_grid_bf16(L);
+}
+
+bool shared_plan_args_ok(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                         int block_size, int max_blocks_per_seq, int dtype)
+{
+    return plan_args_ok(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+                        max_blocks_per_seq, dtype) &&
+           num_q_heads / num_kv_heads <= kHeadsPerItem;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t pa_decode_shared_plan_bytes(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                                   int block_size, int max_blocks_per_seq, pa_dtype dtype)
+{
+    if (!shared_plan_args_ok(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+                             max_blocks_per_seq, dtype))
+        return (size_t)-1;
+    const int g1 = plan_grid_shared(dtype, num_q_heads, num_kv_heads, head_dim, block_size, 1);
+    const int g0 = plan_grid_shared(dtype, num_q_heads, num_kv_heads, head_dim, block_size, 0);
+    if (g1 <= 0 || g1 != g0)
+        return (size_t)-1;
+    return 2 * (size_t)g1 * kPlanInts * sizeof(int32_t);
+}
+
+pa_status pa_decode_shared_plan(int32_t *plan, size_t plan_bytes, const int32_t *block_tables,
+                                int max_blocks_per_seq, const int32_t *context_lens,
+                                const int32_t *share, int num_seqs, int num_q_heads,
+                                int num_kv_heads, int head_dim, int block_size, pa_dtype dtype)
+{
+    if (!plan || (num_seqs > 0 && (!block_tables || !context_lens || !share)))
+        return PA_ERR_INVALID;
+    if (!shared_plan_args_ok(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+                             max_blocks_per_seq, dtype))
+        return PA_ERR_INVALID;
+    // both launches' entries for the same persistent grid: the plan's size gives it
+    const size_t entry = (size_t)kPlanInts * sizeof(int32_t);
+    if (plan_bytes == 0 || plan_bytes % (2 * entry) != 0 || plan_bytes / (2 * entry) > (1u << 20))
+        return PA_ERR_INVALID;
+    const int grid = (int)(plan_bytes / (2 * entry));
+    const int S = num_seqs, W = max_blocks_per_seq, B = block_size;
+    const int group = num_q_heads / num_kv_heads;
+    const int U = num_kv_heads * ((group + kHeadsPerItem - 1) / kHeadsPerItem);
+    const int bps = blocks_per_stage(dtype == PA_F32 ? 4 : 2, B);
+    const int mpi = (group <= 8 ? 8 : kHeadsPerItem) / group;  // members per pass-1 item
+    // each sequence's entries as the kernel reads them (seq_units)
+    std::vector<int> len((size_t)S), lead((size_t)S), shared((size_t)S);
+    for (int s = 0; s < S; ++s) {
+        const long long t = context_lens[s];
+        len[s] = (int)std::min<long long>(std::max<long long>(t, 0), (long long)W * B);
+        lead[s] = share[2 * s];
+        const int sp = share[2 * s + 1];
+        shared[s] = (lead[s] >= 0 && sp > 0) ? std::min(sp, W) : 0;
+    }
+    PassStream p1, p0;
+    for (PassStream *ps : {&p1, &p0}) {
+        ps->n.assign((size_t)S, 0);
+        ps->ns.assign((size_t)S, 0);
+        ps->first.assign((size_t)S, 0);
+        ps->nb.assign((size_t)S, 0);
+        ps->len.assign((size_t)S, 0);
+        ps->aux.assign((size_t)S, 0);
+    }
+    // pass 1: a group's first member streams its shared blocks once per kv head
+    // and member group of up to mpi members
+    for (int s = 0; s < S; ++s) {
+        if (lead[s] != s || shared[s] <= 0)
+            continue;
+        int m = 1;
+        while (s + m < S && lead[s + m] == s)
+            ++m;
+        p1.n[s] = num_kv_heads * ((m + mpi - 1) / mpi);
+        p1.ns[s] = (shared[s] + bps - 1) / bps;
+        p1.nb[s] = shared[s];
+        p1.len[s] = shared[s];  // pass 1: the group's shared blocks
+        p1.aux[s] = m;
+    }
+    // pass 0: every sequence's own blocks, after its group's shared ones
+    bool prefix = false;
+    for (int s = 0; s < S; ++s) {
+        const int nb = (len[s] + B - 1) / B;
+        int P = std::min(shared[s], nb);
+        int flags = 0;
+        if (P > 0 && len[s] <= shared[s] * B) {
+            P = 0;  // ends inside the shared blocks: decoded alone, flagged
+            flags |= kAuxShareErr;
+        }
+        p0.n[s] = U;
+        p0.ns[s] = (nb - P + bps - 1) / bps;
+        p0.first[s] = P;
+        p0.nb[s] = nb;
+        p0.len[s] = len[s];
+        p0.aux[s] = P | flags;
+        prefix |= P > 0;
+    }
+    p0.unit_major = prefix;
+    if (prefix)
+        for (int s = 0; s < S; ++s)
+            p0.aux[s] |= kAuxUnitMajor;
+    fill_pass_plan(plan, grid, p1, block_tables, W, bps);
+    fill_pass_plan(plan + (size_t)grid * kPlanInts, grid, p0, block_tables, W, bps);
+    return PA_OK;
+}
+
+pa_status pa_decode_shared_planned(void *out, const void *q, void *k_cache, void *v_cache,
+                                   const void *k_new, const void *v_new,
+                                   const int32_t *block_tables, int max_blocks_per_seq,
+                                   const int32_t *context_lens, const int32_t *share, int num_seqs,
+                                   int num_blocks, float scale, int num_q_heads, int num_kv_heads,
+                                   int head_dim, int block_size, pa_dtype dtype,
+                                   const int32_t *plan, size_t plan_bytes, void *workspace,
+                                   size_t workspace_bytes, void *stream)
+{
+    if (num_seqs == 0)
+        return PA_OK;
+    if (!plan || !aligned(plan, 16))
+        return PA_ERR_INVALID;
+    const size_t need = pa_decode_shared_plan_bytes(num_seqs, num_q_heads, num_kv_heads, head_dim,
+                                                    block_size, max_blocks_per_seq, dtype);
+    if (need == (size_t)-1) {
+        const bool unsupported =
+            !dtype_ok(dtype) || (head_dim != 64 && head_dim != 128) ||
+            (block_size != 16 && block_size != 32) ||
+            (num_kv_heads > 0 && num_q_heads / num_kv_heads > kHeadsPerItem);
+        return unsupported ? PA_ERR_UNSUPPORTED : PA_ERR_INVALID;
+    }
+    if (plan_bytes != need)
+        return PA_ERR_INVALID;
+    if (!share || !aligned(share, 8))
+        return PA_ERR_INVALID;
+    if ((k_new == nullptr) != (v_new == nullptr) ||
+        (k_new && (!aligned(k_new, 16) || !aligned(v_new, 16))))
+        return PA_ERR_INVALID;
+    return decode_impl(out, q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
+                       num_seqs, num_blocks, scale, num_q_heads, num_kv_heads, head_dim, block_size,
+                       dtype, 0, workspace, workspace_bytes, k_new, v_new, stream, share, plan,
+                       (int)(plan_bytes / (2 * kPlanInts * sizeof(int32_t))));
 }
 
 size_t pa_decode_shared_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads,

@@ -118,6 +118,12 @@ constexpr bool kTraceLite = true;
 #else
 constexpr bool kTraceLite = false;
 #endif
+// Per-stage and per-item stamps: the stamps-only build reads no timer for them (a
+// %globaltimer read per stage slowed the decode by a fifth).
+__device__ __forceinline__ unsigned long long trace_clock()
+{
+    return kTraceLite ? 0ull : dev::global_timer_ns();
+}
 __device__ __forceinline__ void trace_set(int pass, int slot, unsigned long long v)
 {
     const int r = trace_row(pass);
@@ -633,7 +639,7 @@ struct Producer {
 #ifdef PA_TRACE
             if (!t_last_issue)
                 PA_TRACE_SET(14, dev::global_timer_ns());  // first tile issued
-            t_last_issue = dev::global_timer_ns();
+            t_last_issue = kTraceLite ? 1ull : dev::global_timer_ns();
             PA_TRACE_ADD(7, 1);
 #endif
         }
@@ -1025,20 +1031,22 @@ __device__ __forceinline__ bool walk_chunk_unit_major(const DecodeParams &p, int
     return !*pr.c.abort;
 }
 
-// pa_decode_planned: the walk of the plain balanced split from the CTA's start as
-// the host computed it (pa_decode_plan).  The stream total, the CTA's range, its
-// first sequence with that sequence's first position and length, and the block ids
-// of its first item's first window come from the plan, so the first copies need
-// no pass over the context lengths and no block-table read.  Later sequences'
-// lengths are read as the walk reaches them.  The items are the ones the walk from
-// scratch emits.  A plan made for other lengths gives wrong rows but never an
-// access outside the arguments: every field is bounded before use, the CTA count
-// is recomputed from the total as the merge recomputes it, and a walk whose
-// positions would pass the total stops and raises PA_DEVERR_PLAN.
-template <class Prod>
+// pa_decode_planned / pa_decode_shared_planned: the walk of the balanced split
+// from the CTA's start as the host computed it (pa_decode_plan,
+// pa_decode_shared_plan).  The stream total, the CTA's range, its first sequence
+// with that sequence's first position and units, and the block ids of its first
+// item's first window come from the plan, so the first copies need no pass over
+// the context lengths (or the shared-prefix entries) and no block-table read.
+// Later sequences' entries are read as the walk reaches them.  The items are the
+// ones the walk from scratch emits.  A plan made for other inputs gives wrong rows
+// but never an access outside the arguments: every field is bounded before use,
+// the CTA count is recomputed from the total as the merge recomputes it, and a
+// walk whose positions would pass the total stops and raises PA_DEVERR_PLAN.
+template <int kMode, class Prod>
 __device__ __forceinline__ void walk_planned(const DecodeParams &p, int bs, int bps, Prod &pr,
                                              int lane)
 {
+    constexpr bool kShare = kMode == kModePrefix || kMode == kModeOwn;
     const int v = p.plan[(size_t)blockIdx.x * kPlanInts + lane];
     auto get = [&](int f) { return __shfl_sync(0xffffffffu, v, f); };
     auto get64 = [&](int f) {
@@ -1053,14 +1061,63 @@ __device__ __forceinline__ void walk_planned(const DecodeParams &p, int bs, int 
     const long long e_c = min(max(get64(kPlanEnd), 0ll), total);
     const long long s_c = min(max(get64(kPlanStart), 0ll), e_c);
     long long base = min(max(get64(kPlanBase), 0ll), s_c);
-    const int len0 = min(max(get(kPlanLen), 0), p.max_blocks * bs);
+    const int aux = kShare ? get(kPlanAux) : 0;
     pr.plan_blk = v;
     pr.plan_seq = seq;
     pr.plan_j0 = get(kPlanJ0);
+    // the first sequence's units
+    SeqUnits su0;
+    if constexpr (kMode == kModePrefix) {
+        // the group's shared blocks, streamed with the rows of its members
+        const int members = min(max(aux & kAuxValueMask, 1), p.num_seqs - seq);
+        const int shared = min(max(get(kPlanLen), 0), p.max_blocks);
+        const int mpi = members_per_item(p.group);
+        su0.members = members;
+        su0.mgroups = (members + mpi - 1) / mpi;
+        su0.nunits = p.num_kv_heads * su0.mgroups;
+        su0.ns = (shared + bps - 1) / bps;
+        su0.start = 0;
+        su0.nb = shared;
+        su0.len = shared * bs;
+    } else {
+        su0 = seq_units_of_len(p, min(max(get(kPlanLen), 0), p.max_blocks * bs), bs, bps);
+        if (kMode == kModeOwn) {
+            // its own blocks, after the group's shared ones
+            su0.start = min(aux & kAuxValueMask, su0.nb);
+            su0.ns = (su0.nb - su0.start + bps - 1) / bps;
+            if ((aux & kAuxShareErr) && lane == 0)
+                atomicOr(p.errors, PA_DEVERR_SHARE);
+        }
+    }
     const long long cta = blockIdx.x;
+    if (kMode == kModeOwn && (aux & kAuxUnitMajor)) {
+        // (unit, sequence) order, as walk_chunk_unit_major
+        const long long U = (long long)p.num_kv_heads * p.head_groups;
+        const long long W = total / U;
+        if (W <= 0)
+            return;
+        bool first = true;
+        int s = seq;
+        for (long long u = s_c / W; u < U && base < e_c && !*pr.c.abort; ++u, s = 0) {
+            for (; s < p.num_seqs && base < e_c; ++s) {
+                const SeqUnits su = first ? su0 : seq_units<true>(p, s, bs, bps);
+                first = false;
+                if (base + kUnitCost + su.ns > total) {
+                    if (lane == 0)
+                        atomicOr(p.errors, PA_DEVERR_PLAN);
+                    return;
+                }
+                if (!emit_unit<true>(p, pr, su, s, u, base, s_c, e_c, total, G, cta, bps, div))
+                    return;
+                base += kUnitCost + su.ns;
+            }
+        }
+        return;
+    }
     for (int s = seq; s < p.num_seqs && base < e_c && !*pr.c.abort; ++s) {
-        const SeqUnits su =
-            s == seq ? seq_units_of_len(p, len0, bs, bps) : seq_units<false>(p, s, bs, bps);
+        const SeqUnits su = s == seq ? su0 : seq_units<kShare>(p, s, bs, bps);
+        if (kShare && su.nunits == 0)
+            continue;
         const long long span = kUnitCost + su.ns;
         if (base + (long long)su.nunits * span > total) {
             if (lane == 0)
@@ -1070,8 +1127,8 @@ __device__ __forceinline__ void walk_planned(const DecodeParams &p, int bs, int 
         const long long u_lo = s_c > base ? (s_c - base) / span : 0;
         const long long u_hi = min((long long)su.nunits - 1, (e_c - 1 - base) / span);
         for (long long u = u_lo; u <= u_hi; ++u)
-            if (!emit_unit<false>(p, pr, su, s, u, base + u * span, s_c, e_c, total, G, cta, bps,
-                                  div))
+            if (!emit_unit<kShare>(p, pr, su, s, u, base + u * span, s_c, e_c, total, G, cta, bps,
+                                   div))
                 return;
         base += (long long)su.nunits * span;
     }
@@ -1118,8 +1175,11 @@ __device__ __forceinline__ void producer_loop(const DecodeParams &p, const CUten
                                               const CUtensorMap *tv, const CtaState &c, int lane)
 {
     Producer<T, D, BS, kBPS, kChunks, kTileBytes, kStages, kCopy> pr(p, tk, tv, c, lane);
+    constexpr bool kShare = kMode == kModePrefix || kMode == kModeOwn;
     if constexpr (kMode == kModePlan)
-        walk_planned(p, BS, kBPS, pr, lane);
+        walk_planned<kModePlan>(p, BS, kBPS, pr, lane);
+    else if (kShare && p.plan != nullptr)
+        walk_planned<kMode>(p, BS, kBPS, pr, lane);
     else if (p.balanced)
         walk_balanced<kMode>(p, BS, kBPS, pr, lane);
     else
@@ -1570,14 +1630,14 @@ __device__ __forceinline__ bool consume_item_n8(const DecodeParams &p, const Cta
             continue;
         const uint32_t st = g % C::kStages;
 #ifdef PA_TRACE
-        const unsigned long long t_sw = dev::global_timer_ns();
+        const unsigned long long t_sw = trace_clock();
 #endif
         if (!warp_wait(p, c, &c.full[st], (g / C::kStages) & 1u)) {
             return false;
         }
 #ifdef PA_TRACE
         if (threadIdx.x == 0) {
-            const unsigned long long t_now = dev::global_timer_ns();
+            const unsigned long long t_now = trace_clock();
             PA_TRACE_ADD(13, t_now - t_sw);
             PA_TRACE_SET(11, t_now);
             if (trace_first_tile(p.pass)) {
@@ -1797,22 +1857,22 @@ __global__ void __launch_bounds__(kThreads, 2)
     for (uint32_t n = 0;; ++n) {
         const uint32_t slot = n % kItemSlots;
 #ifdef PA_TRACE
-        const unsigned long long t_iw = dev::global_timer_ns();
+        const unsigned long long t_iw = trace_clock();
 #endif
         if (!warp_wait(p, c, &c.item_full[slot], (n / kItemSlots) & 1u)) {
             break;
         }
 #ifdef PA_TRACE
         if (threadIdx.x == 0)
-            PA_TRACE_ADD(12, dev::global_timer_ns() - t_iw);
+            PA_TRACE_ADD(12, trace_clock() - t_iw);
 #endif
         const Item it = load_item(&c.items[slot]);
         if (it.seq < 0)
             break;
         // a planned first item takes its length from the plan: its append is stored
         // only if that is the length the launch reads (read here, used stages later)
-        const bool append_ok =
-            kMode != kModePlan || p.k_new == nullptr || clamp_len(p, it.tseq, BS) == it.len;
+        const bool append_ok = (kMode != kModePlan && (kMode != kModeOwn || p.plan == nullptr)) ||
+                               p.k_new == nullptr || clamp_len(p, it.tseq, BS) == it.len;
         const bool merge_pfx = kShare && (it.flags() & kMergePrefix) != 0;
         float *pfx_s = c.pfx + (n & 1) * pfx_rows * (D + kPfxPad);
         if (merge_pfx && pfx_ready)
@@ -1868,7 +1928,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                 continue;
             const uint32_t st = g % C::kStages;
 #ifdef PA_TRACE
-            const unsigned long long t_sw = dev::global_timer_ns();
+            const unsigned long long t_sw = trace_clock();
 #endif
             if (!warp_wait(p, c, &c.full[st], (g / C::kStages) & 1u)) {
                 alive = false;
@@ -1876,7 +1936,7 @@ __global__ void __launch_bounds__(kThreads, 2)
             }
 #ifdef PA_TRACE
             if (threadIdx.x == 0) {
-                const unsigned long long t_now = dev::global_timer_ns();
+                const unsigned long long t_now = trace_clock();
                 PA_TRACE_ADD(13, t_now - t_sw);
                 PA_TRACE_SET(11, t_now);
                 if (first_tile) {
@@ -2024,7 +2084,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
         }
 #ifdef PA_TRACE
-        const unsigned long long t_m0 = dev::global_timer_ns();
+        const unsigned long long t_m0 = trace_clock();
 #endif
         if (merge_pfx) {
             if (!pfx_ready) {  // first prefix row of this CTA: wait for pass 1 once
@@ -2045,7 +2105,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
 #ifdef PA_TRACE
         if (threadIdx.x == 0) {
-            PA_TRACE_ADD(9, dev::global_timer_ns() - t_m0);
+            PA_TRACE_ADD(9, trace_clock() - t_m0);
             if (p.balanced && it.partial && *c.merge)
                 PA_TRACE_ADD(10, 1);
         }
@@ -2125,8 +2185,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
         // a planned first item takes its length from the plan: its append is stored
         // only if that is the length the launch reads (read here, used stages later)
-        const bool append_ok =
-            kMode != kModePlan || p.k_new == nullptr || clamp_len(p, it.tseq, BS) == it.len;
+        const bool append_ok = (kMode != kModePlan && (kMode != kModeOwn || p.plan == nullptr)) ||
+                               p.k_new == nullptr || clamp_len(p, it.tseq, BS) == it.len;
         const bool merge_pfx = kShare && (it.flags() & kMergePrefix) != 0;
         float *pfx_s = c.pfx + (n & 1) * pfx_rows * (D + kPfxPad);
         if (merge_pfx && pfx_ready)
@@ -2150,7 +2210,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 continue;
             const uint32_t st = g % C::kStages;
 #ifdef PA_TRACE
-            const unsigned long long t_sw = dev::global_timer_ns();
+            const unsigned long long t_sw = trace_clock();
 #endif
             if (!warp_wait(p, c, &c.full[st], (g / C::kStages) & 1u)) {
                 alive = false;
@@ -2158,7 +2218,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
 #ifdef PA_TRACE
             if (threadIdx.x == 0) {
-                const unsigned long long t_now = dev::global_timer_ns();
+                const unsigned long long t_now = trace_clock();
                 PA_TRACE_ADD(13, t_now - t_sw);
                 PA_TRACE_SET(11, t_now);
                 if (trace_first_tile(p.pass))
@@ -2290,7 +2350,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             dev::cp_async_wait_all();
         }
 #ifdef PA_TRACE
-        const unsigned long long t_m0 = dev::global_timer_ns();
+        const unsigned long long t_m0 = trace_clock();
         if (threadIdx.x == 0)
             PA_TRACE_SET(12, t_m0);  // warp 0 done with the item's stages
 #endif
@@ -2301,7 +2361,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
 #ifdef PA_TRACE
         if (threadIdx.x == 0)
-            PA_TRACE_SET(10, dev::global_timer_ns());  // all warps done
+            PA_TRACE_SET(10, trace_clock());  // all warps done
 #endif
         finalize_item<float, D, kShare>(p, it, c.macc, c.mml, rows_cap, threadIdx.x, pfx_s,
                                 *c.merge == 2);
@@ -2310,7 +2370,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
 #ifdef PA_TRACE
         if (threadIdx.x == 0)
-            PA_TRACE_ADD(9, dev::global_timer_ns() - t_m0);
+            PA_TRACE_ADD(9, trace_clock() - t_m0);
 #endif
         if (*c.abort)
             break;
@@ -2392,14 +2452,12 @@ __global__ void __launch_bounds__(128)
 // Launch helpers
 // ---------------------------------------------------------------------------
 // The kernel instance a launch takes: plain decode (walked or planned), or one of
-// the shared-prefix decode's two launches.
+// the shared-prefix decode's two launches (walked or planned alike).
 inline int launch_mode(const DecodeParams &p)
 {
-    if (p.plan != nullptr)
-        return kModePlan;
-    if (p.share == nullptr)
-        return kModePlain;
-    return p.pass == 1 ? kModePrefix : kModeOwn;
+    if (p.share != nullptr)
+        return p.pass == 1 ? kModePrefix : kModeOwn;
+    return p.plan != nullptr ? kModePlan : kModePlain;
 }
 
 // Items of at most 8 query rows (group <= 8) take the transposed-product
@@ -2510,6 +2568,9 @@ cudaError_t launch_decode_impl(const DecodeLaunch &L, cudaStream_t stream)
     }
     if (grid < 1)
         grid = 1;
+    // a planned launch runs on exactly the grid its plan has an entry per CTA of
+    if (p.plan != nullptr && grid != L.grid)
+        return cudaErrorInvalidConfiguration;
     void *args[] = {const_cast<DecodeParams *>(&L.p), const_cast<CUtensorMap *>(&L.tmap_k),
                     const_cast<CUtensorMap *>(&L.tmap_v)};
     // Both kernels are programmatic dependents of whatever precedes them in the

@@ -126,9 +126,16 @@ enum PlanField {
     kPlanEnd = 11,
     kPlanJ0 = 13,       // first block of the CTA's first item
     kPlanSeqs = 14,     // batch size the plan was made for
+    kPlanAux = 15,      // shared-prefix passes: see kAux* below
     kPlanBlocks = 16,   // block ids j0 .. j0 + 15 of the first item's sequence (-1 past it)
 };
 constexpr int kPlanWindow = kPlanInts - kPlanBlocks;
+// kPlanAux of a shared-prefix pass's plan: the first sequence's units beyond its
+// length -- pass 1: the members of its group; pass 0: the first block of its own
+// units -- in the low bits, and two flags.
+constexpr int kAuxValueMask = (1 << 29) - 1;
+constexpr int kAuxUnitMajor = 1 << 29;  // pass 0 streams in (unit, sequence) order
+constexpr int kAuxShareErr = 1 << 30;   // the first sequence ends inside its shared blocks
 
 struct DecodeLaunch {
     DecodeParams p;

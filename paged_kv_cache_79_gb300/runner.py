@@ -13,9 +13,10 @@ from typing import Callable, List, Optional
 
 import numpy as np
 
-from . import (BlockAllocator, alloc_workspace, pa_copy_blocks, pa_decode, pa_decode_append,
-               pa_decode_plan, pa_decode_planned, pa_decode_shared, pa_decode_shared_workspace_size,
-               pa_reshape_and_cache, share_groups, share_pays)
+from . import (BlockAllocator, PagedKVError, alloc_workspace, pa_copy_blocks, pa_decode, pa_decode_append,
+               pa_decode_plan, pa_decode_planned, pa_decode_shared, pa_decode_shared_plan,
+               pa_decode_shared_planned, pa_decode_shared_workspace_size, pa_reshape_and_cache,
+               share_groups, share_pays)
 
 
 def _kind(ev) -> str:
@@ -57,6 +58,7 @@ class DecodeStep:
     share: "object" = None      # int32 [S, 2] shared-prefix groups, None if none share
     share_pays: bool = False    # the groups save enough reads for pa_decode_shared (share_pays)
     plan: "object" = None       # int32 device copy of pa_decode_plan for these tables and lengths
+    shared_plan: "object" = None  # int32 device copy of pa_decode_shared_plan (with share)
 
     def run_planned(self, stream=None):
         """copy-on-write pairs, then the balanced-split decode with its CTAs starting
@@ -73,22 +75,27 @@ class DecodeStep:
                                  v_new=self.step_v if self.fusable else None,
                                  workspace=self.workspace, stream=stream)
 
-    def run_shared(self, stream=None):
+    def run_shared(self, stream=None, planned=True):
         """copy-on-write pairs, then the shared-prefix decode (which also appends the new
-        tokens when the step is fusable)."""
+        tokens when the step is fusable), its CTAs starting from the host plan when
+        there is one."""
         if self.pairs.shape[0]:
             pa_copy_blocks(self.k_cache, self.v_cache, self.pairs, stream)
         if not self.fusable:
             pa_reshape_and_cache(self.step_k, self.step_v, self.k_cache, self.v_cache, self.slots, stream)
-        return self.decode_shared(stream, append=self.fusable)
+        return self.decode_shared(stream, append=self.fusable, planned=planned)
 
-    def decode_shared(self, stream=None, append=False):
+    def decode_shared(self, stream=None, append=False, planned=True):
+        kw = dict(k_new=self.step_k if append else None, v_new=self.step_v if append else None,
+                  workspace=self.workspace, stream=stream)
+        if planned and self.shared_plan is not None:
+            return pa_decode_shared_planned(self.out, self.q, self.k_cache, self.v_cache,
+                                            self.block_tables, self.context_lens, self.share,
+                                            self.shared_plan, self.scale, self.num_q_heads,
+                                            self.num_kv_heads, self.head_dim, self.block_size, **kw)
         return pa_decode_shared(self.out, self.q, self.k_cache, self.v_cache, self.block_tables,
                                 self.context_lens, self.share, self.scale, self.num_q_heads,
-                                self.num_kv_heads, self.head_dim, self.block_size,
-                                k_new=self.step_k if append else None,
-                                v_new=self.step_v if append else None,
-                                workspace=self.workspace, stream=stream)
+                                self.num_kv_heads, self.head_dim, self.block_size, **kw)
 
     def run(self, stream=None):
         """copy-on-write pairs, then the new tokens' K/V, then decode."""
@@ -144,6 +151,18 @@ class PackedInputs:
     @property
     def nbytes(self) -> int:
         return sum(t.numel() * t.element_size() for t in self.host.values())
+
+
+def _shared_plan(bt, cl, share, w, dtype, dev):
+    """Device copy of pa_decode_shared_plan for the step, or None where the two
+    launches have no common grid (some fp32 shapes): they then walk from scratch."""
+    import torch
+    try:
+        plan = pa_decode_shared_plan(bt, cl, share, w.num_q_heads, w.num_kv_heads, w.head_dim,
+                                     w.block_size, dtype)
+    except PagedKVError:
+        return None
+    return torch.from_numpy(plan).to(dev)
 
 
 def execute(w, k_cache, v_cache, step_kv: Callable, query: Callable,
@@ -207,6 +226,7 @@ def execute(w, k_cache, v_cache, step_kv: Callable, query: Callable,
                 head_dim=w.head_dim, block_size=w.block_size, partition_size=w.partition_size,
                 fusable=fusable,
                 share=torch.from_numpy(share).to(dev) if has_share else None,
+                shared_plan=_shared_plan(bt, cl, share, w, k_cache.dtype, dev) if has_share else None,
                 plan=torch.from_numpy(pa_decode_plan(bt, cl, w.num_q_heads, w.num_kv_heads, w.head_dim,
                                                      w.block_size, k_cache.dtype)).to(dev),
                 share_pays=has_share and share_pays(

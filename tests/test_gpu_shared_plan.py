@@ -176,3 +176,22 @@ def test_plan_of_another_size_is_rejected():
     with pytest.raises(P.PagedKVError):
         P.pa_decode_shared_planned(out, q.to(DEV), kc.to(DEV), vc.to(DEV), bt.to(DEV), cl.to(DEV),
                                    torch.from_numpy(share).to(DEV), plan[:-32], 0.1, 8, 8, 128, 16)
+
+
+def test_planned_without_groups_equals_plain_decode_bitwise():
+    """No group shares a block: the shared blocks' launch has an empty stream and the
+    own blocks' launch walks in (sequence, unit) order from its plan."""
+    groups = [([300], 0), ([17], 0), ([1000], 0), ([1], 0)]
+    q, kc, vc, bt, cl, share = shared_case(5, "bf16", 128, 16, 32, 8, groups)
+    plan = P.pa_decode_shared_plan(bt.numpy(), cl.numpy(), share, 32, 8, 128, 16, "bf16")
+    assert (plan.reshape(2, -1, 32)[0, :, 0] == -1).all()
+    got = torch.empty(q.shape, dtype=q.dtype, device=DEV)
+    P.pa_decode_shared_planned(got, q.to(DEV), kc.to(DEV), vc.to(DEV), bt.to(DEV), cl.to(DEV),
+                               torch.from_numpy(share).to(DEV), torch.from_numpy(plan).to(DEV), 0.09,
+                               32, 8, 128, 16)
+    out = torch.empty_like(got)
+    P.pa_decode(out, q.to(DEV), kc.to(DEV), vc.to(DEV), bt.to(DEV), cl.to(DEV), 0.09, 32, 8, 128, 16,
+                partition_size=0)
+    torch.cuda.synchronize()
+    assert torch.equal(got, out)
+    assert P.pa_device_errors() == 0

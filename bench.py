@@ -523,7 +523,9 @@ def run_ours(args):
         "bytes_per_step": by,
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_kind": f"{peak_kind} copy bandwidth",
-                     "traffic": profiled_traffic(w.name, 2 if shared else 1),
+                     # the profiled bytes are those of the workload at its own sizes
+                     "traffic": (profiled_traffic(w.name, 2 if shared else 1)
+                                 if not workload_kw(args) else None),
                      "kernel": (("pa_decode_shared_planned" if shared_planned else "pa_decode_shared") +
                                 " (partition kernel twice: shared prefixes, then own "
                                 "blocks" + (" + append" if fused else "") + ", merges inside)" if shared
